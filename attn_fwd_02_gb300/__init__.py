@@ -1,0 +1,17 @@
+"""GB300 (sm_103a) exact attention forward: FlashAttention-style prefill and paged-KV decode.
+
+The compute path is the CUDA shared library built from ``csrc/`` (C-ABI declared in
+``include/attn_gb300.h``).  ``binding`` marshals torch tensors into that ABI; it has no
+fallback: if the library is missing, every call raises.
+"""
+from .binding import (  # noqa: F401
+    AttnError,
+    attn_check_device_status,
+    attn_fwd,
+    attn_fwd_kvlen,
+    attn_status_string,
+    library_path,
+    load_library,
+    paged_attn_decode,
+    paged_attn_decode_workspace_size,
+)

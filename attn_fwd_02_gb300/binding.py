@@ -1,0 +1,196 @@
+"""ctypes binding of the C ABI declared in include/attn_gb300.h.
+
+Argument marshalling only: shapes are read off the torch tensors, pointers and
+the current CUDA stream are handed to the library, and a non-zero status
+raises ``AttnError``.  Every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the shared library has not been built
+(``__graft_entry__.build()`` or ``python -m attn_fwd_02_gb300.build``), every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libattn_gb300.so"
+_lib = None
+_lock = threading.Lock()
+
+ATTN_OK = 0
+_STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
+    4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT",
+}
+
+# name -> (restype, argtypes); mirrors include/attn_gb300.h
+P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "attn_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P]),
+    "attn_fwd_kvlen": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P]),
+    "paged_attn_decode_workspace_size": (Z, [I, I, I, I, I]),
+    "paged_attn_decode": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P, Z, P]),
+    "attn_check_device_status": (I, [P]),
+    "attn_status_string": (ctypes.c_char_p, [I]),
+    "attn_version": (ctypes.c_char_p, []),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {_STATUS_NAMES.get(status, status)} ({text})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, LIB_NAME)
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{LIB_NAME} is not built; run `python -m attn_fwd_02_gb300.build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnError(fn, status, attn_status_string(status))
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _require(t, name, dtype, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd_kvlen(q, k, v, causal: bool, scale: float | None = None, kv_lens=None,
+                   out=None, lse=None, return_lse: bool = True, stream=None):
+    """Prefill attention. q [B,H,Nq,d], k/v [B,H,Nkv,d] bf16 CUDA tensors;
+    kv_lens optional int32 [B] CUDA tensor.  Returns (o, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16, 4)
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
+        raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    if kv_lens is not None:
+        _require(kv_lens, "kv_lens", torch.int32, 1)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    st = lib.attn_fwd_kvlen(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, H, Nq, Nkv, d,
+                            int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
+    _check("attn_fwd_kvlen", st)
+    return out, lse
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None,
+             return_lse: bool = True, stream=None):
+    """Prefill attention without key padding (calls the C entry point attn_fwd)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16, 4)
+    B, H, Nq, d = q.shape
+    Nkv = k.shape[2]
+    if tuple(k.shape) != (B, H, Nkv, d) or tuple(v.shape) != (B, H, Nkv, d):
+        raise ValueError("k and v must be [B, H, Nkv, d] matching q")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    st = lib.attn_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, H, Nq, Nkv, d,
+                      int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check("attn_fwd", st)
+    return out, lse
+
+
+def paged_attn_decode_workspace_size(B: int, H: int, d: int, max_pages_per_seq: int,
+                                     page_size: int = 16) -> int:
+    return int(load_library().paged_attn_decode_workspace_size(B, H, d, max_pages_per_seq, page_size))
+
+
+def paged_attn_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float | None = None,
+                      out=None, lse=None, workspace=None, return_lse: bool = True, stream=None):
+    """Paged decode. q [B,H,d]; k_pages/v_pages [P,H,page_size,d] bf16; page_table
+    [B,max_pages] int32; ctx_lens [B] int32 (all CUDA).  ``workspace``: optional uint8
+    CUDA tensor of at least paged_attn_decode_workspace_size() bytes (allocated with torch
+    here if not given).  Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, d = q.shape
+    num_pages, Hk, page_size, dk = k_pages.shape
+    if (Hk, dk) != (H, d) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages must be [num_pages, H, page_size, d] matching q")
+    if page_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
+    max_pages = page_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, page_size))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = lib.paged_attn_decode(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table),
+                               _dptr(ctx_lens), page_size, _dptr(out), _dptr(lse), B, H, d,
+                               max_pages, num_pages, float(scale), _dptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("paged_attn_decode", st)
+    return out, lse
+
+
+def attn_check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status word."""
+    return int(load_library().attn_check_device_status(_stream_ptr(stream)))

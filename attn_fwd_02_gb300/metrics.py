@@ -1,0 +1,44 @@
+"""Work accounting for the throughput metrics (FLOPs and algorithmic bytes).
+
+Prefill FLOPs follow the convention the gpu-inference blog (section 02, "Why
+there is no throughput table here") spells out: full attention costs
+4*b*h*n^2*d FLOPs (two matmuls of 2*n^2*d each per head) and causal attention
+is credited half of that.  The inference-kernel-cookbook README's recipe 01
+output (N=2048, d=64: 12.28 ms -> 0.087 TFLOPS, 996.18 ms -> 0.001 TFLOPS)
+is consistent with 4*N^2*d, which the tests check.
+
+Algorithmic bytes count every input read once and every output written once.
+"""
+from __future__ import annotations
+
+
+def prefill_flops(B: int, H: int, Nq: int, Nkv: int, d: int, causal: bool) -> float:
+    """Metric FLOPs: 4*B*H*Nq*Nkv*d, halved when causal."""
+    f = 4.0 * B * H * Nq * Nkv * d
+    return f / 2.0 if causal else f
+
+
+def prefill_flops_kvlen(H: int, Nq: int, d: int, kv_lens) -> float:
+    """FLOPs actually required with key padding: 4*H*Nq*d*sum_b(kv_len_b) (non-causal)."""
+    return 4.0 * H * Nq * d * float(sum(int(x) for x in kv_lens))
+
+
+def prefill_bytes(B: int, H: int, Nq: int, Nkv: int, d: int, elem: int = 2, lse: bool = True,
+                  kv_lens=None) -> float:
+    """Q and O once, K and V once (only the valid prefix when key lengths are given), LSE fp32."""
+    qo = 2.0 * B * H * Nq * d * elem
+    if kv_lens is None:
+        kv = 2.0 * B * H * Nkv * d * elem
+    else:
+        kv = 2.0 * H * d * elem * float(sum(min(int(x), Nkv) for x in kv_lens))
+    return qo + kv + (4.0 * B * H * Nq if lse else 0.0)
+
+
+def decode_bytes(H: int, d: int, ctx_lens, page_size: int, elem: int = 2, lse: bool = True) -> float:
+    """K and V of every cached token once, q and o once, LSE fp32, page-table entries used."""
+    ctx = [int(x) for x in ctx_lens]
+    B = len(ctx)
+    kv = 2.0 * H * d * elem * float(sum(ctx))
+    qo = 2.0 * B * H * d * elem
+    pt = 4.0 * float(sum(-(-c // page_size) for c in ctx))
+    return kv + qo + pt + (4.0 * B * H if lse else 0.0)

@@ -1,0 +1,142 @@
+/*
+ * attn_gb300.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Two operations, both exact scaled-dot-product attention computed the
+ * FlashAttention way (K/V streamed in tiles past a resident Q tile, running
+ * max m and normaliser l, accumulator rescaled by exp(m_old - m_new), the
+ * score matrix never written to memory):
+ *
+ *   attn_fwd / attn_fwd_kvlen -- prefill forward, causal or not, emitting O
+ *       and the per-row log-sum-exp.  The method: NanoInfer README ("Flash
+ *       Attention v1/v2" bullets and the naive-vs-flash paragraph);
+ *       gpu-inference blog, section 02 (online softmax, rescale by
+ *       exp(m_old - m_new), log-sum-exp saved, causal mask combined with the
+ *       padding mask before the softmax); llm-kernel-lib README, kernel 1
+ *       (causal tile skipping); Kernel-Inference-Engine README, the tile-loop
+ *       flowchart (Q tile held, K/V tiles streamed, normalise and store).
+ *
+ *   paged_attn_decode -- one query token per sequence attending over a KV
+ *       cache split into fixed-size pages reached through a page table; the
+ *       result equals that of a contiguous cache (inference-kernel-cookbook
+ *       README, recipes 02 "KV Cache" and 03 "Paged Attention").  Long
+ *       contexts are split into chunks whose partial (m, l, O) are merged by
+ *       their log-sum-exp weights in a second pass.
+ *
+ * Definition computed (per batch b, head h, query row i):
+ *   J     = { j < Nkv : j < kv_len[b] and (not causal or j <= i + Nkv - Nq) }
+ *   s_j   = scale * <q_i, k_j>
+ *   O_i   = sum_J exp(s_j - m) v_j / sum_J exp(s_j - m),   m = max_J s_j
+ *   LSE_i = m + ln(sum_J exp(s_j - m))        (natural log, of the scaled scores)
+ *   A row with no valid key gets O_i = 0 and LSE_i = -inf.
+ *   Causal alignment is bottom-right: with Nq < Nkv the queries are the last
+ *   Nq positions of the key sequence.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     row-major.  bf16 tensors are passed as void* (storage of __nv_bfloat16).
+ *     Every tensor pointer must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  The library never allocates device memory, never copies
+ *     between host and device and never synchronises the stream.
+ *   - Host-side checks happen before any launch; on error nothing is launched
+ *     and the outputs are untouched.
+ *   - Device-resident lengths (kv_lens, ctx_lens, page_table) are not read on
+ *     the host.  The kernels clamp lengths to [0, capacity] and treat a page id
+ *     outside [0, num_pages) as an empty page (its keys are skipped), so bad
+ *     values give wrong numbers, never out-of-bounds accesses.
+ *   - Every wait inside a kernel is bounded.  A wait that runs out sets a
+ *     device status word (ATTN_ERR_DEVICE_TIMEOUT) and the kernel exits
+ *     cleanly; attn_check_device_status() reports and clears it.
+ *   - Supported: head dim d in {64, 128}; page_size 16.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, size overflow */
+    ATTN_ERR_UNSUPPORTED = 2,     /* d not in {64,128}, page_size != 16, no sm_103 device */
+    ATTN_ERR_MISALIGNED = 3,      /* a tensor pointer not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,       /* workspace missing, misaligned or too small */
+    ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call or launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 6   /* a bounded in-kernel wait ran out (see attn_check_device_status) */
+} attn_status_t;
+
+/*
+ * Prefill forward.
+ *   q   [B, H, Nq,  d] bf16      k, v [B, H, Nkv, d] bf16
+ *   o   [B, H, Nq,  d] bf16 (written, round-to-nearest-even from fp32)
+ *   lse [B, H, Nq]     fp32 (written; may be NULL to skip)
+ *   causal: 0 or 1 (bottom-right aligned).  scale: multiplier of q.k (e.g. 1/sqrt(d)).
+ * Returns ATTN_OK or an attn_status_t error code.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int Nq, int Nkv, int d, int causal, float scale,
+             attn_stream_t stream);
+
+/*
+ * Prefill forward with per-sequence key padding: key j of sequence b is valid
+ * only if j < kv_lens[b] (device int32 [B]; NULL means every key is valid).
+ * The padding mask applies to every query row and is ANDed with the causal
+ * mask.  Other arguments as attn_fwd.
+ */
+int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int Nq, int Nkv, int d, int causal, float scale,
+                   const int32_t *kv_lens, attn_stream_t stream);
+
+/*
+ * Bytes of device workspace paged_attn_decode needs for these sizes (0 on
+ * invalid sizes).  The caller allocates it (16-byte aligned) and may reuse it
+ * across calls on the same stream; calls that overlap on the GPU need
+ * separate workspaces.
+ */
+size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pages_per_seq,
+                                        int page_size);
+
+/*
+ * Paged-KV decode: one query per sequence over its cached tokens.
+ *   q          [B, H, d] bf16
+ *   k_pages    [num_pages, H, page_size, d] bf16 (one page of one head is a
+ *   v_pages     contiguous page_size x d block)
+ *   page_table [B, max_pages_per_seq] int32: physical page of logical page p of
+ *              sequence b; token t of b is slot t % page_size of page
+ *              page_table[b][t / page_size]
+ *   ctx_lens   [B] int32: number of cached tokens of each sequence (the query
+ *              attends to all of them; clamped to [0, max_pages_per_seq*page_size])
+ *   o          [B, H, d] bf16 (written)      lse [B, H] fp32 (written; may be NULL)
+ *   workspace  device scratch of at least paged_attn_decode_workspace_size() bytes
+ */
+int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                      void *o, float *lse, int B, int H, int d, int max_pages_per_seq,
+                      int num_pages, float scale, void *workspace, size_t workspace_bytes,
+                      attn_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word:
+ * ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since
+ * the last check, or ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_check_device_status(attn_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char *attn_status_string(int status);
+
+/* Library version as "major.minor.patch" (static string). */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,234 @@
+/*
+ * attn_oracle.c -- plain, slow, fp64 CPU oracle for exact scaled-dot-product
+ * attention (prefill forward) and paged-KV decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it computes (the plain definition, written out):
+ *   The pages describe FlashAttention as *exact* attention that reaches the
+ *   same result as naive attention which materialises the full N x N score
+ *   matrix (NanoInfer README, "Flash Attention v1" bullet and the naive vs
+ *   flash paragraph; inference-kernel-cookbook README, recipe 01 "Same
+ *   result").  The online-softmax recurrence is stated there to be identical
+ *   to the safe three-pass softmax (NanoInfer README, online softmax
+ *   paragraph).  So this oracle is the three-pass form:
+ *
+ *     for every batch b, head h, query row i:
+ *       J   = { j < Nkv : j < kv_len[b]  and  (not causal or j <= i + Nkv - Nq) }
+ *       s_j = scale * sum_k q[i,k] * k[j,k]                 (pass 1, with m = max s_j)
+ *       l   = sum_{j in J} exp(s_j - m)                     (pass 2)
+ *       O_i = sum_{j in J} exp(s_j - m) * v[j,:] / l        (pass 3)
+ *       LSE_i = m + ln(l)         (natural log of the sum of exp of the scaled scores)
+ *
+ *   The log-sum-exp per row is the statistic the FlashAttention-2 forward
+ *   saves for the backward (gpu-inference blog, section 02).  The causal mask
+ *   is combined with the key-padding mask before the softmax (same section).
+ *   Causal alignment when Nq != Nkv is bottom-right (query i sees keys up to
+ *   i + Nkv - Nq); the pages are silent on it and it is the reading that
+ *   matches decoding after a prefill.  A row with no valid key yields O = 0
+ *   and LSE = -inf (pages silent; chosen so the value is well defined).
+ *
+ *   Paged decode: one query per sequence attends over all ctx_len[b] cached
+ *   tokens, which live in fixed-size pages found through a page table, and
+ *   must give exactly the result of a contiguous cache (inference-kernel-
+ *   cookbook README, recipe 03 "Paged Attention").  The oracle gathers the
+ *   pages into a contiguous [ctx_len, d] buffer and applies the definition
+ *   above with Nq = 1, Nkv = ctx_len, non-causal.
+ *
+ * Inputs are bf16 bit patterns (uint16); each is widened exactly to fp64
+ * (bf16 -> fp32 by a 16-bit shift, fp32 -> fp64 exactly), so the oracle sees
+ * the very values the GPU reads.  All arithmetic is in fp64.
+ *
+ * Layouts (row-major, contiguous):
+ *   q [B,H,Nq,d], k/v [B,H,Nkv,d], o [B,H,Nq,d] (fp64), lse [B,H,Nq] (fp64)
+ *   paged: q [B,H,d]; k_pages/v_pages [num_pages,H,page_size,d];
+ *          page_table [B,max_pages] int32; ctx_lens [B] int32
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One query row against a contiguous K/V block of n_keys rows.
+ * valid[j] != 0 marks the keys in J.  srow is caller scratch of n_keys doubles. */
+static void attend_row(const uint16_t *qrow, const uint16_t *kb, const uint16_t *vb,
+                       const unsigned char *valid, int n_keys, int d, double scale,
+                       double *srow, double *out, double *lse_out) {
+    /* pass 1: scores and their maximum over the valid keys */
+    double m = -INFINITY;
+    int any = 0;
+    for (int j = 0; j < n_keys; ++j) {
+        if (!valid[j]) continue;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += bf16_to_f64(qrow[c]) * bf16_to_f64(kb[(size_t)j * d + c]);
+        srow[j] = scale * dot;
+        if (!any || srow[j] > m) m = srow[j];
+        any = 1;
+    }
+    if (!any) {
+        for (int c = 0; c < d; ++c) out[c] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
+    /* pass 2: normaliser */
+    double l = 0.0;
+    for (int j = 0; j < n_keys; ++j)
+        if (valid[j]) l += exp(srow[j] - m);
+    /* pass 3: probabilities times V */
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    for (int j = 0; j < n_keys; ++j) {
+        if (!valid[j]) continue;
+        double p = exp(srow[j] - m) / l;
+        for (int c = 0; c < d; ++c) out[c] += p * bf16_to_f64(vb[(size_t)j * d + c]);
+    }
+    *lse_out = m + log(l);
+}
+
+static int key_valid(int i, int j, int Nq, int Nkv, int kv_len, int causal) {
+    if (j >= Nkv || j >= kv_len) return 0;
+    if (causal && (long)j > (long)i + (long)Nkv - (long)Nq) return 0;
+    return 1;
+}
+
+/* Rows selected by flat index r = (b*H + h)*Nq + i.  o_rows [nrows,d], lse_rows [nrows]. */
+int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const int32_t *kv_lens, int B, int H, int Nq, int Nkv, int d,
+                         int causal, double scale, const int64_t *rows, int64_t nrows,
+                         double *o_rows, double *lse_rows, int nthreads) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0 || nrows < 0) return 1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc(sizeof(double) * (size_t)Nkv);
+        unsigned char *valid = (unsigned char *)malloc((size_t)Nkv);
+        if (!srow || !valid) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < nrows; ++t) {
+                int64_t r = rows[t];
+                if (r < 0 || r >= (int64_t)B * H * Nq) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                int i = (int)(r % Nq);
+                int64_t bh = r / Nq;
+                int b = (int)(bh / H);
+                int kv_len = kv_lens ? kv_lens[b] : Nkv;
+                for (int j = 0; j < Nkv; ++j) valid[j] = (unsigned char)key_valid(i, j, Nq, Nkv, kv_len, causal);
+                attend_row(q + (size_t)r * d, k + (size_t)bh * Nkv * d, v + (size_t)bh * Nkv * d,
+                           valid, Nkv, d, scale, srow, o_rows + (size_t)t * d, lse_rows + t);
+            }
+        }
+        free(srow);
+        free(valid);
+    }
+    return err;
+}
+
+/* Every row: o [B,H,Nq,d], lse [B,H,Nq]. */
+int oracle_attn_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const int32_t *kv_lens, int B, int H, int Nq, int Nkv, int d, int causal,
+                        double scale, double *o, double *lse, int nthreads) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0) return 1;
+    int64_t n = (int64_t)B * H * Nq;
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+    if (!rows) return 2;
+    for (int64_t r = 0; r < n; ++r) rows[r] = r;
+    int err = oracle_attn_rows_f64(q, k, v, kv_lens, B, H, Nq, Nkv, d, causal, scale, rows, n,
+                                   o, lse, nthreads);
+    free(rows);
+    return err;
+}
+
+/* Paged decode: o [B,H,d], lse [B,H]. */
+int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                            const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                            int B, int H, int d, int max_pages, int num_pages, double scale,
+                            double *o, double *lse, int nthreads) {
+    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0) return 1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+    int cap = max_pages * page_size;
+#pragma omp parallel
+    {
+        uint16_t *kc = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)cap * d);
+        uint16_t *vc = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)cap * d);
+        double *srow = (double *)malloc(sizeof(double) * (size_t)cap);
+        unsigned char *valid = (unsigned char *)malloc((size_t)cap);
+        if (!kc || !vc || !srow || !valid) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+                int b = (int)(bh / H), h = (int)(bh % H);
+                int n = ctx_lens[b];
+                if (n < 0 || n > cap) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                /* gather: logical token t lives in page page_table[b][t / page_size],
+                 * slot t % page_size, of head h */
+                int bad = 0;
+                for (int t = 0; t < n; ++t) {
+                    int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
+                    if (pg < 0 || pg >= num_pages) { bad = 1; break; }
+                    size_t src = (((size_t)pg * H + h) * page_size + (size_t)(t % page_size)) * d;
+                    memcpy(kc + (size_t)t * d, k_pages + src, sizeof(uint16_t) * (size_t)d);
+                    memcpy(vc + (size_t)t * d, v_pages + src, sizeof(uint16_t) * (size_t)d);
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                for (int t = 0; t < n; ++t) valid[t] = 1;
+                attend_row(q + (size_t)bh * d, kc, vc, valid, n, d, scale, srow,
+                           o + (size_t)bh * d, lse + bh);
+            }
+        }
+        free(kc);
+        free(vc);
+        free(srow);
+        free(valid);
+    }
+    return err;
+}
+
+/* Number of threads OpenMP would use (for reporting the CPU baseline's cores). */
+int oracle_num_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) return nthreads;
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}

@@ -1,0 +1,174 @@
+"""fp64 CPU oracle for exact attention (prefill) and paged-KV decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs may import this module.  The product
+path (the ``attn_fwd_02_gb300`` package and its CUDA library) never imports,
+loads or calls anything here, and this module imports nothing from the
+product package.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over query
+rows); this file compiles it with gcc and marshals arrays through ctypes.
+What it computes is the plain three-pass definition of attention:
+
+    s_j   = scale * q_i . k_j            over the valid keys J of row i
+    O_i   = sum_J exp(s_j - m) v_j / sum_J exp(s_j - m),   m = max_J s_j
+    LSE_i = m + ln sum_J exp(s_j - m)
+
+with J the keys that survive the key-padding mask and, if causal, the
+bottom-right causal mask j <= i + Nkv - Nq.  FlashAttention is stated on the
+pages to reach exactly this result without materialising the score matrix
+(NanoInfer README, Flash Attention bullets; inference-kernel-cookbook README,
+recipe 01).  The paged form gathers pages through the page table into a
+contiguous cache and applies the same definition (inference-kernel-cookbook
+README, recipe 03 "Paged Attention").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into a shared library (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-Wall", "-Wextra",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_attn_rows_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double,
+                                                 P, ctypes.c_int64, P, P, I]
+            lib.oracle_attn_fwd_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double,
+                                                P, P, I]
+            lib.oracle_paged_decode_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I,
+                                                    ctypes.c_double, P, P, I]
+            lib.oracle_num_threads.argtypes = [I]
+            for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
+                      lib.oracle_paged_decode_f64, lib.oracle_num_threads):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def bf16_bits(x) -> np.ndarray:
+    """bf16 bit patterns (uint16, C-contiguous) of a torch bf16 tensor or a uint16 array."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("numpy input must hold bf16 bit patterns as uint16")
+        return np.ascontiguousarray(x)
+    import torch  # plain CPU PyTorch, used only to reinterpret bits
+    if x.dtype != torch.bfloat16:
+        raise TypeError("torch input must be bfloat16")
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def bf16_to_f64(x) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    b = bf16_bits(x).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def _i32(x) -> np.ndarray | None:
+    if x is None:
+        return None
+    if not isinstance(x, np.ndarray):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads(nthreads: int = 0) -> int:
+    return int(_load().oracle_num_threads(nthreads))
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, kv_lens=None, nthreads: int = 0):
+    """Full prefill attention. q [B,H,Nq,d], k/v [B,H,Nkv,d] bf16.
+
+    Returns (O float64 [B,H,Nq,d], LSE float64 [B,H,Nq])."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    B, H, Nq, d = qb.shape
+    Nkv = kb.shape[2]
+    if kb.shape != (B, H, Nkv, d) or vb.shape != kb.shape:
+        raise ValueError("shape mismatch")
+    kl = _i32(kv_lens)
+    if kl is not None and kl.shape != (B,):
+        raise ValueError("kv_lens must be [B]")
+    o = np.empty((B, H, Nq, d), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    err = _load().oracle_attn_fwd_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(kl), B, H, Nq, Nkv, d,
+                                      int(bool(causal)), float(scale), _ptr(o), _ptr(lse), nthreads)
+    if err:
+        raise RuntimeError(f"oracle_attn_fwd_f64 failed ({err})")
+    return o, lse
+
+
+def attn_rows(q, k, v, causal: bool, scale: float, rows, kv_lens=None, nthreads: int = 0):
+    """Selected query rows, flat index r = (b*H + h)*Nq + i.
+
+    Returns (O float64 [n,d], LSE float64 [n])."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    B, H, Nq, d = qb.shape
+    Nkv = kb.shape[2]
+    if kb.shape != (B, H, Nkv, d) or vb.shape != kb.shape:
+        raise ValueError("shape mismatch")
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    kl = _i32(kv_lens)
+    o = np.empty((len(r), d), np.float64)
+    lse = np.empty((len(r),), np.float64)
+    err = _load().oracle_attn_rows_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(kl), B, H, Nq, Nkv, d,
+                                       int(bool(causal)), float(scale), _ptr(r), len(r), _ptr(o),
+                                       _ptr(lse), nthreads)
+    if err:
+        raise RuntimeError(f"oracle_attn_rows_f64 failed ({err})")
+    return o, lse
+
+
+def paged_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nthreads: int = 0):
+    """Paged decode. q [B,H,d]; k_pages/v_pages [P,H,page_size,d] bf16;
+    page_table [B,max_pages] int32; ctx_lens [B] int32.
+
+    Returns (O float64 [B,H,d], LSE float64 [B,H])."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k_pages), bf16_bits(v_pages)
+    B, H, d = qb.shape
+    P, Hk, ps, dk = kb.shape
+    if (Hk, dk) != (H, d) or vb.shape != kb.shape:
+        raise ValueError("shape mismatch")
+    pt = _i32(page_table)
+    cl = _i32(ctx_lens)
+    if pt.ndim != 2 or pt.shape[0] != B or cl.shape != (B,):
+        raise ValueError("page_table must be [B,max_pages] and ctx_lens [B]")
+    o = np.empty((B, H, d), np.float64)
+    lse = np.empty((B, H), np.float64)
+    err = _load().oracle_paged_decode_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(cl), ps, B,
+                                          H, d, pt.shape[1], P, float(scale), _ptr(o), _ptr(lse),
+                                          nthreads)
+    if err:
+        raise RuntimeError(f"oracle_paged_decode_f64 failed ({err})")
+    return o, lse

@@ -1,0 +1,327 @@
+"""Pins for the fp64 oracle: closed forms, invariants, a hand-worked example and a
+library special case.  None of these re-types the oracle's own formula; each is a
+fact the definition of exact attention fixes independently of how it is computed.
+Every test here runs on the CPU."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from attn_fwd_02_gb300 import workloads
+from attn_fwd_02_gb300.metrics import prefill_flops
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def rand_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# ----------------------------------------------------------------------------- hand-worked
+
+def test_hand_worked_tiny_example(oracle_mod):
+    g = json.load(open(os.path.join(GOLDEN, "tiny_hand.json")))
+    q = bf(g["q"]).reshape(1, 1, 2, 2)
+    k = bf(g["k"]).reshape(1, 1, 2, 2)
+    v = bf(g["v"]).reshape(1, 1, 2, 2)
+    for key, causal, kl in (("noncausal", False, None), ("causal", True, None),
+                            ("kvlen1", False, [1])):
+        o, lse = oracle_mod.attn_fwd(q, k, v, causal, g["scale"],
+                                     kv_lens=None if kl is None else np.array(kl, np.int32))
+        np.testing.assert_allclose(o[0, 0], np.array(g[key]["o"]), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, 0], np.array(g[key]["lse"]), rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_of_P_sum_to_one(oracle_mod, causal):
+    # With V = identity (Nkv = d) the output row IS the probability row P_i.
+    d = 16
+    q = rand_bf16((2, 3, d, d), 1)
+    k = rand_bf16((2, 3, d, d), 2)
+    v = torch.eye(d).to(torch.bfloat16).expand(2, 3, d, d).contiguous()
+    o, lse = oracle_mod.attn_fwd(q, k, v, causal, 0.25)
+    np.testing.assert_allclose(o.sum(-1), 1.0, rtol=0, atol=1e-12)
+    assert (o >= 0).all()
+    if causal:
+        # key j > i has probability exactly 0
+        iu = np.triu_indices(d, 1)
+        assert np.all(o[:, :, iu[0], iu[1]] == 0.0)
+    # P_ij = exp(s_ij - LSE_i): the LSE is the log-normaliser of these probabilities
+    s = 0.25 * np.einsum("bhid,bhjd->bhij", f64(q), f64(k))
+    p = np.exp(s - lse[..., None])
+    if causal:
+        p = np.tril(p)
+    np.testing.assert_allclose(o, p, rtol=0, atol=1e-12)
+
+
+def test_constant_V_returns_the_constant(oracle_mod):
+    q = rand_bf16((2, 2, 37, 64), 3)
+    k = rand_bf16((2, 2, 53, 64), 4)
+    c = bf(np.linspace(-3, 3, 64)).reshape(1, 1, 1, 64).expand(2, 2, 53, 64).contiguous()
+    for causal in (False, True):
+        o, _ = oracle_mod.attn_fwd(q, k, c, causal, 0.125)
+        np.testing.assert_allclose(o, np.broadcast_to(f64(c[:, :, :1]), o.shape), rtol=0, atol=1e-12)
+
+
+def test_zero_query_gives_mean_of_valid_values(oracle_mod):
+    B, H, N, d = 2, 3, 40, 32
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    k = rand_bf16((B, H, N, d), 5)
+    v = rand_bf16((B, H, N, d), 6)
+    kl = np.array([17, 40], np.int32)
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 0.3, kv_lens=kl)
+    for b in range(B):
+        np.testing.assert_allclose(o[b], np.broadcast_to(f64(v[b, :, :kl[b]]).mean(1, keepdims=True),
+                                                         o[b].shape), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[b], math.log(kl[b]), rtol=0, atol=1e-12)
+    # causal: row i sees i+1 keys -> LSE = ln(i+1), O_i = mean of v_0..v_i
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.3)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, N + 1)), lse.shape),
+                               rtol=0, atol=1e-12)
+    vv = f64(v)
+    cm = np.cumsum(vv, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, cm, rtol=0, atol=1e-12)
+
+
+def test_causal_query0_and_single_key(oracle_mod):
+    q = rand_bf16((1, 2, 9, 16), 7)
+    k = rand_bf16((1, 2, 9, 16), 8)
+    v = rand_bf16((1, 2, 9, 16), 9)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.5)
+    np.testing.assert_allclose(o[:, :, 0], f64(v[:, :, 0]), rtol=0, atol=1e-15)
+    s00 = 0.5 * np.einsum("bhd,bhd->bh", f64(q[:, :, 0]), f64(k[:, :, 0]))
+    np.testing.assert_allclose(lse[:, :, 0], s00, rtol=0, atol=1e-12)
+    # a single key: every query returns that key's value row, LSE = its score
+    o1, lse1 = oracle_mod.attn_fwd(q, k[:, :, :1].contiguous(), v[:, :, :1].contiguous(), False, 0.5)
+    np.testing.assert_allclose(o1, np.broadcast_to(f64(v[:, :, :1]), o1.shape), rtol=0, atol=1e-15)
+    s = 0.5 * np.einsum("bhid,bhd->bhi", f64(q), f64(k[:, :, 0]))
+    np.testing.assert_allclose(lse1, s, rtol=0, atol=1e-12)
+
+
+def test_fully_masked_row_is_zero_and_minus_inf(oracle_mod):
+    q = rand_bf16((1, 1, 6, 8), 10)
+    k = rand_bf16((1, 1, 4, 8), 11)
+    v = rand_bf16((1, 1, 4, 8), 12)
+    # causal, Nq > Nkv, bottom-right: row i sees keys j <= i - 2, rows 0,1 see nothing
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 1.0)
+    assert np.all(o[0, 0, :2] == 0.0) and np.all(np.isneginf(lse[0, 0, :2]))
+    assert np.all(np.isfinite(lse[0, 0, 2:]))
+    np.testing.assert_allclose(o[0, 0, 2], f64(v[0, 0, 0]), rtol=0, atol=1e-15)
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 1.0, kv_lens=np.array([0], np.int32))
+    assert np.all(o == 0.0) and np.all(np.isneginf(lse))
+
+
+# ----------------------------------------------------------------------------- invariants
+
+def test_causal_row_equals_noncausal_on_prefix(oracle_mod):
+    B, H, N, d = 1, 2, 23, 16
+    q, k, v = rand_bf16((B, H, N, d), 13), rand_bf16((B, H, N, d), 14), rand_bf16((B, H, N, d), 15)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.25)
+    for i in (0, 5, 11, 22):
+        oi, li = oracle_mod.attn_fwd(q[:, :, i:i + 1].contiguous(), k[:, :, :i + 1].contiguous(),
+                                     v[:, :, :i + 1].contiguous(), False, 0.25)
+        np.testing.assert_allclose(o[:, :, i], oi[:, :, 0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], li[:, :, 0], rtol=0, atol=1e-13)
+
+
+def test_bottom_right_causal_with_fewer_queries(oracle_mod):
+    # Nq < Nkv: query i (of Nq) is the last Nq positions of the key sequence
+    q, k, v = rand_bf16((1, 1, 4, 8), 16), rand_bf16((1, 1, 10, 8), 17), rand_bf16((1, 1, 10, 8), 18)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.5)
+    for i in range(4):
+        n = 10 - 4 + i + 1
+        oi, li = oracle_mod.attn_fwd(q[:, :, i:i + 1].contiguous(), k[:, :, :n].contiguous(),
+                                     v[:, :, :n].contiguous(), False, 0.5)
+        np.testing.assert_allclose(o[0, 0, i], oi[0, 0, 0], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, 0, i], li[0, 0, 0], rtol=0, atol=1e-13)
+
+
+def test_key_padding_equals_truncated_keys(oracle_mod):
+    B, H, N, d = 3, 2, 30, 16
+    q, k, v = rand_bf16((B, H, N, d), 19), rand_bf16((B, H, N, d), 20), rand_bf16((B, H, N, d), 21)
+    kl = np.array([1, 17, 30], np.int32)
+    for causal in (False, True):
+        o, lse = oracle_mod.attn_fwd(q, k, v, causal, 0.25, kv_lens=kl)
+        for b in range(B):
+            n = int(kl[b])
+            ob, lb = oracle_mod.attn_fwd(q[b:b + 1], k[b:b + 1, :, :n].contiguous(),
+                                         v[b:b + 1, :, :n].contiguous(), False, 0.25)
+            if not causal:
+                np.testing.assert_allclose(o[b], ob[0], rtol=0, atol=1e-13)
+                np.testing.assert_allclose(lse[b], lb[0], rtol=0, atol=1e-13)
+            else:
+                # AND of the masks: rows i < n see keys 0..i; rows i >= n see keys 0..n-1
+                oc, lc = oracle_mod.attn_fwd(q[b:b + 1], k[b:b + 1], v[b:b + 1], True, 0.25)
+                np.testing.assert_allclose(o[b, :, :n], oc[0, :, :n], rtol=0, atol=1e-13)
+                np.testing.assert_allclose(o[b, :, n:], ob[0, :, n:], rtol=0, atol=1e-13)
+                np.testing.assert_allclose(lse[b, :, n:], lb[0, :, n:], rtol=0, atol=1e-13)
+
+
+def test_permuting_keys_and_values_together(oracle_mod):
+    q, k, v = rand_bf16((2, 2, 12, 16), 22), rand_bf16((2, 2, 31, 16), 23), rand_bf16((2, 2, 31, 16), 24)
+    perm = torch.randperm(31, generator=torch.Generator().manual_seed(5))
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 0.25)
+    op, lp = oracle_mod.attn_fwd(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), False, 0.25)
+    np.testing.assert_allclose(o, op, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lp, rtol=0, atol=1e-13)
+    # permuting V alone must change the result (V rows are tied to their keys)
+    ov, _ = oracle_mod.attn_fwd(q, k, v[:, :, perm].contiguous(), False, 0.25)
+    assert np.abs(ov - o).max() > 1e-3
+
+
+def test_large_score_shift_is_stable(oracle_mod):
+    # k[..., 0] = 1 for every key; moving q[..., 0] from 0 to delta shifts every score by
+    # scale*delta: O is unchanged and LSE moves by exactly scale*delta.
+    d, delta, scale = 16, 8000.0, 0.125
+    q, k, v = rand_bf16((1, 2, 7, d), 25), rand_bf16((1, 2, 11, d), 26), rand_bf16((1, 2, 11, d), 27)
+    k[..., 0] = 1.0
+    q0 = q.clone(); q0[..., 0] = 0.0
+    q1 = q.clone(); q1[..., 0] = delta
+    for causal in (False, True):
+        o0, l0 = oracle_mod.attn_fwd(q0, k, v, causal, scale)
+        o1, l1 = oracle_mod.attn_fwd(q1, k, v, causal, scale)
+        assert np.isfinite(o1).all() and np.isfinite(l1).all()
+        np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l1 - l0, scale * delta, rtol=0, atol=1e-9)
+
+
+def test_split_kv_merge_identity(oracle_mod):
+    # attention over [0,n) == LSE-weighted merge of attention over [0,c) and [c,n)
+    q, k, v = rand_bf16((2, 2, 5, 32), 28), rand_bf16((2, 2, 50, 32), 29), rand_bf16((2, 2, 50, 32), 30)
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 0.2)
+    c = 19
+    o1, l1 = oracle_mod.attn_fwd(q, k[:, :, :c].contiguous(), v[:, :, :c].contiguous(), False, 0.2)
+    o2, l2 = oracle_mod.attn_fwd(q, k[:, :, c:].contiguous(), v[:, :, c:].contiguous(), False, 0.2)
+    L = np.logaddexp(l1, l2)
+    om = (np.exp(l1 - L)[..., None] * o1 + np.exp(l2 - L)[..., None] * o2)
+    np.testing.assert_allclose(L, lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(om, o, rtol=0, atol=1e-12)
+
+
+def test_rows_api_matches_full(oracle_mod):
+    q, k, v = rand_bf16((2, 3, 20, 16), 31), rand_bf16((2, 3, 26, 16), 32), rand_bf16((2, 3, 26, 16), 33)
+    kl = np.array([26, 9], np.int32)
+    o, lse = oracle_mod.attn_fwd(q, k, v, True, 0.25, kv_lens=kl)
+    rows = [0, 7, 19, 20, 61, 119]
+    orow, lrow = oracle_mod.attn_rows(q, k, v, True, 0.25, rows, kv_lens=kl)
+    np.testing.assert_array_equal(orow, o.reshape(-1, 16)[rows])
+    np.testing.assert_array_equal(lrow, lse.reshape(-1)[rows])
+
+
+# ----------------------------------------------------------------------------- library case
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_against_torch_sdpa_fp64(oracle_mod, causal):
+    # torch's CPU scaled_dot_product_attention in fp64 is an independent implementation
+    # of the same definition (top-left causal alignment, equal to ours when Nq == Nkv).
+    B, H, N, d = 2, 3, 37, 64
+    q, k, v = rand_bf16((B, H, N, d), 34), rand_bf16((B, H, N, d), 35), rand_bf16((B, H, N, d), 36)
+    kl = np.array([37, 21], np.int32)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle_mod.attn_fwd(q, k, v, causal, scale, kv_lens=kl)
+    mask = torch.arange(N)[None, :] < torch.as_tensor(kl, dtype=torch.int64)[:, None]  # [B, Nkv]
+    mask = mask[:, None, None, :].expand(B, H, N, N)
+    if causal:
+        mask = mask & torch.ones(N, N, dtype=torch.bool).tril()
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    s = (qd @ kd.transpose(-1, -2)) * scale
+    ref_lse = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- paged gather
+
+def test_paged_equals_contiguous(oracle_mod):
+    shape = workloads.DecodeShape("t", 5, 3, 32, (1, 70), page_size=16, seed=7)
+    inp = workloads.decode_inputs(shape, ctx_lens=[1, 16, 17, 70, 33])
+    o, lse = oracle_mod.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                     inp["ctx_lens"], 0.17)
+    ps = 16
+    for b, n in enumerate(inp["ctx_lens"].tolist()):
+        # build the contiguous cache by indexing pages with torch (independent of the oracle)
+        pages = inp["page_table"][b, : (n + ps - 1) // ps].long()
+        kc = inp["k_pages"][pages].permute(1, 0, 2, 3).reshape(3, -1, 32)[:, :n]
+        vc = inp["v_pages"][pages].permute(1, 0, 2, 3).reshape(3, -1, 32)[:, :n]
+        oc, lc = oracle_mod.attn_fwd(inp["q"][b][None, :, None].contiguous(), kc[None].contiguous(),
+                                     vc[None].contiguous(), False, 0.17)
+        np.testing.assert_array_equal(o[b], oc[0, :, 0])
+        np.testing.assert_array_equal(lse[b], lc[0, :, 0])
+        assert np.abs(o[b]).max() < 100.0  # no poison reached the result
+
+
+def test_paged_rejects_bad_page_ids(oracle_mod):
+    shape = workloads.DecodeShape("t", 2, 1, 8, (1, 20), seed=8)
+    inp = workloads.decode_inputs(shape, ctx_lens=[20, 5])
+    pt = inp["page_table"].clone()
+    pt[0, 1] = 10_000
+    with pytest.raises(RuntimeError):
+        oracle_mod.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], pt, inp["ctx_lens"], 1.0)
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def test_flop_formula_reproduces_printed_numbers():
+    g = json.load(open(os.path.join(GOLDEN, "flop_accounting.json")))
+    f = prefill_flops(1, 1, g["N"], g["N"], g["d"], causal=False)
+    assert f == 4 * 2048 * 2048 * 64
+    for c in g["cases"]:
+        tflops = f / (c["ms"] * 1e-3) / 1e12
+        assert round(tflops, 3) == c["tflops_printed"]
+    assert prefill_flops(2, 3, 64, 64, 32, True) == 0.5 * prefill_flops(2, 3, 64, 64, 32, False)
+
+
+def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
+    """Mutation check: a plausible bug planted in a copy of the oracle C source
+    (on the CPU) must fail at least one of the pins above."""
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle_mod.__file__), "attn_oracle.c")).read()
+    mutants = {
+        "no_max_subtraction": ("l += exp(srow[j] - m);", "l += exp(srow[j]);"),
+        "causal_off_by_one": ("(long)j > (long)i + (long)Nkv - (long)Nq", "(long)j >= (long)i + (long)Nkv - (long)Nq"),
+        "lse_missing_max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
+        "transposed_v": ("bf16_to_f64(vb[(size_t)j * d + c])", "bf16_to_f64(vb[(size_t)c * d + j % d])"),
+    }
+    q = rand_bf16((1, 2, 16, 16), 40)
+    k = rand_bf16((1, 2, 16, 16), 41)
+    v = rand_bf16((1, 2, 16, 16), 42)
+    good_o, good_l = oracle_mod.attn_fwd(q, k, v, True, 0.25)
+    for name, (a, b) in mutants.items():
+        assert a in src, name
+        path = tmp_path / f"{name}.c"
+        path.write_text(src.replace(a, b, 1))
+        so = tmp_path / f"{name}.so"
+        subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(path), "-lm"],
+                       check=True)
+        lib = ctypes.CDLL(str(so))
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_attn_fwd_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, P, I]
+        o = np.empty_like(good_o)
+        l = np.empty_like(good_l)
+        qb, kb, vb = (oracle_mod.bf16_bits(t) for t in (q, k, v))
+        lib.oracle_attn_fwd_f64(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, None, 1, 2, 16, 16, 16, 1,
+                                0.25, o.ctypes.data, l.ctypes.data, 1)
+        # the same closed forms used above: causal query 0 returns v_0 and the torch fp64 reference
+        qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+        ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, is_causal=True, scale=0.25)
+        s = (qd @ kd.transpose(-1, -2)) * 0.25
+        ref_l = torch.logsumexp(s.masked_fill(~torch.ones(16, 16, dtype=torch.bool).tril(), float("-inf")), -1)
+        assert np.allclose(good_l, ref_l.numpy(), atol=1e-12)
+        caught = (not np.allclose(o, ref.numpy(), atol=1e-9)) or (not np.allclose(l, ref_l.numpy(), atol=1e-9))
+        assert caught, f"planted mistake {name} not caught"
