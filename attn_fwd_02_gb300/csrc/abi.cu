@@ -1,0 +1,136 @@
+// abi.cu -- the C ABI declared in include/attn_gb300.h: host-side argument
+// checks, the device status word, and dispatch to the kernel launchers.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/attn_gb300.h"
+#include "launch.h"
+
+#define ATTN_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+__device__ int g_status[2];  // [0]: bit flags (1 = a bounded wait ran out), [1]: first failing site
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+std::mutex g_mu;
+
+// Per-device set-up: status-word address and architecture check.
+int device_setup(int **status_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_arch_ok[dev] == 0) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ERR_CUDA;
+        g_arch_ok[dev] = (prop.major == 10 && prop.minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1) return ATTN_ERR_UNSUPPORTED;
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *status_out = g_status_ptr[dev];
+    return ATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int prefill_checks(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
+                   int Nkv, int d, int causal, float scale, const int32_t *kv_lens) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;  // finite, positive
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    // grid = ceil(Nq/128) * B * H CTAs and 32-bit TMA coordinates
+    const uint64_t bh = (uint64_t)B * (uint64_t)H;
+    const uint64_t ctas = ((uint64_t)Nq + 127) / 128 * bh;
+    if (bh > (1ull << 31) - 1 || ctas > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+    if ((lse && !aligned4(lse)) || (kv_lens && !aligned4(kv_lens))) return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+ATTN_API int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                            int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens,
+                            attn_stream_t stream) {
+    int st = prefill_checks(q, k, v, o, lse, B, H, Nq, Nkv, d, causal, scale, kv_lens);
+    if (st != ATTN_OK) return st;
+    int *status = nullptr;
+    st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::PrefillArgs a{q, k, v, o, lse, kv_lens, status, B, H, Nq, Nkv, d, causal, scale};
+    cudaError_t e = attn::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
+                      int Nkv, int d, int causal, float scale, attn_stream_t stream) {
+    return attn_fwd_kvlen(q, k, v, o, lse, B, H, Nq, Nkv, d, causal, scale, nullptr, stream);
+}
+
+ATTN_API size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size) {
+    return attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+}
+
+ATTN_API int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                               const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int d,
+                               int max_pages_per_seq, int num_pages, float scale, void *workspace,
+                               size_t workspace_bytes, attn_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;  // grid y/z limits
+    if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+    if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
+    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, workspace, status, B, H, d, page_size,
+                       max_pages_per_seq, num_pages, scale};
+    cudaError_t e = attn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int attn_check_device_status(attn_stream_t stream) {
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int h[2] = {0, 0};
+    if (cudaMemcpy(h, status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (h[0] == 0) return ATTN_OK;
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+ATTN_API const char *attn_status_string(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or oversized dimension, bad scale)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128, page size 16, device sm_103)";
+        case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment)";
+        case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size()";
+        case ATTN_ERR_CUDA: return "CUDA runtime error or launch failure";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out; results of the affected calls are invalid";
+        default: return "unknown status";
+    }
+}
+
+ATTN_API const char *attn_version(void) { return "0.1.0"; }

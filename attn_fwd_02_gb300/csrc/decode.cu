@@ -1,0 +1,352 @@
+// decode.cu -- paged-KV decode attention for sm_103a.
+//
+// One query token per sequence attends over its ctx_len cached tokens, which
+// live in fixed-size pages reached through a page table (inference-kernel-
+// cookbook README, recipe 03 "Paged Attention": scattered physical pages, same
+// result as a contiguous cache).  The work is HBM-bound: every cached K/V byte
+// is read once and used for two FMAs.
+//
+// Pass 1 (decode_split_kernel): grid (splits, H, B).  A CTA owns one chunk of
+// kDecodeChunkTokens tokens of one (sequence, head).  Each of its 4 warps owns
+// every 4th page of the chunk and streams those pages through a private ring of
+// shared-memory slots with cp.async.bulk (one 1-D bulk copy per page per K/V:
+// a page of one head is a contiguous page_size x d block), so each SM keeps
+// tens of KB of page data in flight.  A warp keeps an online-softmax state
+// (running max m, normaliser l, unnormalised O) in the log2 domain; the four
+// warp states merge in shared memory and the CTA writes its partial (m, l, O)
+// to the workspace.
+//
+// Pass 2 (decode_combine_kernel): per (sequence, head), the partials of all
+// chunks merge with weights 2^(m_s - M):  L = sum l_s 2^(m_s-M),
+// O = sum O_s 2^(m_s-M) / L, LSE = ln2 * (M + log2 L).
+#include "launch.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kSlots = 3;  // ring slots per warp
+constexpr int kPS = 16;    // page size (tokens)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct DecodeSmem {
+    // [warp][slot][0 = K, 1 = V][kPS * D] bf16; each block is 16-byte aligned
+    alignas(128) __nv_bfloat16 kv[kWarps][kSlots][2][kPS * D];
+    uint64_t full[kWarps][kSlots];
+    float red_o[kWarps][D];
+    float red_m[kWarps];
+    float red_l[kWarps];
+    int abort_flag;
+};
+
+template <int D>
+constexpr int ws_stride() {
+    return D + 4;  // floats per partial: O[D], m, l, pad (keeps 16-byte alignment)
+}
+
+__device__ __forceinline__ float warp_max_pairs(float x) {
+    // lanes 2t and 2t+1 hold the same value; reduce over the 16 distinct values
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+    x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+    return x;
+}
+__device__ __forceinline__ float warp_sum_pairs(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 16);
+    return x;
+}
+
+// Load DPL consecutive bf16 from shared memory as fp32.
+template <int DPL>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL]) {
+    if constexpr (DPL == 4) {
+        uint2 u = *reinterpret_cast<const uint2 *>(p);
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+        uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        f[0] = __uint_as_float(u << 16);
+        f[1] = __uint_as_float(u & 0xffff0000u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits) {
+    constexpr int DPL = D / 32;  // head dims per lane
+    constexpr uint32_t kBlockBytes = kPS * D * 2;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    DecodeSmem<D> &sm = *reinterpret_cast<DecodeSmem<D> *>(smem_raw);
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cap = a.max_pages * kPS;
+    const int ctx = min(max(a.ctx_lens[b], 0), cap);
+    const int tok0 = split * kDecodeChunkTokens;
+    if (tok0 >= ctx) return;  // uniform over the CTA: this chunk is empty
+    const int tok1 = min(ctx, tok0 + kDecodeChunkTokens);
+    const int page0 = tok0 / kPS;
+    const int npages = (tok1 - tok0 + kPS - 1) / kPS;  // <= kDecodeChunkTokens / kPS = 32
+    const int nk = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;  // pages of this warp (<= 8)
+
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < kWarps; ++w)
+            for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[w][s], 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    WaitCtx wc{&sm.abort_flag, a.status};
+
+    // Page ids of this warp's pages: lane k holds the id of local page k.
+    int my_pid = -1;
+    if (lane < nk) my_pid = a.page_table[(size_t)b * a.max_pages + page0 + warp + kWarps * lane];
+    const bool my_ok = (my_pid >= 0 && my_pid < a.num_pages);
+
+    const __nv_bfloat16 *kbase = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
+    const __nv_bfloat16 *vbase = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+    auto issue = [&](int k) {
+        const int pid = __shfl_sync(0xffffffffu, my_pid, k);
+        const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
+        if (lane == 0) {
+            uint64_t *bar = &sm.full[warp][k % kSlots];
+            if (ok) {
+                const size_t off = ((size_t)pid * a.H + h) * (size_t)(kPS * D);
+                mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
+                bulk_load(sm.kv[warp][k % kSlots][0], kbase + off, kBlockBytes, bar);
+                bulk_load(sm.kv[warp][k % kSlots][1], vbase + off, kBlockBytes, bar);
+            } else {
+                mbar_arrive(bar);  // nothing to load: complete the phase so the consumer stays in step
+            }
+        }
+    };
+    const int first = nk < kSlots ? nk : kSlots;
+    for (int k = 0; k < first; ++k) issue(k);
+
+    // Query, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k
+    const float c = a.scale * kLog2e;
+    float qf[DPL];
+    {
+        const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * a.H + h) * D;
+        float t[DPL];
+        if constexpr (DPL == 4) {
+            uint2 u = *reinterpret_cast<const uint2 *>(qp + lane * DPL);
+            t[0] = __uint_as_float(u.x << 16);
+            t[1] = __uint_as_float(u.x & 0xffff0000u);
+            t[2] = __uint_as_float(u.y << 16);
+            t[3] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            uint32_t u = *reinterpret_cast<const uint32_t *>(qp + lane * DPL);
+            t[0] = __uint_as_float(u << 16);
+            t[1] = __uint_as_float(u & 0xffff0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) qf[i] = t[i] * c;
+    }
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+
+    int issued = first;
+    bool failed = false;
+    for (int k = 0; k < nk; ++k) {
+        const int slot = k % kSlots;
+        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSlots) & 1), wc, 100 + warp)) {
+            failed = true;
+            break;
+        }
+        const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
+        const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
+        const int ntok = min(kPS, tok1 - page_tok0);
+        if (ok) {
+            const __nv_bfloat16 *Ks = sm.kv[warp][slot][0];
+            const __nv_bfloat16 *Vs = sm.kv[warp][slot][1];
+            // partial dot products of the 16 tokens over this lane's DPL dims
+            float part[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                float kf[DPL];
+                load_bf16<DPL>(Ks + t * D + lane * DPL, kf);
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc = fmaf(qf[i], kf[i], acc);
+                part[t] = acc;
+            }
+            // reduce-scatter over the 32 lanes: afterwards lane L holds the full
+            // score of token L >> 1 (lanes 2t, 2t+1 hold the same value)
+            float r8[8];
+            {
+                const bool up = lane & 16;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float send = up ? part[i] : part[i + 8];
+                    const float keep = up ? part[i + 8] : part[i];
+                    r8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+            }
+            float r4[4];
+            {
+                const bool up = lane & 8;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float send = up ? r8[i] : r8[i + 4];
+                    const float keep = up ? r8[i + 4] : r8[i];
+                    r4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                }
+            }
+            float r2[2];
+            {
+                const bool up = lane & 4;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float send = up ? r4[i] : r4[i + 2];
+                    const float keep = up ? r4[i + 2] : r4[i];
+                    r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                }
+            }
+            float x;
+            {
+                const bool up = lane & 2;
+                const float send = up ? r2[0] : r2[1];
+                const float keep = up ? r2[1] : r2[0];
+                x = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            if ((lane >> 1) >= ntok) x = -INFINITY;  // slots past the context end
+
+            const float m_page = warp_max_pairs(x);
+            const float m_new = fmaxf(m_run, m_page);  // finite: ntok >= 1
+            const float alpha = ex2_approx(m_run - m_new);
+            const float p = ex2_approx(x - m_new);
+            l_run = l_run * alpha + warp_sum_pairs(p);
+            m_run = m_new;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] *= alpha;
+            for (int t = 0; t < ntok; ++t) {
+                const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
+                float vf[DPL];
+                load_bf16<DPL>(Vs + t * D + lane * DPL, vf);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) o[i] = fmaf(pt, vf[i], o[i]);
+            }
+        }
+        // the slot is free again: order this warp's reads before the next bulk write
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + kSlots < nk) {
+            issue(k + kSlots);
+            ++issued;
+        }
+    }
+    if (failed) {
+        // drain this warp's copies still in flight (bounded) before the CTA exits
+        WaitCtx drain{nullptr, a.status};
+        for (int k = 0; k < issued; ++k) {
+            if (lane == 0) {
+                // the last use of each slot is the one that matters
+                if (k + kSlots >= issued) {
+                    (void)mbar_wait(&sm.full[warp][k % kSlots], (uint32_t)((k / kSlots) & 1), drain, 199);
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    // merge the four warp states
+    if (lane == 0) {
+        sm.red_m[warp] = m_run;
+        sm.red_l[warp] = l_run;
+    }
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) sm.red_o[warp][lane * DPL + i] = o[i];
+    __syncthreads();
+    if (sm.abort_flag) return;
+    float *ws = reinterpret_cast<float *>(a.workspace) +
+                (((size_t)b * a.H + h) * max_splits + split) * (size_t)ws_stride<D>();
+    for (int dd = threadIdx.x; dd < D; dd += blockDim.x) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wgt = ex2_approx(sm.red_m[w] - M);
+                L += sm.red_l[w] * wgt;
+                O += sm.red_o[w][dd] * wgt;
+            }
+        }
+        ws[dd] = O;
+        if (dd == 0) {
+            ws[D] = M;
+            ws[D + 1] = L;
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, int max_splits) {
+    const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+    const int cap = a.max_pages * kPS;
+    const int ctx = min(max(a.ctx_lens[b], 0), cap);
+    const int nsplit = (ctx + kDecodeChunkTokens - 1) / kDecodeChunkTokens;
+    const float *ws = reinterpret_cast<const float *>(a.workspace) +
+                      ((size_t)b * a.H + h) * max_splits * (size_t)ws_stride<D>();
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ws[(size_t)s * ws_stride<D>() + D]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < nsplit; ++s) {
+            const float *w = ws + (size_t)s * ws_stride<D>();
+            const float wgt = ex2_approx(w[D] - M);
+            L += w[D + 1] * wgt;
+            O += w[dd] * wgt;
+        }
+    }
+    const size_t row = (size_t)b * a.H + h;
+    __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(a.o) + row * D;
+    const bool any = L > 0.f;
+    op[dd] = __float2bfloat16_rn(any ? O / L : 0.f);
+    if (dd == 0 && a.lse) a.lse[row] = any ? kLn2 * (M + __log2f(L)) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
+    const int max_splits = (a.max_pages * kPS + kDecodeChunkTokens - 1) / kDecodeChunkTokens;
+    const size_t smem = sizeof(DecodeSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 g1(max_splits, a.H, a.B);
+    decode_split_kernel<D><<<g1, kWarps * 32, smem, stream>>>(a, max_splits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g2(a.H, a.B);
+    decode_combine_kernel<D><<<g2, D, 0, stream>>>(a, max_splits);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size) {
+    if (B <= 0 || H <= 0 || max_pages <= 0 || page_size != kPS || (d != 64 && d != 128)) return 0;
+    const size_t max_splits = ((size_t)max_pages * kPS + kDecodeChunkTokens - 1) / kDecodeChunkTokens;
+    return (size_t)B * H * max_splits * (size_t)(d + 4) * sizeof(float);
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.d == 128) return launch_decode_d<128>(a, stream);
+    return launch_decode_d<64>(a, stream);
+}
+
+}  // namespace attn

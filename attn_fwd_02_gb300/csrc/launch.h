@@ -1,0 +1,45 @@
+// launch.h -- internal interface between the C ABI (abi.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct PrefillArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;              // may be null
+    const int32_t *kv_lens;  // may be null
+    int *status;             // device status word [2]
+    int B, H, Nq, Nkv, d, causal;
+    float scale;
+};
+
+struct DecodeArgs {
+    const void *q, *k_pages, *v_pages;
+    const int32_t *page_table, *ctx_lens;
+    void *o;
+    float *lse;  // may be null
+    void *workspace;
+    int *status;
+    int B, H, d, page_size, max_pages, num_pages;
+    float scale;
+};
+
+// Encodes the TMA descriptors and launches the prefill kernel.
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Launches the split kernel and the combine kernel.
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// Workspace bytes the decode needs (0 if the sizes are unsupported).
+size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size);
+
+// Tokens per split of the paged decode.
+constexpr int kDecodeChunkTokens = 512;
+
+}  // namespace attn

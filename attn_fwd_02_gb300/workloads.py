@@ -39,10 +39,11 @@ class PrefillShape:
     value_scale: float = 1.0
     kv_len_range: tuple[int, int] | None = None  # inclusive [lo, hi]; None = all keys valid
     seed: int = 0
+    softmax_scale: float | None = None  # None = 1/sqrt(d)
 
     @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(self.d)
+        return self.softmax_scale if self.softmax_scale is not None else 1.0 / math.sqrt(self.d)
 
 
 @dataclasses.dataclass(frozen=True)

@@ -1,0 +1,138 @@
+"""Host-only checks of the C-ABI library: it loads without a GPU, exports every
+function include/attn_gb300.h declares, and rejects bad arguments before
+touching the device.  No test here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attn_fwd_02_gb300 import build as buildmod
+    from attn_fwd_02_gb300 import binding
+    buildmod.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_kvlen", "paged_attn_decode", "paged_attn_decode_workspace_size",
+              "attn_check_device_status", "attn_status_string", "attn_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_signatures_cover_the_header():
+    from attn_fwd_02_gb300 import binding
+    assert set(binding.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    from attn_fwd_02_gb300 import binding
+    for code in range(7):
+        assert binding.attn_status_string(code)
+    assert binding.attn_status_string(99) == "unknown status"
+    assert lib.attn_version().decode().count(".") == 2
+
+
+def test_workspace_size(lib):
+    ws = lib.paged_attn_decode_workspace_size
+    # 32 x 32 heads, 512 pages of 16 tokens -> 16 chunks of 512 tokens, (d + 4) floats each
+    assert ws(32, 32, 128, 512, 16) == 32 * 32 * 16 * (128 + 4) * 4
+    assert ws(1, 1, 64, 1, 16) == 1 * 1 * 1 * (64 + 4) * 4
+    assert ws(0, 1, 64, 1, 16) == 0
+    assert ws(1, 1, 96, 1, 16) == 0
+    assert ws(1, 1, 64, 1, 32) == 0
+
+
+ALIGNED = 1 << 20  # fake, 16-byte aligned addresses: the checks below fail before any use
+
+
+def call_fwd(lib, q=ALIGNED, k=ALIGNED, v=ALIGNED, o=ALIGNED, lse=None, B=1, H=1, Nq=128, Nkv=128, d=64,
+             causal=0, scale=0.125, kv_lens=None):
+    return lib.attn_fwd_kvlen(q, k, v, o, lse, B, H, Nq, Nkv, d, causal, scale, kv_lens, None)
+
+
+def test_prefill_argument_checks(lib):
+    assert call_fwd(lib, q=None) == 1
+    assert call_fwd(lib, o=None) == 1
+    assert call_fwd(lib, B=0) == 1
+    assert call_fwd(lib, Nkv=-5) == 1
+    assert call_fwd(lib, causal=2) == 1
+    assert call_fwd(lib, scale=0.0) == 1
+    assert call_fwd(lib, scale=-1.0) == 1
+    assert call_fwd(lib, scale=float("nan")) == 1
+    assert call_fwd(lib, scale=float("inf")) == 1
+    assert call_fwd(lib, d=96) == 2
+    assert call_fwd(lib, d=32) == 2
+    assert call_fwd(lib, q=ALIGNED + 8) == 3
+    assert call_fwd(lib, o=ALIGNED + 2) == 3
+    assert call_fwd(lib, lse=ALIGNED + 2) == 3
+    assert call_fwd(lib, B=1 << 16, H=1 << 16) == 1  # B*H beyond the grid
+    assert lib.attn_fwd(None, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 1, 1, 64, 0, 0.1, None) == 1
+
+
+def call_dec(lib, q=ALIGNED, kp=ALIGNED, vp=ALIGNED, pt=ALIGNED, cl=ALIGNED, ps=16, o=ALIGNED, lse=None,
+             B=2, H=2, d=128, maxp=4, npages=8, scale=0.1, ws=ALIGNED, wsb=1 << 20):
+    return lib.paged_attn_decode(q, kp, vp, pt, cl, ps, o, lse, B, H, d, maxp, npages, scale, ws, wsb, None)
+
+
+def test_decode_argument_checks(lib):
+    assert call_dec(lib, pt=None) == 1
+    assert call_dec(lib, cl=None) == 1
+    assert call_dec(lib, B=0) == 1
+    assert call_dec(lib, npages=0) == 1
+    assert call_dec(lib, scale=0.0) == 1
+    assert call_dec(lib, d=80) == 2
+    assert call_dec(lib, ps=32) == 2
+    assert call_dec(lib, kp=ALIGNED + 4) == 3
+    assert call_dec(lib, pt=ALIGNED + 2) == 3
+    assert call_dec(lib, ws=None) == 4
+    assert call_dec(lib, ws=ALIGNED + 4) == 4
+    need = lib.paged_attn_decode_workspace_size(2, 2, 128, 4, 16)
+    assert call_dec(lib, wsb=need - 1) == 4
+    assert call_dec(lib, B=70000) == 1
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    from attn_fwd_02_gb300 import binding
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.attn_fwd(q, q, q, causal=False)
+    with pytest.raises(TypeError):
+        binding.attn_fwd(q.float(), q, q, causal=False)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from attn_fwd_02_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "_HERE", str(tmp_path))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load_library()
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "attn_fwd_02_gb300")
+    pat = re.compile(r"(import\s+oracle|from\s+oracle|liboracle|attn_oracle)")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                assert not pat.search(open(os.path.join(dirpath, f)).read()), f
