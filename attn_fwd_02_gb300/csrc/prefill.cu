@@ -219,7 +219,8 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-        // P = 2^(s*c - m_use), packed to bf16 pairs in place
+        // P = 2^(s*c - m_use), packed to bf16 pairs in place; l sums the fp32 values
+        // (the exact normaliser the log-sum-exp needs).
         float rowsum = 0.f;
         uint32_t pk[64];
 #pragma unroll

@@ -1,0 +1,524 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the attention hot path on GB300.
+
+A step is one pass of the whole hot path on one batch of synthetic input:
+one prefill forward on the long-context causal workload (B=2, H=32, N=8192,
+d=128, inputs x0.5) followed by one paged decode (B=32, H=32, d=128, contexts
+U[512, 8192] in 16-token pages).  Both inputs are larger than the 129 MB L2, so
+no flush is needed between steps (and the 2.3 GB decode pass evicts the prefill
+data anyway).
+
+Output: one JSON line.  `value` is the prefill rate in TFLOP/s (FLOPs =
+4*B*H*N^2*d / 2 for causal) summed over ranks; the `decode` object carries the
+paged-decode rate in GB/s of algorithmic HBM traffic.  Each carries a roofline
+against the measured peaks of this GPU type.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from attn_fwd_02_gb300 import metrics, workloads  # noqa: E402
+
+METRIC = "attention TFLOP/s (prefill) and HBM GB/s (paged decode), % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+KERNEL_SOURCES = {
+    "prefill_kernel": ["attn_fwd_02_gb300/csrc/prefill.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
+    "decode_split_kernel": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
+}
+
+PREFILL_BY_NAME = {
+    "tile": workloads.TILE_128x64,
+    "encoder": workloads.ENCODER_PAD,
+    "decoder": workloads.DECODER_CAUSAL,
+    "long": workloads.LONG_CAUSAL,
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    want = source_sha(kernel)
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            parts = line.split()
+            # "<kernel> <source sha> <dram bytes per launch> ..."
+            if len(parts) >= 3 and parts[0] == kernel and parts[1] == want:
+                try:
+                    return float(parts[2])
+                except ValueError:
+                    return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            if self.t_start is None or not (self.t_start - 0.05 <= t <= (self.t_stop or t) + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:  # timed region shorter than the sampling period: use everything sampled
+            rows = [[p.strip() for p in l.split(",")] for _, l in self.lines if len(l.split(",")) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier_sync(world):
+    import torch
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class PrefillCase:
+    def __init__(self, shape, torch, A):
+        self.shape, self.A = shape, A
+        inp = workloads.prefill_inputs(shape)
+        self.host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+        self.dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+        self.o = torch.empty_like(self.dev["q"])
+        self.lse = torch.empty(self.dev["q"].shape[:3], dtype=torch.float32, device="cuda")
+        kl = inp["kv_lens"]
+        self.kv_lens = None if kl is None else [int(x) for x in kl]
+        s = shape
+        if kl is None:
+            self.flops = metrics.prefill_flops(s.B, s.H, s.Nq, s.Nkv, s.d, s.causal)
+        else:
+            self.flops = metrics.prefill_flops_kvlen(s.H, s.Nq, s.d, self.kv_lens)
+        self.flops_nominal = metrics.prefill_flops(s.B, s.H, s.Nq, s.Nkv, s.d, s.causal)
+        self.bytes = metrics.prefill_bytes(s.B, s.H, s.Nq, s.Nkv, s.d, kv_lens=self.kv_lens)
+        self.launches = 1
+        # e2e buffers
+        self.o_host = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
+        self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values() if v is not None)
+        self.d2h_bytes = self.o.numel() * 2 + self.lse.numel() * 4
+
+    def run(self):
+        s, d = self.shape, self.dev
+        if d["kv_lens"] is None:
+            self.A.attn_fwd(d["q"], d["k"], d["v"], s.causal, s.scale, out=self.o, lse=self.lse)
+        else:
+            self.A.attn_fwd_kvlen(d["q"], d["k"], d["v"], s.causal, s.scale, kv_lens=d["kv_lens"], out=self.o,
+                                  lse=self.lse)
+
+    def run_e2e(self):
+        for k, v in self.host.items():
+            if v is not None:
+                self.dev[k].copy_(v, non_blocking=True)
+        self.run()
+        self.o_host.copy_(self.o, non_blocking=True)
+        self.lse_host.copy_(self.lse, non_blocking=True)
+
+
+class DecodeCase:
+    def __init__(self, shape, torch, A):
+        self.shape, self.A = shape, A
+        inp = workloads.decode_inputs(shape)
+        self.host = {k: v.pin_memory() for k, v in inp.items()}
+        self.dev = {k: v.cuda() for k, v in inp.items()}
+        d = self.dev
+        self.o = torch.empty_like(d["q"])
+        self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+        need = A.paged_attn_decode_workspace_size(shape.B, shape.H, shape.d, d["page_table"].shape[1],
+                                                  shape.page_size)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+        self.ctx = [int(x) for x in inp["ctx_lens"]]
+        self.bytes = metrics.decode_bytes(shape.H, shape.d, self.ctx, shape.page_size)
+        self.launches = 2
+        self.o_host = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
+        self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h_bytes = self.o.numel() * 2 + self.lse.numel() * 4
+
+    def run(self):
+        d = self.dev
+        self.A.paged_attn_decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"],
+                                 self.shape.scale, out=self.o, lse=self.lse, workspace=self.ws)
+
+    def run_e2e(self):
+        for k, v in self.host.items():
+            self.dev[k].copy_(v, non_blocking=True)
+        self.run()
+        self.o_host.copy_(self.o, non_blocking=True)
+        self.lse_host.copy_(self.lse, non_blocking=True)
+
+
+def time_parts(torch, parts, steps, warmup, world, sampler=None):
+    """Warm up, then time `steps` steps; each step runs every part once.  Returns the
+    region time (max over ranks) and each part's mean per-call device time (ms)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for p in parts:
+            p.run()
+    barrier_sync(world)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+           for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark(True)
+    t0.record(stream)
+    for s in range(steps):
+        for i, p in enumerate(parts):
+            evs[s][i][0].record(stream)
+            p.run()
+            evs[s][i][1].record(stream)
+    t1.record(stream)
+    barrier_sync(world)
+    if sampler:
+        sampler.mark(False)
+    region_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    part_ms = [max_over_ranks(sum(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(steps)) / steps, world)
+               for i in range(len(parts))]
+    return region_ms, part_ms
+
+
+def time_e2e(torch, part, steps, warmup, world):
+    stream = torch.cuda.current_stream()
+    for _ in range(max(1, warmup)):
+        part.run_e2e()
+    barrier_sync(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        part.run_e2e()
+    t1.record(stream)
+    barrier_sync(world)
+    return max_over_ranks(t0.elapsed_time(t1), world) / steps
+
+
+def roofline_prefill(case, ms, peaks, peak_kind):
+    achieved = case.flops / (ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = ncu_traffic("prefill_kernel") if case.shape is workloads.LONG_CAUSAL else None
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "prefill_kernel",
+            "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed in sub-second steps)"}
+
+
+def roofline_decode(case, ms_split, ms_total, peaks, peak_kind):
+    achieved = case.bytes / (ms_split * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic = ncu_traffic("decode_split_kernel")
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "decode_split_kernel",
+            "peak_source": f"{peak_kind} hbm_gbs"}
+
+
+def gpu_arm(args):
+    import torch
+
+    import attn_fwd_02_gb300 as A
+    rank, world, local = dist_setup()
+    A.load_library()
+    peaks, peak_kind = load_peaks()
+
+    if args.workload == "default":
+        pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
+        dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
+        parts = [pre, dec]
+    elif args.workload == "decode":
+        pre, dec = None, DecodeCase(workloads.PAGED_DECODE, torch, A)
+        parts = [dec]
+    else:
+        pre, dec = PrefillCase(PREFILL_BY_NAME[args.workload], torch, A), None
+        parts = [pre]
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    region_ms, part_ms = time_parts(torch, parts, args.steps, args.warmup, world, sampler)
+    clocks = sampler.stop() if sampler else None
+    status = A.attn_check_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # end-to-end through the public API with host buffers (copies inside the timed region)
+    e2e_steps = max(3, min(args.steps, 20))
+    out = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(region_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn -> bf16)"}
+    cfg = {"l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if world > 1 else "single GPU"}
+    launches = 0
+    if pre is not None:
+        i = parts.index(pre)
+        ms = part_ms[i]
+        out["value"] = round(pre.flops * world / (ms * 1e-3) / 1e12, 2)
+        out["unit"] = "TFLOP/s"
+        out["roofline"] = roofline_prefill(pre, ms, peaks, peak_kind)
+        e2e_ms = time_e2e(torch, pre, e2e_steps, 1, world)
+        out["e2e"] = {"value": round(pre.flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": int(pre.h2d_bytes), "d2h_bytes_per_step": int(pre.d2h_bytes),
+                      "ms_per_step": round(e2e_ms, 3), "part": "prefill"}
+        cfg["workload"] = pre.shape.name
+        s = pre.shape
+        cfg["prefill"] = {"B": s.B, "H": s.H, "Nq": s.Nq, "Nkv": s.Nkv, "d": s.d, "causal": s.causal,
+                          "scale": s.scale, "value_scale": s.value_scale, "kv_len_range": s.kv_len_range,
+                          "flops_per_call": pre.flops, "flops_nominal": pre.flops_nominal,
+                          "ms_per_call": round(ms, 4), "bytes_per_call": pre.bytes}
+        launches += pre.launches * args.steps
+    if dec is not None:
+        i = parts.index(dec)
+        ms = part_ms[i]
+        dec_val = dec.bytes * world / (ms * 1e-3) / 1e9
+        e2e_ms = time_e2e(torch, dec, e2e_steps, 1, world)
+        dec_obj = {"value": round(dec_val, 1), "unit": "GB/s", "ms_per_call": round(ms, 4),
+                   "bytes_per_call": dec.bytes,
+                   "roofline": roofline_decode(dec, ms, ms, peaks, peak_kind),
+                   "e2e": {"value": round(dec.bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                           "h2d_bytes_per_step": int(dec.h2d_bytes), "d2h_bytes_per_step": int(dec.d2h_bytes),
+                           "ms_per_step": round(e2e_ms, 3)}}
+        s = dec.shape
+        cfg["decode"] = {"workload": s.name, "B": s.B, "H": s.H, "d": s.d, "page_size": s.page_size,
+                         "ctx_range": s.ctx_range, "ctx_total": sum(dec.ctx)}
+        if pre is None:
+            out["value"], out["unit"] = dec_obj["value"], "GB/s"
+            out["roofline"] = dec_obj["roofline"]
+            out["e2e"] = dec_obj["e2e"]
+            cfg["workload"] = s.name
+        else:
+            out["decode"] = dec_obj
+            cfg["workload"] = f"{pre.shape.name} + {s.name}"
+        launches += dec.launches * args.steps
+    out["config"] = cfg
+    out["gpu_launches"] = launches
+    if clocks is not None:
+        out["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(pre, dec, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_prefill_sample(shape, inp, budget_s, rng_seed=0):
+    """Time the oracle on seeded random query rows until about budget_s seconds of work."""
+    import numpy as np
+
+    from oracle import oracle
+    B, H, Nq, Nkv, d = shape.B, shape.H, shape.Nq, shape.Nkv, shape.d
+    kl = inp["kv_lens"]
+    rows_all = np.random.default_rng(rng_seed).permutation(B * H * Nq)
+    done, flops, t_used, chunk = 0, 0.0, 0.0, 64
+    while done < len(rows_all) and t_used < budget_s:
+        rows = rows_all[done:done + chunk]
+        t = time.perf_counter()
+        oracle.attn_rows(inp["q"], inp["k"], inp["v"], shape.causal, shape.scale, rows, kv_lens=kl)
+        t_used += time.perf_counter() - t
+        for r in rows:  # FLOPs of these rows, counted as the metric counts them (4*d per valid key)
+            i, b = int(r % Nq), int(r // (H * Nq))
+            n = Nkv if kl is None else min(int(kl[b]), Nkv)
+            if shape.causal:
+                n = max(0, min(n, i + Nkv - Nq + 1))
+            flops += 4.0 * d * n
+        done += len(rows)
+        chunk = min(4096, chunk * 2)
+    return flops, t_used, done
+
+
+def cpu_baseline(pre, dec, budget_s):
+    from oracle import oracle
+    cores = oracle.num_threads()
+    out = {"kind": "oracle", "cores": cores}
+    if pre is not None:
+        inp = workloads.prefill_inputs(pre.shape)
+        flops, t, rows = oracle_prefill_sample(pre.shape, inp, budget_s)
+        out.update(value=round(flops / t / 1e12, 6), unit="TFLOP/s",
+                   sample=f"{rows} seeded random query rows of {pre.shape.name} ({t:.1f} s of fp64 C, OpenMP)")
+    if dec is not None:
+        inp = workloads.decode_inputs(dec.shape)
+        t = time.perf_counter()
+        oracle.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                            dec.shape.scale)
+        t = time.perf_counter() - t
+        dobj = {"value": round(dec.bytes / t / 1e9, 3), "unit": "GB/s",
+                "sample": f"the whole {dec.shape.name} ({t:.1f} s)"}
+        if pre is None:
+            out.update(dobj)
+        else:
+            out["decode"] = dobj
+    return out
+
+
+def reference_arm(args):
+    """The oracle, as it stands, on the host cores: same metric, unit and config."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    shape = workloads.LONG_CAUSAL if args.workload in ("default", "long") else PREFILL_BY_NAME.get(args.workload)
+    budget = max(2.0, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    if shape is None:  # decode only
+        dshape = workloads.PAGED_DECODE
+        inp = workloads.decode_inputs(dshape)
+        bytes_ = metrics.decode_bytes(dshape.H, dshape.d, [int(x) for x in inp["ctx_lens"]], dshape.page_size)
+        times = []
+        for s in range(args.warmup + args.steps):
+            t = time.perf_counter()
+            oracle.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                dshape.scale)
+            if s >= args.warmup:
+                times.append(time.perf_counter() - t)
+        val, unit = bytes_ / statistics.mean(times) / 1e9, "GB/s"
+        sample = f"the whole {dshape.name} per step"
+        cfgname = dshape.name
+        ms = statistics.mean(times) * 1e3
+    else:
+        inp = workloads.prefill_inputs(shape)
+        rates, ms_l = [], []
+        for s in range(args.warmup + args.steps):
+            flops, t, rows = oracle_prefill_sample(shape, inp, budget, rng_seed=s)
+            if s >= args.warmup:
+                rates.append(flops / t)
+                ms_l.append(t * 1e3)
+        val, unit = statistics.mean(rates) / 1e12, "TFLOP/s"
+        sample = f"per step, seeded random query rows of {shape.name} for about {budget:.0f} s of fp64 C"
+        cfgname = shape.name
+        ms = statistics.mean(ms_l)
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": unit, "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn -> bf16)",
+           "config": {"workload": cfgname, "l2": "n/a (CPU)"},
+           "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": round(val, 6),
+                            "unit": unit},
+           "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+           "gpu_launches": 0}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["default", "decode", *PREFILL_BY_NAME], default="default")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -26,11 +26,11 @@ def lib():
     return binding
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", o_max=O_MAX):
     o = o_gpu.float().cpu().numpy().astype(np.float64)
     err = np.abs(o - o_ref)
     assert np.isfinite(o).all(), what
-    assert err.max() <= O_MAX, f"{what}: O max-abs {err.max():.3e}"
+    assert err.max() <= o_max, f"{what}: O max-abs {err.max():.3e}"
     assert err.mean() <= O_MEAN, f"{what}: O mean-abs {err.mean():.3e}"
     if lse_gpu is not None:
         l = lse_gpu.cpu().numpy().astype(np.float64)
@@ -86,7 +86,13 @@ SMALL_PREFILL = [
 def test_prefill_small_vs_oracle(lib, oracle_mod, shape):
     inp, kl, o, lse = run_prefill(lib, shape)
     o_ref, lse_ref = oracle_mod.attn_fwd(inp["q"], inp["k"], inp["v"], shape.causal, shape.scale, kv_lens=kl)
-    compare(o, lse, o_ref, lse_ref, shape.name)
+    o_max = O_MAX
+    if shape.softmax_scale is not None:
+        # Outside the stated conditions (scale 1/sqrt(d)) the softmax can be nearly one-hot;
+        # then rounding P to bf16 moves O by up to 2^-9 * max|V| and rounding O by 2^-9 * |O|,
+        # so the bound is 2^-8 * max|V|.
+        o_max = max(O_MAX, 2.0 ** -8 * float(inp["v"].float().abs().max()))
+    compare(o, lse, o_ref, lse_ref, shape.name, o_max=o_max)
 
 
 def test_prefill_zero_length_and_full_padding(lib, oracle_mod):
