@@ -13,5 +13,6 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
     paged_attn_decode,
+    paged_attn_decode_noalloc,
     paged_attn_decode_workspace_size,
 )

@@ -21,7 +21,7 @@ _lock = threading.Lock()
 ATTN_OK = 0
 _STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
-    4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT",
+    4: "ATTN_ERR_WORKSPACE", 5: "ATTN_ERR_CUDA", 6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_SCRATCH_LIMIT",
 }
 
 # name -> (restype, argtypes); mirrors include/attn_gb300.h
@@ -31,6 +31,7 @@ SIGNATURES = {
     "attn_fwd_kvlen": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P]),
     "paged_attn_decode_workspace_size": (Z, [I, I, I, I, I]),
     "paged_attn_decode": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P, Z, P]),
+    "paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P]),
     "attn_check_device_status": (I, [P]),
     "attn_status_string": (ctypes.c_char_p, [I]),
     "attn_version": (ctypes.c_char_p, []),
@@ -188,6 +189,38 @@ def paged_attn_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float | 
                                max_pages, num_pages, float(scale), _dptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("paged_attn_decode", st)
+    return out, lse
+
+
+def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: float | None = None,
+                              out=None, lse=None, return_lse: bool = True, stream=None):
+    """paged_attn_decode without a workspace, for callers that cannot allocate device
+    memory: the library keeps the chunk partials in its own fixed 12 MiB device array.
+    Pass ``out`` (and ``lse``) to avoid any allocation here as well.  Calls that may
+    overlap on the GPU share that array and must be ordered by the caller.
+    Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, d = q.shape
+    num_pages, Hk, page_size, dk = k_pages.shape
+    if (Hk, dk) != (H, d) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages must be [num_pages, H, page_size, d] matching q")
+    if page_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    st = load_library().paged_attn_decode_noalloc(
+        _dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table), _dptr(ctx_lens), page_size, _dptr(out),
+        _dptr(lse), B, H, d, page_table.shape[1], num_pages, float(scale), _stream_ptr(stream))
+    _check("paged_attn_decode_noalloc", st)
     return out, lse
 
 

@@ -107,6 +107,34 @@ ATTN_API int paged_attn_decode(const void *q, const void *k_pages, const void *v
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Decode with the chunk partials in the library's static scratch array (decode.cu);
+// for callers that cannot allocate device memory.  Same checks as paged_attn_decode
+// minus the workspace, plus the scratch capacity.
+ATTN_API int paged_attn_decode_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                                       const int32_t *page_table, const int32_t *ctx_lens, int page_size, void *o,
+                                       float *lse, int B, int H, int d, int max_pages_per_seq, int num_pages,
+                                       float scale, attn_stream_t stream) {
+    if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;
+    if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+    if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
+    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    if (need == 0 || need > attn::decode_noalloc_scratch_bytes()) return ATTN_ERR_SCRATCH_LIMIT;
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, nullptr, status, B, H, d, page_size,
+                       max_pages_per_seq, num_pages, scale};
+    cudaError_t e = attn::launch_decode_noalloc(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 ATTN_API int attn_check_device_status(attn_stream_t stream) {
     int *status = nullptr;
     int st = device_setup(&status);
@@ -129,6 +157,7 @@ ATTN_API const char *attn_status_string(int status) {
         case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size()";
         case ATTN_ERR_CUDA: return "CUDA runtime error or launch failure";
         case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out; results of the affected calls are invalid";
+        case ATTN_ERR_SCRATCH_LIMIT: return "sizes need more decode scratch than the 12 MiB static array of paged_attn_decode_noalloc (use paged_attn_decode with a workspace)";
         default: return "unknown status";
     }
 }

@@ -19,6 +19,8 @@
 // Pass 2 (decode_combine_kernel): per (sequence, head), the partials of all
 // chunks merge with weights 2^(m_s - M):  L = sum l_s 2^(m_s-M),
 // O = sum O_s 2^(m_s-M) / L, LSE = ln2 * (M + log2 L).
+#include <mutex>
+
 #include "launch.h"
 #include "sm103_ptx.cuh"
 
@@ -347,6 +349,66 @@ size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size)
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (a.d == 128) return launch_decode_d<128>(a, stream);
     return launch_decode_d<64>(a, stream);
+}
+
+}  // namespace attn
+
+// ---------------------------------------------------------------------------
+// Decode without any device allocation by the caller.
+//
+// Some callers cannot call cudaMalloc at the point where they decode: code that
+// runs inside a memory pool or allocator that forbids nested allocation, a
+// real-time serving loop that must not take the allocator's lock or risk an
+// out-of-memory error mid-step, or a host that only hands over input and output
+// buffers.  For them the chunk partials live in a fixed array in this library's
+// own device memory.  Every GPU that loads the library holds this array until
+// the process exits.  All calls share it: its contents are whatever the last
+// call left, and nothing in it needs clearing because each call writes every
+// slot it later reads.  Calls that overlap on the GPU (different streams, or
+// different host threads without ordering) race on it.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 12u << 20;  // 12 MiB: e.g. B=32, H=32, d=128, 8192-token contexts
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxScratchDevices = 64;
+float *g_scratch_ptr[kMaxScratchDevices];
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device.  Looked up once per
+// device (the first call on each device does it; make that call before any
+// stream capture).  In host code g_decode_scratch names a host-side stand-in,
+// not device memory, so only this address may be handed to a kernel.
+cudaError_t scratch_address(float **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        if (!p) return cudaErrorInvalidSymbol;
+        g_scratch_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+namespace attn {
+
+size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_decode_noalloc(const DecodeArgs &a_in, cudaStream_t stream) {
+    float *scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    DecodeArgs a = a_in;
+    a.workspace = scratch;
+    return launch_decode(a, stream);
 }
 
 }  // namespace attn

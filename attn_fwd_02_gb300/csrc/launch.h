@@ -39,6 +39,11 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 // Workspace bytes the decode needs (0 if the sizes are unsupported).
 size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size);
 
+// Same kernels with the chunk partials in the library's static scratch array
+// (no workspace from the caller); see decode.cu.
+cudaError_t launch_decode_noalloc(const DecodeArgs &a, cudaStream_t stream);
+size_t decode_noalloc_scratch_bytes();
+
 // Tokens per split of the paged decode.
 constexpr int kDecodeChunkTokens = 512;
 

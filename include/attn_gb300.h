@@ -69,7 +69,8 @@ typedef enum {
     ATTN_ERR_MISALIGNED = 3,      /* a tensor pointer not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,       /* workspace missing, misaligned or too small */
     ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call or launch failed */
-    ATTN_ERR_DEVICE_TIMEOUT = 6   /* a bounded in-kernel wait ran out (see attn_check_device_status) */
+    ATTN_ERR_DEVICE_TIMEOUT = 6,  /* a bounded in-kernel wait ran out (see attn_check_device_status) */
+    ATTN_ERR_SCRATCH_LIMIT = 7    /* paged_attn_decode_noalloc: sizes need more than its fixed scratch */
 } attn_status_t;
 
 /*
@@ -121,6 +122,32 @@ int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                       void *o, float *lse, int B, int H, int d, int max_pages_per_seq,
                       int num_pages, float scale, void *workspace, size_t workspace_bytes,
                       attn_stream_t stream);
+
+/*
+ * paged_attn_decode for callers that cannot allocate device memory.  The pages
+ * describe no such variant; it exists for callers such as code running inside
+ * a memory pool or allocator callback (where a nested cudaMalloc is not
+ * allowed), serving loops that must not block on the allocator or risk an
+ * out-of-memory failure in the middle of a step, and hosts that can only pass
+ * the input and output buffers they already own.
+ *
+ * Arguments, layouts and results are those of paged_attn_decode without the
+ * workspace: the chunk partials live in a fixed 12 MiB array inside the
+ * library's device memory (every GPU that loads the library holds it until the
+ * process exits).  Sizes whose workspace (paged_attn_decode_workspace_size)
+ * exceeds 12 MiB are rejected with ATTN_ERR_SCRATCH_LIMIT before anything is
+ * launched.  No call allocates or frees memory.
+ *
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls that may overlap on the GPU (other streams, other
+ * host threads) race on it and must be ordered by the caller.  Each call writes
+ * every part of the array it later reads, so leftover contents do no harm.
+ */
+int paged_attn_decode_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                              const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                              void *o, float *lse, int B, int H, int d, int max_pages_per_seq,
+                              int num_pages, float scale, attn_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word:
