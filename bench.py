@@ -169,13 +169,21 @@ def barrier_sync(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's value: the job is done when the last rank is done."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float, scale: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank (weak scaling, replicas),
+    the job takes the slowest rank's time.  `scale` converts units/s to the reported unit."""
+    return units_per_rank * world / (ms_max * 1e-3) / scale
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -354,11 +362,11 @@ def gpu_arm(args):
     if pre is not None:
         i = parts.index(pre)
         ms = part_ms[i]
-        out["value"] = round(pre.flops * world / (ms * 1e-3) / 1e12, 2)
+        out["value"] = round(job_rate(pre.flops, world, ms, 1e12), 2)
         out["unit"] = "TFLOP/s"
         out["roofline"] = roofline_prefill(pre, ms, peaks, peak_kind)
         e2e_ms = time_e2e(torch, pre, e2e_steps, 1, world)
-        out["e2e"] = {"value": round(pre.flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        out["e2e"] = {"value": round(job_rate(pre.flops, world, e2e_ms, 1e12), 2), "unit": "TFLOP/s",
                       "h2d_bytes_per_step": int(pre.h2d_bytes), "d2h_bytes_per_step": int(pre.d2h_bytes),
                       "ms_per_step": round(e2e_ms, 3), "part": "prefill"}
         cfg["workload"] = pre.shape.name
@@ -371,12 +379,12 @@ def gpu_arm(args):
     if dec is not None:
         i = parts.index(dec)
         ms = part_ms[i]
-        dec_val = dec.bytes * world / (ms * 1e-3) / 1e9
+        dec_val = job_rate(dec.bytes, world, ms, 1e9)
         e2e_ms = time_e2e(torch, dec, e2e_steps, 1, world)
         dec_obj = {"value": round(dec_val, 1), "unit": "GB/s", "ms_per_call": round(ms, 4),
                    "bytes_per_call": dec.bytes,
                    "roofline": roofline_decode(dec, ms, ms, peaks, peak_kind),
-                   "e2e": {"value": round(dec.bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "e2e": {"value": round(job_rate(dec.bytes, world, e2e_ms, 1e9), 1), "unit": "GB/s",
                            "h2d_bytes_per_step": int(dec.h2d_bytes), "d2h_bytes_per_step": int(dec.d2h_bytes),
                            "ms_per_step": round(e2e_ms, 3)}}
         s = dec.shape
