@@ -2,28 +2,34 @@
 //
 // The method (NanoInfer README, Flash Attention bullets; gpu-inference blog,
 // section 02; llm-kernel-lib README, kernel 1; Kernel-Inference-Engine README,
-// tile-loop flowchart): a 128-row Q tile stays resident while 128-key K/V tiles
-// stream past it; per tile S = Q K^T * scale, mask, online softmax with a
-// running max m and normaliser l, O rescaled by exp(m_old - m_new), O += P V;
-// at the end O / l and LSE = m + ln l are stored.  The score matrix never
-// reaches global memory, and K/V tiles wholly above the causal diagonal (or
-// past the key-padding length) are never visited.
+// tile-loop flowchart): a Q tile stays resident while 128-key K/V tiles stream
+// past it; per tile S = Q K^T * scale, mask, online softmax with a running max
+// m and normaliser l, O rescaled by exp(m_old - m_new), O += P V; at the end
+// O / l and LSE = m + ln l are stored.  The score matrix never reaches global
+// memory, and K/V tiles wholly above the causal diagonal (or past the
+// key-padding length) are never visited.
 //
-// GB300 mapping (one CTA = one (batch, head, 128-row query tile), 6 warps):
-//   warp 4     TMA producer: Q once, then K and V tiles into 2-stage rings
+// GB300 mapping.  One CTA = one (batch, head) and 256 query rows held as two
+// 128-row tiles Q0, Q1 that share every K/V tile.  10 warps:
+//   warps 0-3  softmax warpgroup 0 (rows of Q0), warps 4-7  softmax warpgroup 1
+//              (rows of Q1).  Thread r of a warpgroup owns query row r = TMEM
+//              lane r: it loads its 128 scores from TMEM, masks, takes the row
+//              max, and keeps a reference max that only moves when the new max
+//              exceeds it by more than 2^8 (O and l always share the reference,
+//              so the final O / l is unchanged; only then is O rescaled in TMEM).
+//              P = 2^(x - m) is rounded to bf16 and written back into TMEM over
+//              the scores it came from, where the PV product reads it as its A
+//              operand.  The same warps run the epilogue.
+//   warp 8     TMA producer: Q0, Q1 once, then K and V tiles into 2-stage rings
 //              (128-byte swizzled boxes of 128 rows x 64 columns).
-//   warp 5     TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
-//              of two TMEM score buffers (128 lanes x 128 fp32 columns), and
-//              O += P_j V_j into a TMEM accumulator (128 lanes x d columns),
-//              each followed by tcgen05.commit onto an mbarrier.
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  It loads its
-//              128 scores from TMEM, masks, takes the row max, and keeps the
-//              reference max stale until the new max exceeds it by more than
-//              2^8 (O and l always share the same reference, so the final O / l
-//              is unchanged; only then is O in TMEM rescaled).  P = 2^(x - m)
-//              goes to shared memory as bf16 in the 128-byte swizzled K-major
-//              layout the MMA reads.  The same warps run the epilogue.
-// S_{j+1} runs on the tensor core while the softmax warps work on S_j.
+//   warp 9     TMEM owner and MMA issuer (one thread).  TMEM (512 columns):
+//              S0 | S1 (128 fp32 columns each; P_t aliases the first 64 columns
+//              of S_t as packed bf16 pairs) | O0 | O1 (d columns each).
+// Issue order per K/V tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1) -- while one
+// warpgroup turns S_t(j+1) into P, the tensor core works for the other.
+// Every tcgen05 op of the MMA thread completes in issue order, so the commit
+// that signals S_t(j) also tells warpgroup t that PV_t(j-1) has finished with
+// O_t and with the P_t columns.
 #include <cmath>
 #include <mutex>
 
@@ -35,11 +41,13 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
+constexpr int kQTiles = 2;
+constexpr int kRowsPerCta = kBM * kQTiles;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -51,40 +59,50 @@ struct PrefillParams {
     float *lse;
     const int32_t *kv_lens;
     int *status;
-    int B, H, Nq, Nkv, causal, n_qtiles;
+    int B, H, Nq, Nkv, causal, n_units;  // n_units = ceil(Nq / 256) per (b, h)
     float scale_log2;
 };
 
 template <int D>
 struct alignas(1024) PrefillSmem {
-    __nv_bfloat16 q[kBM * D];               // D/64 boxes
-    __nv_bfloat16 k[kKStages][kBN * D];     // D/64 boxes each
-    __nv_bfloat16 v[kVStages][kBN * D];     // D/64 boxes each
-    __nv_bfloat16 p[kBM * kBN];             // 2 boxes (keys 0-63, 64-127)
+    __nv_bfloat16 q[kQTiles][kBM * D];     // D/64 boxes each
+    __nv_bfloat16 k[kKStages][kBN * D];    // D/64 boxes each
+    __nv_bfloat16 v[kVStages][kBN * D];    // D/64 boxes each
     uint64_t q_full;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2];
-    uint64_t p_full;
-    uint64_t o_done;
+    uint64_t s_full[kQTiles];
+    uint64_t p_full[kQTiles];
+    uint64_t o_done[kQTiles];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
+// Key tiles query tile t of this CTA must visit: keys < limit can be valid for some of its rows.
+__device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_end) {
+    if (qs >= p.Nq) return 0;  // no rows in this tile (ragged end)
+    int limit = kv_end;
+    if (p.causal) limit = min(limit, min(qs + kBM, p.Nq) + (p.Nkv - p.Nq));
+    return limit > 0 ? (limit + kBN - 1) / kBN : 0;
+}
+
 // ------------------------------------------------------------------ producer
 template <int D>
 __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const CUtensorMap *tmK,
-                             const CUtensorMap *tmV, int bh, int q0, int n_tiles, WaitCtx wc) {
+                             const CUtensorMap *tmV, int bh, int q0, int n_all, WaitCtx wc) {
     constexpr int kBoxes = D / 64;
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
-    mbar_arrive_expect_tx(&sm.q_full, kBoxes * kBoxBytes);
+    mbar_arrive_expect_tx(&sm.q_full, kQTiles * kBoxes * kBoxBytes);
 #pragma unroll
-    for (int i = 0; i < kBoxes; ++i) tma_load_3d(sm.q + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0, bh);
+    for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
+        for (int i = 0; i < kBoxes; ++i)
+            tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
     int k_fills = 0, v_fills = 0;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < n_all; ++j) {
         const int ks = j % kKStages, kuse = j / kKStages;
         if (kuse > 0 && !mbar_wait(&sm.k_empty[ks], (uint32_t)((kuse - 1) & 1), wc, 1)) break;
         mbar_arrive_expect_tx(&sm.k_full[ks], kBoxes * kBoxBytes);
@@ -113,48 +131,66 @@ __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const C
 
 // ------------------------------------------------------------------ MMA issuer
 template <int D>
-__device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, int n_tiles, WaitCtx wc) {
+__device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTiles], int n_all, WaitCtx wc) {
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-    const uint32_t tO = tmem + 256;
-    const uint32_t q_addr = smem_u32(sm.q);
-    const uint32_t p_addr = smem_u32(sm.p);
 
-    auto issue_S = [&](int j) -> bool {
-        const int ks = j % kKStages;
-        if (!mbar_wait(&sm.k_full[ks], (uint32_t)((j / kKStages) & 1), wc, 10)) return false;
-        tc_fence_after_sync();
-        const uint32_t k_addr = smem_u32(sm.k[ks]);
-        const uint32_t tS = tmem + (uint32_t)((j & 1) * kBN);
+    // S_t(j) = Q_t K_j^T  (A = Q_t, B = K_j: both K-major, 128-byte swizzle)
+    auto issue_S = [&](int t, int j) {
+        const uint32_t q_addr = smem_u32(sm.q[t]);
+        const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
+        const uint32_t tS = tmem + (uint32_t)(t * kBN);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
             tc_mma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idS,
                       kk > 0 ? 1u : 0u);
         }
-        tc_commit(&sm.s_full[j & 1]);
-        tc_commit(&sm.k_empty[ks]);
-        return true;
+        tc_commit(&sm.s_full[t]);
+    };
+    // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
+    auto issue_PV = [&](int t, int j) {
+        const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
+        const uint32_t tP = tmem + (uint32_t)(t * kBN);
+        const uint32_t tO = tmem + 256 + (uint32_t)(t * D);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+            tc_mma_ts(tO, tP + (uint32_t)(kk * 8), sdesc_sw128(v_addr + (uint32_t)(kk * 16 * 128), kBoxBytes, 1024),
+                      idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
     };
 
-    if (mbar_wait(&sm.q_full, 0, wc, 11) && issue_S(0)) {
-        for (int j = 0; j < n_tiles; ++j) {
-            if (j + 1 < n_tiles && !issue_S(j + 1)) break;
-            if (!mbar_wait(&sm.p_full, (uint32_t)(j & 1), wc, 12)) break;
-            const int vs = j % kVStages;
-            if (!mbar_wait(&sm.v_full[vs], (uint32_t)((j / kVStages) & 1), wc, 13)) break;
-            tc_fence_after_sync();
-            const uint32_t v_addr = smem_u32(sm.v[vs]);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-                // A = P (K-major, keys contiguous); B = V (MN-major: d contiguous, 16 keys = 2048 B)
-                const uint32_t a_off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
-                const uint32_t b_off = (uint32_t)(kk * 16 * 128);
-                tc_mma_ss(tO, sdesc_sw128(p_addr + a_off, 16, 1024), sdesc_sw128(v_addr + b_off, kBoxBytes, 1024),
-                          idPV, (j > 0 || kk > 0) ? 1u : 0u);
+    bool ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.k_full[0], 0, wc, 10);
+    if (ok) {
+        tc_fence_after_sync();
+        for (int t = 0; t < kQTiles; ++t)
+            if (n[t] > 0) issue_S(t, 0);
+        tc_commit(&sm.k_empty[0]);
+        for (int j = 0; j < n_all && ok; ++j) {
+            ok = mbar_wait(&sm.v_full[j % kVStages], (uint32_t)((j / kVStages) & 1), wc, 13);
+            if (!ok) break;
+            bool k_next_ready = false;
+            for (int t = 0; t < kQTiles; ++t) {
+                if (j < n[t]) {
+                    if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
+                    tc_fence_after_sync();
+                    issue_PV(t, j);
+                    if (j == n[t] - 1) tc_commit(&sm.o_done[t]);
+                }
+                if (j + 1 < n[t]) {
+                    if (!k_next_ready) {
+                        if (!(ok = mbar_wait(&sm.k_full[(j + 1) % kKStages], (uint32_t)(((j + 1) / kKStages) & 1),
+                                             wc, 14)))
+                            break;
+                        tc_fence_after_sync();
+                        k_next_ready = true;
+                    }
+                    issue_S(t, j + 1);
+                }
             }
-            tc_commit(&sm.o_done);
-            tc_commit(&sm.v_empty[vs]);
+            if (!ok) break;
+            tc_commit(&sm.v_empty[j % kVStages]);
+            if (k_next_ready) tc_commit(&sm.k_empty[(j + 1) % kKStages]);
         }
     }
     // wait (bounded) until every MMA issued above has finished with TMEM and smem
@@ -164,51 +200,122 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, int n_tiles, WaitCtx 
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
+// O row *= alpha in TMEM (whole warp; alpha = 1 for rows that keep their reference max).
+// Rare (only when a row max grows by more than 2^8); done 16 columns at a time so it adds
+// few registers to the softmax loop.
 template <int D>
-__device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t tmem, int bh, int q0,
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+#pragma unroll 1
+    for (int cc = 0; cc < D / 16; ++cc) {
+        uint32_t ov[16];
+        tmem_ld16(tO + cc * 16, ov);
+        tmem_wait_ld16(ov);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st16(tO + cc * 16, ov);
+    }
+}
+
+// Scores at positions >= nvalid (relative to the first of the 64 held) become -inf.
+__device__ __forceinline__ void mask_chunks(uint32_t (&s)[2][32], int nvalid) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (cc * 32 + i >= nvalid) s[cc][i] = __float_as_uint(-INFINITY);
+}
+
+// Max of 64 scores: eight independent three-input chains, then a tree.
+__device__ __forceinline__ float max64(const uint32_t (&s)[2][32]) {
+    float m[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) m[a] = fmaxf(__uint_as_float(s[0][a]), __uint_as_float(s[0][a + 8]));
+#pragma unroll
+    for (int a = 0; a < 8; ++a) m[a] = fmax3(m[a], __uint_as_float(s[0][a + 16]), __uint_as_float(s[0][a + 24]));
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        m[a] = fmax3(m[a], __uint_as_float(s[1][a]), __uint_as_float(s[1][a + 8]));
+        m[a] = fmax3(m[a], __uint_as_float(s[1][a + 16]), __uint_as_float(s[1][a + 24]));
+    }
+    return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// p = 2^(s*c - m) for 64 scores (two per packed FMA), summed into rs2 and stored to TMEM
+// as 32 columns of bf16 pairs starting at tP.
+__device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t tP, uint64_t c2, uint64_t negm2,
+                                          uint64_t (&rs2)[4]) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const uint64_t x2 =
+                f32x2_fma(f32x2_pack(__uint_as_float(s[cc][i]), __uint_as_float(s[cc][i + 1])), c2, negm2);
+            float x0, x1;
+            f32x2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            rs2[(i >> 1) & 3] = f32x2_add(rs2[(i >> 1) & 3], f32x2_pack(p0, p1));
+            pk[i / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tP + cc * 16, pk);
+    }
+}
+
+template <int D>
+__device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t tmem, int t, int bh, int q0,
                             int n_tiles, int kv_end, WaitCtx wc) {
-    const int t = threadIdx.x;  // 0..127 = query row in the tile = TMEM lane
-    const int warp = t >> 5;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int row = q0 + t;
+    const int r = threadIdx.x & 127;  // query row in the tile = TMEM lane
+    const int wq = (threadIdx.x >> 5) & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t tS = lane_base + (uint32_t)(t * kBN);
+    const uint32_t tO = lane_base + 256 + (uint32_t)(t * D);
+    const int qs = q0 + t * kBM;  // first row of this tile
+    const int row = qs + r;
     const int delta = p.Nkv - p.Nq;
     const float c = p.scale_log2;
+    const uint64_t c2 = f32x2_pack(c, c);
 
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by l and O
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-        // every decision that guards a .sync.aligned tcgen05 instruction is made warp-uniform
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[j & 1], (uint32_t)((j >> 1) & 1), wc, 20))) {
+        // every decision that guards a .sync.aligned tcgen05 instruction is warp-uniform
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], (uint32_t)(j & 1), wc, 20 + t))) {
             ok = false;
             break;
         }
         tc_fence_after_sync();
-        uint32_t s[4][32];
-        const uint32_t tS = lane_base + (uint32_t)((j & 1) * kBN);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, s[cc]);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_wait_ld(s[cc]);
 
-        // mask keys that are invalid for this row (only tiles that straddle a boundary)
+        // Keys key0 .. key0+nvalid-1 are valid for this row; masking is needed only on tiles
+        // that straddle the causal diagonal or the key-padding length.
         const int key0 = j * kBN;
-        const bool need_mask = (key0 + kBN > kv_end) || (p.causal && key0 + kBN - 1 > q0 + delta);
+        const bool need_mask = (key0 + kBN > kv_end) || (p.causal && key0 + kBN - 1 > qs + delta);
+        int nvalid = kBN;
         if (need_mask) {
             int lim = kv_end;
             if (p.causal) lim = min(lim, row + delta + 1);
-            const int nvalid = lim - key0;  // keys key0 .. key0+nvalid-1 are valid
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (cc * 32 + i >= nvalid) s[cc][i] = __float_as_uint(-INFINITY);
+            nvalid = lim - key0;
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[cc][i]));
+        // At most 64 scores are live at a time: chunks 2-3 (keys 64-127) for their max, then
+        // chunks 0-1 for the max and P; chunks 2-3 are read again for their P afterwards (their
+        // TMEM columns are untouched by the P of keys 0-63, which lands in columns 0-31).
+        uint32_t s[2][32];
+        float mx;
+        {
+            tmem_ld32(tS + 64, s[0]);
+            tmem_ld32(tS + 96, s[1]);
+            tmem_wait_ld(s[0]);
+            tmem_wait_ld(s[1]);
+            if (need_mask) mask_chunks(s, nvalid - 64);
+            const float m23 = max64(s);
+            tmem_ld32(tS, s[0]);
+            tmem_ld32(tS + 32, s[1]);
+            tmem_wait_ld(s[0]);
+            tmem_wait_ld(s[1]);
+            if (need_mask) mask_chunks(s, nvalid);
+            mx = fmaxf(m23, max64(s));
+        }
         const float m_cand = mx * c;  // -inf stays -inf (c > 0)
         const bool resc = m_cand > m_ref + kRescaleThreshold;
         float alpha = 1.f;
@@ -218,74 +325,48 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             l *= alpha;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
 
-        // P = 2^(s*c - m_use), packed to bf16 pairs in place; l sums the fp32 values
-        // (the exact normaliser the log-sum-exp needs).
-        float rowsum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[cc][i]), c, -m_use));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[cc][i + 1]), c, -m_use));
-                rowsum += p0 + p1;
-                pk[cc * 16 + i / 2] = pack_bf16x2(p0, p1);
-            }
-        l += rowsum;
-
-        // O and the P buffer are free once PV(j-1) has completed
-        if (j > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_done, (uint32_t)((j - 1) & 1), wc, 21))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            if (__any_sync(0xffffffffu, resc)) {
-                const uint32_t tO = lane_base + 256;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + cc * 32, ov);
-                    tmem_wait_ld(ov);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(tO + cc * 32, ov);
-                }
-                tmem_wait_st();
-            }
-        }
-        // P row -> shared memory, 128-byte swizzle: 16-byte chunk ch of row t lands at chunk ch ^ (t & 7)
+        // P = 2^(s*c - m_use) as bf16 pairs (even key in the low half, as the TMEM A operand
+        // expects), 16 TMEM columns per 32 keys, written over scores already consumed.
+        uint64_t rs2[4] = {0, 0, 0, 0};
+        exp_store(s, tS, c2, negm2, rs2);
+        tmem_ld32(tS + 64, s[0]);
+        tmem_ld32(tS + 96, s[1]);
+        tmem_wait_ld(s[0]);
+        tmem_wait_ld(s[1]);
+        if (need_mask) mask_chunks(s, nvalid - 64);
+        exp_store(s, tS + 32, c2, negm2, rs2);
         {
-            const uint32_t pbase = smem_u32(sm.p) + (uint32_t)t * 128;
-#pragma unroll
-            for (int c16 = 0; c16 < 16; ++c16) {
-                const uint32_t box = (uint32_t)(c16 >> 3) * kBoxBytes;
-                const uint32_t ch = (uint32_t)((c16 & 7) ^ (t & 7));
-                st_shared_v4(pbase + box + ch * 16, pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2],
-                             pk[c16 * 4 + 3]);
-            }
+            const uint64_t t01 = f32x2_add(rs2[0], rs2[1]);
+            const uint64_t t23 = f32x2_add(rs2[2], rs2[3]);
+            float a0, a1;
+            f32x2_unpack(f32x2_add(t01, t23), a0, a1);
+            l += a0 + a1;
         }
-        fence_proxy_async_smem();
+
+        // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled)
+        if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<D>(tO, alpha);
+        tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(&sm.p_full);
+        mbar_arrive(&sm.p_full[t]);
     }
 
     // epilogue: O / l -> bf16, LSE = ln2 * (m_ref + log2 l)
     if (ok && n_tiles > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_done, (uint32_t)((n_tiles - 1) & 1), wc, 22))) ok = false;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], 0, wc, 22 + t))) ok = false;
         else tc_fence_after_sync();
     }
     if (!ok) return;
     const bool have = (n_tiles > 0) && (l > 0.f);
     const float inv_l = have ? 1.f / l : 0.f;
-    __nv_bfloat16 *orow = p.o + ((size_t)bh * p.Nq + row) * D;
     const bool store = row < p.Nq;
+    __nv_bfloat16 *orow = p.o + ((size_t)bh * p.Nq + (store ? row : 0)) * D;
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t ov[32];
         if (n_tiles > 0) {
-            tmem_ld32(lane_base + 256 + cc * 32, ov);
+            tmem_ld32(tO + cc * 32, ov);
             tmem_wait_ld(ov);
         }
         if (store) {
@@ -311,16 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<PrefillSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = p.B * p.H;
-    const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / BH);  // heaviest (last) query tiles first
-    const int bh = (int)(blockIdx.x % BH);
+    // Head-major order: the query tiles of one (b, h) run side by side and share its K/V
+    // through L2; within a head the heaviest (last, for causal) units go first.
+    const int bh = (int)(blockIdx.x / p.n_units);
+    const int unit = p.n_units - 1 - (int)(blockIdx.x % p.n_units);
     const int b = bh / p.H;
-    const int q0 = qt * kBM;
+    const int q0 = unit * kRowsPerCta;
     int kv_end = p.Nkv;
     if (p.kv_lens) kv_end = min(max(p.kv_lens[b], 0), p.Nkv);
-    int limit = kv_end;  // keys < limit may be valid for some row of this tile
-    if (p.causal) limit = min(limit, min(q0 + kBM, p.Nq) + (p.Nkv - p.Nq));
-    const int n_tiles = limit > 0 ? (limit + kBN - 1) / kBN : 0;
+    int n[kQTiles];
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end);
+    const int n_all = max(n[0], n[1]);
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
@@ -332,10 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.v_full[s], 1);
             mbar_init(&sm.v_empty[s], 1);
         }
-        mbar_init(&sm.s_full[0], 1);
-        mbar_init(&sm.s_full[1], 1);
-        mbar_init(&sm.p_full, kBM);
-        mbar_init(&sm.o_done, 1);
+        for (int t = 0; t < kQTiles; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.p_full[t], kBM);
+            mbar_init(&sm.o_done[t], 1);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -351,11 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     WaitCtx wc{&sm.abort_flag, p.status};
 
     if (warp == kProducerWarp) {
-        if (lane == 0 && n_tiles > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, q0, n_tiles, wc);
+        if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, q0, n_all, wc);
     } else if (warp == kMmaWarp) {
-        if (lane == 0 && n_tiles > 0) run_mma<D>(sm, tmem, n_tiles, wc);
+        if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
     } else {
-        run_softmax<D>(sm, p, tmem, bh, q0, n_tiles, kv_end, wc);
+        const int t = warp >> 2;  // warpgroup = query tile
+        run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, wc);
     }
 
     tc_fence_before_sync();
@@ -415,12 +500,12 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.Nq = a.Nq;
     p.Nkv = a.Nkv;
     p.causal = a.causal;
-    p.n_qtiles = (a.Nq + kBM - 1) / kBM;
+    p.n_units = (a.Nq + kRowsPerCta - 1) / kRowsPerCta;
     p.scale_log2 = a.scale * kLog2e;
     const size_t smem = sizeof(PrefillSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((size_t)p.n_qtiles * BH);
+    const unsigned grid = (unsigned)((size_t)p.n_units * BH);
     prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
