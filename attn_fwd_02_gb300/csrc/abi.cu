@@ -5,7 +5,7 @@
 
 #include <mutex>
 
-#include "../../include/attn_gb300.h"
+#include "attn_gb300.h"
 #include "launch.h"
 
 #define ATTN_API extern "C" __attribute__((visibility("default")))

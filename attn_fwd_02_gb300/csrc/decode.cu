@@ -45,7 +45,7 @@ struct DecodeSmem {
 };
 
 template <int D>
-constexpr int ws_stride() {
+__host__ __device__ constexpr int ws_stride() {
     return D + 4;  // floats per partial: O[D], m, l, pad (keeps 16-byte alignment)
 }
 

@@ -20,7 +20,7 @@
 //              P = 2^(x - m) is rounded to bf16 and written back into TMEM over
 //              the scores it came from, where the PV product reads it as its A
 //              operand.  The same warps run the epilogue.
-//   warp 8     TMA producer: Q0, Q1 once, then K and V tiles into 2-stage rings
+//   warp 8     TMA producer: Q0, Q1 once, then K and V tiles through a 2-slot ring
 //              (128-byte swizzled boxes of 128 rows x 64 columns).
 //   warp 9     TMEM owner and MMA issuer (one thread).  TMEM (512 columns):
 //              S0 | S1 (128 fp32 columns each; P_t aliases the first 64 columns
@@ -43,8 +43,6 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kQTiles = 2;
 constexpr int kRowsPerCta = kBM * kQTiles;
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -63,14 +61,20 @@ struct PrefillParams {
     float scale_log2;
 };
 
+// K/V ring.  Step j of the MMA issuer (PV(j) then S(j+1)) needs V(j) and K(j+1) together,
+// so they travel as one ring unit: unit u = {K(u), V(u-1)} (unit 0 has only K(0), unit n only
+// V(n-1)); K(j) sits in slot j % kStages, V(j) in slot (j+1) % kStages.  One full and one
+// empty barrier per unit keeps the single MMA-issuing thread's synchronisation per step at
+// one wait and one commit for the ring.
+constexpr int kStages = 2;
+
 template <int D>
 struct alignas(1024) PrefillSmem {
     __nv_bfloat16 q[kQTiles][kBM * D];     // D/64 boxes each
-    __nv_bfloat16 k[kKStages][kBN * D];    // D/64 boxes each
-    __nv_bfloat16 v[kVStages][kBN * D];    // D/64 boxes each
+    __nv_bfloat16 k[kStages][kBN * D];     // D/64 boxes each
+    __nv_bfloat16 v[kStages][kBN * D];     // D/64 boxes each
     uint64_t q_full;
-    uint64_t k_full[kKStages], k_empty[kKStages];
-    uint64_t v_full[kVStages], v_empty[kVStages];
+    uint64_t u_full[kStages], u_empty[kStages];
     uint64_t s_full[kQTiles];
     uint64_t p_full[kQTiles];
     uint64_t o_done[kQTiles];
@@ -101,31 +105,30 @@ __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const C
 #pragma unroll
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
-    int k_fills = 0, v_fills = 0;
-    for (int j = 0; j < n_all; ++j) {
-        const int ks = j % kKStages, kuse = j / kKStages;
-        if (kuse > 0 && !mbar_wait(&sm.k_empty[ks], (uint32_t)((kuse - 1) & 1), wc, 1)) break;
-        mbar_arrive_expect_tx(&sm.k_full[ks], kBoxes * kBoxBytes);
+    int fills = 0;
+    for (int u = 0; u <= n_all; ++u) {
+        const int slot = u % kStages, use = u / kStages;
+        if (use > 0 && !mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 1)) break;
+        const bool has_k = u < n_all, has_v = u > 0;
+        mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kBoxBytes);
+        if (has_k) {
 #pragma unroll
-        for (int i = 0; i < kBoxes; ++i)
-            tma_load_3d(sm.k[ks] + i * (kBN * 64), tmK, &sm.k_full[ks], i * 64, j * kBN, bh);
-        ++k_fills;
-        const int vs = j % kVStages, vuse = j / kVStages;
-        if (vuse > 0 && !mbar_wait(&sm.v_empty[vs], (uint32_t)((vuse - 1) & 1), wc, 2)) break;
-        mbar_arrive_expect_tx(&sm.v_full[vs], kBoxes * kBoxBytes);
+            for (int i = 0; i < kBoxes; ++i)
+                tma_load_3d(sm.k[slot] + i * (kBN * 64), tmK, &sm.u_full[slot], i * 64, u * kBN, bh);
+        }
+        if (has_v) {
 #pragma unroll
-        for (int i = 0; i < kBoxes; ++i)
-            tma_load_3d(sm.v[vs] + i * (kBN * 64), tmV, &sm.v_full[vs], i * 64, j * kBN, bh);
-        ++v_fills;
+            for (int i = 0; i < kBoxes; ++i)
+                tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh);
+        }
+        ++fills;
     }
     if (*wc.abort_flag) {
         // unwinding: let every copy still in flight land before the CTA exits
         WaitCtx drain{nullptr, wc.status};
         (void)mbar_wait(&sm.q_full, 0, drain, 90);
-        for (int f = (k_fills > kKStages ? k_fills - kKStages : 0); f < k_fills; ++f)
-            (void)mbar_wait(&sm.k_full[f % kKStages], (uint32_t)((f / kKStages) & 1), drain, 91);
-        for (int f = (v_fills > kVStages ? v_fills - kVStages : 0); f < v_fills; ++f)
-            (void)mbar_wait(&sm.v_full[f % kVStages], (uint32_t)((f / kVStages) & 1), drain, 92);
+        for (int f = (fills > kStages ? fills - kStages : 0); f < fills; ++f)
+            (void)mbar_wait(&sm.u_full[f % kStages], (uint32_t)((f / kStages) & 1), drain, 91);
     }
 }
 
@@ -138,7 +141,7 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
     // S_t(j) = Q_t K_j^T  (A = Q_t, B = K_j: both K-major, 128-byte swizzle)
     auto issue_S = [&](int t, int j) {
         const uint32_t q_addr = smem_u32(sm.q[t]);
-        const uint32_t k_addr = smem_u32(sm.k[j % kKStages]);
+        const uint32_t k_addr = smem_u32(sm.k[j % kStages]);
         const uint32_t tS = tmem + (uint32_t)(t * kBN);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -150,7 +153,7 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
     };
     // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
     auto issue_PV = [&](int t, int j) {
-        const uint32_t v_addr = smem_u32(sm.v[j % kVStages]);
+        const uint32_t v_addr = smem_u32(sm.v[(j + 1) % kStages]);
         const uint32_t tP = tmem + (uint32_t)(t * kBN);
         const uint32_t tO = tmem + 256 + (uint32_t)(t * D);
 #pragma unroll
@@ -160,16 +163,19 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
         }
     };
 
-    bool ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.k_full[0], 0, wc, 10);
+    // The data waits below (Q, ring units) need no tcgen05 fence: TMA writes and the MMA's
+    // operand reads are both async-proxy traffic ordered by the mbarrier.  The P waits do
+    // (P was written to TMEM by other threads).
+    bool ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.u_full[0], 0, wc, 10);
     if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < kQTiles; ++t)
             if (n[t] > 0) issue_S(t, 0);
-        tc_commit(&sm.k_empty[0]);
+        tc_commit(&sm.u_empty[0]);
         for (int j = 0; j < n_all && ok; ++j) {
-            ok = mbar_wait(&sm.v_full[j % kVStages], (uint32_t)((j / kVStages) & 1), wc, 13);
+            const int u = j + 1;  // unit with V(j) and K(j+1)
+            ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13);
             if (!ok) break;
-            bool k_next_ready = false;
             for (int t = 0; t < kQTiles; ++t) {
                 if (j < n[t]) {
                     if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
@@ -177,20 +183,10 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
                     issue_PV(t, j);
                     if (j == n[t] - 1) tc_commit(&sm.o_done[t]);
                 }
-                if (j + 1 < n[t]) {
-                    if (!k_next_ready) {
-                        if (!(ok = mbar_wait(&sm.k_full[(j + 1) % kKStages], (uint32_t)(((j + 1) / kKStages) & 1),
-                                             wc, 14)))
-                            break;
-                        tc_fence_after_sync();
-                        k_next_ready = true;
-                    }
-                    issue_S(t, j + 1);
-                }
+                if (j + 1 < n[t]) issue_S(t, j + 1);
             }
             if (!ok) break;
-            tc_commit(&sm.v_empty[j % kVStages]);
-            if (k_next_ready) tc_commit(&sm.k_empty[(j + 1) % kKStages]);
+            tc_commit(&sm.u_empty[u % kStages]);
         }
     }
     // wait (bounded) until every MMA issued above has finished with TMEM and smem
@@ -407,13 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&sm.k_full[s], 1);
-            mbar_init(&sm.k_empty[s], 1);
-        }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(&sm.v_full[s], 1);
-            mbar_init(&sm.v_empty[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.u_full[s], 1);
+            mbar_init(&sm.u_empty[s], 1);
         }
         for (int t = 0; t < kQTiles; ++t) {
             mbar_init(&sm.s_full[t], 1);

@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Limits of every in-kernel wait: about two seconds of wall time, and an
 // absolute cap on polls.  A wait that runs out raises the CTA's abort flag and
 // the device status word and returns false; callers then unwind.
@@ -64,8 +77,10 @@ struct WaitCtx {
 };
 
 // A wait with a null abort flag (used to drain copies in flight while unwinding)
-// ignores the CTA's abort state and stops only at its own limits.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, WaitCtx w, int site) {
+// ignores the CTA's abort state and stops only at its own limits.  Inlined, not
+// called: kernels that reconfigure registers per warpgroup (setmaxnreg) cannot
+// contain calls.
+static __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, WaitCtx w, int site) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1; it < kWaitLimitPolls; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -82,6 +97,15 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCtx w, int site) {
     if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, w, site);
+}
+
+// Bounded wait that spins on the non-blocking probe for a while before falling back to
+// the suspending wait: lower wake-up latency for a thread on the critical path.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, WaitCtx w, int site) {
+#pragma unroll 1
+    for (int i = 0; i < 4096; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, w, site);
 }
 
@@ -110,6 +134,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorM
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
+}
+
+// Prefetch one box of a tiled 3-D tensor into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -274,6 +306,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- register reconfiguration
+// Per-warpgroup register limits (all four warps of the warpgroup execute it).  The block's
+// register pool is its launch allocation (threads x registers at launch); the callers keep
+// the sum of the new per-warpgroup limits within it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- math

@@ -75,6 +75,10 @@ LONG_CAUSAL = PrefillShape("long-context causal B2 H32 N8192 d128 inputs x0.5",
 PAGED_DECODE = DecodeShape("paged decode B32 H32 d128 ctx U[512,8192] page16",
                            32, 32, 128, (512, 8192), 16, seed=1005)
 
+# A quarter-size paged decode (same lengths distribution) for multi-pass profiler captures.
+PAGED_DECODE_SMALL = DecodeShape("paged decode B8 H32 d128 ctx U[512,8192] page16",
+                                 8, 32, 128, (512, 8192), 16, seed=1006)
+
 PREFILL_WORKLOADS = (TILE_128x64, ENCODER_PAD, DECODER_CAUSAL, LONG_CAUSAL)
 
 

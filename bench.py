@@ -335,8 +335,9 @@ def gpu_arm(args):
         pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
         dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
         parts = [pre, dec]
-    elif args.workload == "decode":
-        pre, dec = None, DecodeCase(workloads.PAGED_DECODE, torch, A)
+    elif args.workload in ("decode", "decode_small"):
+        shape = workloads.PAGED_DECODE if args.workload == "decode" else workloads.PAGED_DECODE_SMALL
+        pre, dec = None, DecodeCase(shape, torch, A)
         parts = [dec]
     else:
         pre, dec = PrefillCase(PREFILL_BY_NAME[args.workload], torch, A), None
@@ -517,7 +518,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["default", "decode", *PREFILL_BY_NAME], default="default")
+    ap.add_argument("--workload", choices=["default", "decode", "decode_small", *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
