@@ -10,7 +10,7 @@
 // key-padding length) are never visited.
 //
 // GB300 mapping.  One CTA = one (batch, head) and 256 query rows held as two
-// 128-row tiles Q0, Q1 that share every K/V tile.  10 warps:
+// 128-row tiles Q0, Q1 that share every K/V tile.  12 warps (three warpgroups):
 //   warps 0-3  softmax warpgroup 0 (rows of Q0), warps 4-7  softmax warpgroup 1
 //              (rows of Q1).  Thread r of a warpgroup owns query row r = TMEM
 //              lane r: it loads its 128 scores from TMEM, masks, takes the row
@@ -25,6 +25,8 @@
 //   warp 9     TMEM owner and MMA issuer (one thread).  TMEM (512 columns):
 //              S0 | S1 (128 fp32 columns each; P_t aliases the first 64 columns
 //              of S_t as packed bf16 pairs) | O0 | O1 (d columns each).
+//   warps 10-11 idle: the third warpgroup hands its registers to the softmax
+//              warpgroups (setmaxnreg), so a thread holds its whole 128-score row.
 // Issue order per K/V tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1) -- while one
 // warpgroup turns S_t(j+1) into P, the tensor core works for the other.
 // Every tcgen05 op of the MMA thread completes in issue order, so the commit
@@ -43,7 +45,13 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr int kQTiles = 2;
 constexpr int kRowsPerCta = kBM * kQTiles;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split: launched at 168 per thread (384 x 168 = 64512 in the block's pool); the
+// producer/MMA warpgroup drops to 64 and each softmax warpgroup rises to 216:
+// 128 x (64 + 216 + 216) = 63488 <= 64512, and per SM sub-partition (one warp of each
+// warpgroup) 32 x 496 <= 16384 registers.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 64;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -293,25 +301,22 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             if (p.causal) lim = min(lim, row + delta + 1);
             nvalid = lim - key0;
         }
-        // At most 64 scores are live at a time: chunks 2-3 (keys 64-127) for their max, then
-        // chunks 0-1 for the max and P; chunks 2-3 are read again for their P afterwards (their
-        // TMEM columns are untouched by the P of keys 0-63, which lands in columns 0-31).
-        uint32_t s[2][32];
-        float mx;
-        {
-            tmem_ld32(tS + 64, s[0]);
-            tmem_ld32(tS + 96, s[1]);
-            tmem_wait_ld(s[0]);
-            tmem_wait_ld(s[1]);
-            if (need_mask) mask_chunks(s, nvalid - 64);
-            const float m23 = max64(s);
-            tmem_ld32(tS, s[0]);
-            tmem_ld32(tS + 32, s[1]);
-            tmem_wait_ld(s[0]);
-            tmem_wait_ld(s[1]);
-            if (need_mask) mask_chunks(s, nvalid);
-            mx = fmaxf(m23, max64(s));
+        uint32_t s[2][2][32];  // the row's 128 scores as two halves of 64
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tmem_ld32(tS + h * 64, s[h][0]);
+            tmem_ld32(tS + h * 64 + 32, s[h][1]);
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tmem_wait_ld(s[h][0]);
+            tmem_wait_ld(s[h][1]);
+        }
+        if (need_mask) {
+            mask_chunks(s[0], nvalid);
+            mask_chunks(s[1], nvalid - 64);
+        }
+        const float mx = fmaxf(max64(s[0]), max64(s[1]));
         const float m_cand = mx * c;  // -inf stays -inf (c > 0)
         const bool resc = m_cand > m_ref + kRescaleThreshold;
         float alpha = 1.f;
@@ -324,15 +329,11 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
         const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
 
         // P = 2^(s*c - m_use) as bf16 pairs (even key in the low half, as the TMEM A operand
-        // expects), 16 TMEM columns per 32 keys, written over scores already consumed.
+        // expects): keys 0-63 -> columns 0-31, keys 64-127 -> columns 32-63, over scores
+        // already read into registers.
         uint64_t rs2[4] = {0, 0, 0, 0};
-        exp_store(s, tS, c2, negm2, rs2);
-        tmem_ld32(tS + 64, s[0]);
-        tmem_ld32(tS + 96, s[1]);
-        tmem_wait_ld(s[0]);
-        tmem_wait_ld(s[1]);
-        if (need_mask) mask_chunks(s, nvalid - 64);
-        exp_store(s, tS + 32, c2, negm2, rs2);
+        exp_store(s[0], tS, c2, negm2, rs2);
+        exp_store(s[1], tS + 32, c2, negm2, rs2);
         {
             const uint64_t t01 = f32x2_add(rs2[0], rs2[1]);
             const uint64_t t23 = f32x2_add(rs2[2], rs2[3]);
@@ -426,11 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     WaitCtx wc{&sm.abort_flag, p.status};
 
-    if (warp == kProducerWarp) {
-        if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, q0, n_all, wc);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
+    if (warp >= 8) {
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == kProducerWarp) {
+            if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, q0, n_all, wc);
+        } else if (warp == kMmaWarp) {
+            if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
+        }
     } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
         run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, wc);
     }
