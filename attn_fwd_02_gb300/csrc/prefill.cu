@@ -66,6 +66,7 @@ struct PrefillParams {
     const int32_t *kv_lens;
     int *status;
     int B, H, Nq, Nkv, causal, n_units;  // n_units = ceil(Nq / 256) per (b, h)
+    int heads_per_chunk;                 // heads whose K/V share L2 at a time (see the CTA order)
     float scale_log2;
 };
 
@@ -389,10 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<PrefillSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Head-major order: the query tiles of one (b, h) run side by side and share its K/V
-    // through L2; within a head the heaviest (last, for causal) units go first.
-    const int bh = (int)(blockIdx.x / p.n_units);
-    const int unit = p.n_units - 1 - (int)(blockIdx.x % p.n_units);
+    // CTA order: heads are taken in chunks small enough that the chunk's K/V stays in L2
+    // while its query units stream it; inside a chunk the units go heaviest first across
+    // all its heads (the last query rows, which see the most keys under the causal mask).
+    // The hardware dispatches CTAs in index order, so this is a longest-first schedule per
+    // chunk: no heavy unit is left to start at the end of the launch.
+    const int BH = p.B * p.H;
+    const int per_chunk = p.heads_per_chunk * p.n_units;
+    const int chunk = (int)(blockIdx.x / per_chunk);
+    const int h0 = chunk * p.heads_per_chunk;
+    const int heads = min(p.heads_per_chunk, BH - h0);  // the last chunk may be smaller
+    const int in_chunk = (int)(blockIdx.x % per_chunk);
+    const int level = in_chunk / heads;  // 0 = heaviest unit of a head
+    const int bh = h0 + in_chunk % heads;
+    const int unit = p.n_units - 1 - level;
     const int b = bh / p.H;
     const int q0 = unit * kRowsPerCta;
     int kv_end = p.Nkv;
@@ -498,6 +509,13 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.Nkv = a.Nkv;
     p.causal = a.causal;
     p.n_units = (a.Nq + kRowsPerCta - 1) / kRowsPerCta;
+    {
+        // about 48 MB of K/V per chunk: two chunks (the one finishing, the one starting) fit
+        // in the 126 MB L2 together
+        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0;
+        int hpc = (int)(48.0e6 / kv_bytes_per_head);
+        p.heads_per_chunk = hpc < 1 ? 1 : (hpc > BH ? BH : hpc);
+    }
     p.scale_log2 = a.scale * kLog2e;
     const size_t smem = sizeof(PrefillSmem<D>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
