@@ -7,12 +7,15 @@ fallback: if the library is missing, every call raises.
 from .binding import (  # noqa: F401
     AttnError,
     attn_check_device_status,
+    attn_selftest_bounded_wait,
     attn_fwd,
+    attn_fwd_gqa,
     attn_fwd_kvlen,
     attn_status_string,
     library_path,
     load_library,
     paged_attn_decode,
+    paged_attn_decode_gqa,
     paged_attn_decode_noalloc,
     paged_attn_decode_workspace_size,
 )

@@ -29,10 +29,13 @@ P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "attn_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P]),
     "attn_fwd_kvlen": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P]),
+    "attn_fwd_gqa": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]),
     "paged_attn_decode_workspace_size": (Z, [I, I, I, I, I]),
     "paged_attn_decode": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P, Z, P]),
     "paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P]),
+    "paged_attn_decode_gqa": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
     "attn_check_device_status": (I, [P]),
+    "attn_selftest_bounded_wait": (I, [P]),
     "attn_status_string": (ctypes.c_char_p, [I]),
     "attn_version": (ctypes.c_char_p, []),
 }
@@ -127,6 +130,31 @@ def attn_fwd_kvlen(q, k, v, causal: bool, scale: float | None = None, kv_lens=No
     return out, lse
 
 
+def attn_fwd_gqa(q, k, v, causal: bool, scale: float | None = None, kv_lens=None, out=None, lse=None,
+                 return_lse: bool = True, stream=None):
+    """Grouped-query prefill: q [B,Hq,Nq,d], k/v [B,Hkv,Nkv,d] bf16 CUDA tensors with
+    Hq % Hkv == 0 (query head h reads key/value head h // (Hq // Hkv)).  Returns (o, lse)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, torch.bfloat16, 4)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nkv, d) or tuple(v.shape) != (B, Hkv, Nkv, d):
+        raise ValueError("k and v must be [B, Hkv, Nkv, d] matching q")
+    if kv_lens is not None:
+        _require(kv_lens, "kv_lens", torch.int32, 1)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    st = load_library().attn_fwd_gqa(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, Hq, Hkv, Nq, Nkv,
+                                     d, int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
+    _check("attn_fwd_gqa", st)
+    return out, lse
+
+
 def attn_fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None,
              return_lse: bool = True, stream=None):
     """Prefill attention without key padding (calls the C entry point attn_fwd)."""
@@ -192,6 +220,41 @@ def paged_attn_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float | 
     return out, lse
 
 
+def paged_attn_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float | None = None,
+                          out=None, lse=None, workspace=None, return_lse: bool = True, stream=None):
+    """Grouped-query paged decode: q [B,H,d]; k_pages/v_pages [P,Hkv,page_size,d] with
+    H % Hkv == 0; page_table [B,max_pages] int32; ctx_lens [B] int32.  Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, d = q.shape
+    num_pages, Hkv, page_size, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages must be [num_pages, Hkv, page_size, d] matching q")
+    if page_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
+    max_pages = page_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, page_size))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = lib.paged_attn_decode_gqa(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table), _dptr(ctx_lens),
+                                   page_size, _dptr(out), _dptr(lse), B, H, Hkv, d, max_pages, num_pages,
+                                   float(scale), _dptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream_ptr(stream))
+    _check("paged_attn_decode_gqa", st)
+    return out, lse
+
+
 def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: float | None = None,
                               out=None, lse=None, return_lse: bool = True, stream=None):
     """paged_attn_decode without a workspace, for callers that cannot allocate device
@@ -222,6 +285,11 @@ def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: 
         _dptr(lse), B, H, d, page_table.shape[1], num_pages, float(scale), _stream_ptr(stream))
     _check("paged_attn_decode_noalloc", st)
     return out, lse
+
+
+def attn_selftest_bounded_wait(stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (its wait runs out after about 2 s)."""
+    _check("attn_selftest_bounded_wait", load_library().attn_selftest_bounded_wait(_stream_ptr(stream)))
 
 
 def attn_check_device_status(stream=None) -> int:

@@ -42,10 +42,11 @@ int device_setup(int **status_out) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-int prefill_checks(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
-                   int Nkv, int d, int causal, float scale, const int32_t *kv_lens) {
+int prefill_checks(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
+                   int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens) {
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;  // finite, positive
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
@@ -60,17 +61,23 @@ int prefill_checks(const void *q, const void *k, const void *v, void *o, float *
 
 }  // namespace
 
-ATTN_API int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                            int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens,
-                            attn_stream_t stream) {
-    int st = prefill_checks(q, k, v, o, lse, B, H, Nq, Nkv, d, causal, scale, kv_lens);
+ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                          int Hkv, int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens,
+                          attn_stream_t stream) {
+    int st = prefill_checks(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, causal, scale, kv_lens);
     if (st != ATTN_OK) return st;
     int *status = nullptr;
     st = device_setup(&status);
     if (st != ATTN_OK) return st;
-    attn::PrefillArgs a{q, k, v, o, lse, kv_lens, status, B, H, Nq, Nkv, d, causal, scale};
+    attn::PrefillArgs a{q, k, v, o, lse, kv_lens, status, B, Hq, Nq, Nkv, d, causal, scale, Hkv};
     cudaError_t e = attn::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                            int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens,
+                            attn_stream_t stream) {
+    return attn_fwd_gqa(q, k, v, o, lse, B, H, H, Nq, Nkv, d, causal, scale, kv_lens, stream);
 }
 
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
@@ -82,13 +89,14 @@ ATTN_API size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pa
     return attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
 }
 
-ATTN_API int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
-                               const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int d,
-                               int max_pages_per_seq, int num_pages, float scale, void *workspace,
-                               size_t workspace_bytes, attn_stream_t stream) {
+ATTN_API int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_pages,
+                                   const int32_t *page_table, const int32_t *ctx_lens, int page_size, void *o,
+                                   float *lse, int B, int H, int Hkv, int d, int max_pages_per_seq, int num_pages,
+                                   float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
     if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
         return ATTN_ERR_INVALID_ARG;
+    if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
@@ -102,9 +110,17 @@ ATTN_API int paged_attn_decode(const void *q, const void *k_pages, const void *v
     int st = device_setup(&status);
     if (st != ATTN_OK) return st;
     attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, workspace, status, B, H, d, page_size,
-                       max_pages_per_seq, num_pages, scale};
+                       max_pages_per_seq, num_pages, scale, Hkv};
     cudaError_t e = attn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                               const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int d,
+                               int max_pages_per_seq, int num_pages, float scale, void *workspace,
+                               size_t workspace_bytes, attn_stream_t stream) {
+    return paged_attn_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, page_size, o, lse, B, H, H, d,
+                                 max_pages_per_seq, num_pages, scale, workspace, workspace_bytes, stream);
 }
 
 // Decode with the chunk partials in the library's static scratch array (decode.cu);
@@ -130,9 +146,17 @@ ATTN_API int paged_attn_decode_noalloc(const void *q, const void *k_pages, const
     int st = device_setup(&status);
     if (st != ATTN_OK) return st;
     attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, nullptr, status, B, H, d, page_size,
-                       max_pages_per_seq, num_pages, scale};
+                       max_pages_per_seq, num_pages, scale, H};
     cudaError_t e = attn::launch_decode_noalloc(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int attn_selftest_bounded_wait(attn_stream_t stream) {
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    return attn::launch_selftest_wait(status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                     : ATTN_ERR_CUDA;
 }
 
 ATTN_API int attn_check_device_status(attn_stream_t stream) {

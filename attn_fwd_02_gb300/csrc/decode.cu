@@ -33,14 +33,14 @@ constexpr int kPS = 16;    // page size (tokens)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+template <int D, int GP>
 struct DecodeSmem {
     // [warp][slot][0 = K, 1 = V][kPS * D] bf16; each block is 16-byte aligned
     alignas(128) __nv_bfloat16 kv[kWarps][kSlots][2][kPS * D];
     uint64_t full[kWarps][kSlots];
-    float red_o[kWarps][D];
-    float red_m[kWarps];
-    float red_l[kWarps];
+    float red_o[kWarps][GP][D];
+    float red_m[kWarps][GP];
+    float red_l[kWarps][GP];
     int abort_flag;
 };
 
@@ -81,14 +81,82 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits) {
+// Loads DPL consecutive bf16 of global memory (the query) as fp32 scaled by c.
+template <int DPL>
+__device__ __forceinline__ void load_q(const __nv_bfloat16 *qp, float c, float (&qf)[DPL]) {
+    float t[DPL];
+    if constexpr (DPL == 4) {
+        uint2 u = *reinterpret_cast<const uint2 *>(qp);
+        t[0] = __uint_as_float(u.x << 16);
+        t[1] = __uint_as_float(u.x & 0xffff0000u);
+        t[2] = __uint_as_float(u.y << 16);
+        t[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+        uint32_t u = *reinterpret_cast<const uint32_t *>(qp);
+        t[0] = __uint_as_float(u << 16);
+        t[1] = __uint_as_float(u & 0xffff0000u);
+    }
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) qf[i] = t[i] * c;
+}
+
+// Sum of part[t] over the 32 lanes for the 16 tokens t, as a reduce-scatter: afterwards lane
+// L holds the full sum for token L >> 1 (lanes 2t, 2t+1 hold the same value).  16 shuffles.
+__device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int lane) {
+    float r8[8];
+    {
+        const bool up = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = up ? part[i] : part[i + 8];
+            const float keep = up ? part[i + 8] : part[i];
+            r8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+    }
+    float r4[4];
+    {
+        const bool up = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float send = up ? r8[i] : r8[i + 4];
+            const float keep = up ? r8[i + 4] : r8[i];
+            r4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
+    float r2[2];
+    {
+        const bool up = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float send = up ? r4[i] : r4[i + 2];
+            const float keep = up ? r4[i + 2] : r4[i];
+            r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+    }
+    float x;
+    {
+        const bool up = lane & 2;
+        const float send = up ? r2[0] : r2[1];
+        const float keep = up ? r2[1] : r2[0];
+        x = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return x + __shfl_xor_sync(0xffffffffu, x, 1);
+}
+
+// One CTA: one chunk of one sequence's cache for one key/value head, applied to GP query
+// heads that share that head (grouped-query attention; GP = 1 for multi-head attention).
+// Grid (chunks, Hkv * gsplit, B): blockIdx.y = kv_head * gsplit + group slice.
+template <int D, int GP>
+__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits, int Hkv,
+                                                                   int gsplit) {
     constexpr int DPL = D / 32;  // head dims per lane
     constexpr uint32_t kBlockBytes = kPS * D * 2;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    DecodeSmem<D> &sm = *reinterpret_cast<DecodeSmem<D> *>(smem_raw);
+    DecodeSmem<D, GP> &sm = *reinterpret_cast<DecodeSmem<D, GP> *>(smem_raw);
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int kvh = (int)blockIdx.y / gsplit;
+    const int qh0 = kvh * (a.H / Hkv) + ((int)blockIdx.y % gsplit) * GP;  // first query head
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cap = a.max_pages * kPS;
     const int ctx = min(max(a.ctx_lens[b], 0), cap);
@@ -121,7 +189,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         if (lane == 0) {
             uint64_t *bar = &sm.full[warp][k % kSlots];
             if (ok) {
-                const size_t off = ((size_t)pid * a.H + h) * (size_t)(kPS * D);
+                const size_t off = ((size_t)pid * Hkv + kvh) * (size_t)(kPS * D);
                 mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
                 bulk_load(sm.kv[warp][k % kSlots][0], kbase + off, kBlockBytes, bar);
                 bulk_load(sm.kv[warp][k % kSlots][1], vbase + off, kBlockBytes, bar);
@@ -133,31 +201,22 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     const int first = nk < kSlots ? nk : kSlots;
     for (int k = 0; k < first; ++k) issue(k);
 
-    // Query, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k
+    // Queries, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k
     const float c = a.scale * kLog2e;
-    float qf[DPL];
-    {
-        const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * a.H + h) * D;
-        float t[DPL];
-        if constexpr (DPL == 4) {
-            uint2 u = *reinterpret_cast<const uint2 *>(qp + lane * DPL);
-            t[0] = __uint_as_float(u.x << 16);
-            t[1] = __uint_as_float(u.x & 0xffff0000u);
-            t[2] = __uint_as_float(u.y << 16);
-            t[3] = __uint_as_float(u.y & 0xffff0000u);
-        } else {
-            uint32_t u = *reinterpret_cast<const uint32_t *>(qp + lane * DPL);
-            t[0] = __uint_as_float(u << 16);
-            t[1] = __uint_as_float(u & 0xffff0000u);
-        }
+    float qf[GP][DPL];
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) qf[i] = t[i] * c;
-    }
+    for (int g = 0; g < GP; ++g)
+        load_q<DPL>(reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * a.H + qh0 + g) * D + lane * DPL, c,
+                    qf[g]);
 
-    float m_run = -INFINITY, l_run = 0.f;
-    float o[DPL];
+    float m_run[GP], l_run[GP], o[GP][DPL];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    for (int g = 0; g < GP; ++g) {
+        m_run[g] = -INFINITY;
+        l_run[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
+    }
 
     int issued = first;
     bool failed = false;
@@ -173,73 +232,40 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         if (ok) {
             const __nv_bfloat16 *Ks = sm.kv[warp][slot][0];
             const __nv_bfloat16 *Vs = sm.kv[warp][slot][1];
-            // partial dot products of the 16 tokens over this lane's DPL dims
-            float part[16];
+            // this lane's DPL dims of the 16 keys, read once and used for every query head
+            float kf[16][DPL];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                float kf[DPL];
-                load_bf16<DPL>(Ks + t * D + lane * DPL, kf);
-                float acc = 0.f;
+            for (int t = 0; t < 16; ++t) load_bf16<DPL>(Ks + t * D + lane * DPL, kf[t]);
+            float p[GP];  // lane L: probability of token L >> 1, per query head
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) acc = fmaf(qf[i], kf[i], acc);
-                part[t] = acc;
-            }
-            // reduce-scatter over the 32 lanes: afterwards lane L holds the full
-            // score of token L >> 1 (lanes 2t, 2t+1 hold the same value)
-            float r8[8];
-            {
-                const bool up = lane & 16;
+            for (int g = 0; g < GP; ++g) {
+                float part[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float send = up ? part[i] : part[i + 8];
-                    const float keep = up ? part[i + 8] : part[i];
-                    r8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                for (int t = 0; t < 16; ++t) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) acc = fmaf(qf[g][i], kf[t][i], acc);
+                    part[t] = acc;
                 }
-            }
-            float r4[4];
-            {
-                const bool up = lane & 8;
+                float x = reduce_scatter16(part, lane);
+                if ((lane >> 1) >= ntok) x = -INFINITY;  // slots past the context end
+                const float m_new = fmaxf(m_run[g], warp_max_pairs(x));  // finite: ntok >= 1
+                const float alpha = ex2_approx(m_run[g] - m_new);
+                p[g] = ex2_approx(x - m_new);
+                l_run[g] = l_run[g] * alpha + warp_sum_pairs(p[g]);
+                m_run[g] = m_new;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float send = up ? r8[i] : r8[i + 4];
-                    const float keep = up ? r8[i + 4] : r8[i];
-                    r4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                }
+                for (int i = 0; i < DPL; ++i) o[g][i] *= alpha;
             }
-            float r2[2];
-            {
-                const bool up = lane & 4;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float send = up ? r4[i] : r4[i + 2];
-                    const float keep = up ? r4[i + 2] : r4[i];
-                    r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-                }
-            }
-            float x;
-            {
-                const bool up = lane & 2;
-                const float send = up ? r2[0] : r2[1];
-                const float keep = up ? r2[1] : r2[0];
-                x = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-            }
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
-            if ((lane >> 1) >= ntok) x = -INFINITY;  // slots past the context end
-
-            const float m_page = warp_max_pairs(x);
-            const float m_new = fmaxf(m_run, m_page);  // finite: ntok >= 1
-            const float alpha = ex2_approx(m_run - m_new);
-            const float p = ex2_approx(x - m_new);
-            l_run = l_run * alpha + warp_sum_pairs(p);
-            m_run = m_new;
-#pragma unroll
-            for (int i = 0; i < DPL; ++i) o[i] *= alpha;
             for (int t = 0; t < ntok; ++t) {
-                const float pt = __shfl_sync(0xffffffffu, p, 2 * t);
                 float vf[DPL];
                 load_bf16<DPL>(Vs + t * D + lane * DPL, vf);
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) o[i] = fmaf(pt, vf[i], o[i]);
+                for (int g = 0; g < GP; ++g) {
+                    const float pt = __shfl_sync(0xffffffffu, p[g], 2 * t);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) o[g][i] = fmaf(pt, vf[i], o[g][i]);
+                }
             }
         }
         // the slot is free again: order this warp's reads before the next bulk write
@@ -254,40 +280,40 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         // drain this warp's copies still in flight (bounded) before the CTA exits
         WaitCtx drain{nullptr, a.status};
         for (int k = 0; k < issued; ++k) {
-            if (lane == 0) {
-                // the last use of each slot is the one that matters
-                if (k + kSlots >= issued) {
-                    (void)mbar_wait(&sm.full[warp][k % kSlots], (uint32_t)((k / kSlots) & 1), drain, 199);
-                }
-            }
+            if (lane == 0 && k + kSlots >= issued)  // the last use of each slot
+                (void)mbar_wait(&sm.full[warp][k % kSlots], (uint32_t)((k / kSlots) & 1), drain, 199);
         }
         __syncwarp();
     }
 
-    // merge the four warp states
-    if (lane == 0) {
-        sm.red_m[warp] = m_run;
-        sm.red_l[warp] = l_run;
-    }
+    // merge the four warp states of every query head
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) sm.red_o[warp][lane * DPL + i] = o[i];
+    for (int g = 0; g < GP; ++g) {
+        if (lane == 0) {
+            sm.red_m[warp][g] = m_run[g];
+            sm.red_l[warp][g] = l_run[g];
+        }
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) sm.red_o[warp][g][lane * DPL + i] = o[g][i];
+    }
     __syncthreads();
     if (sm.abort_flag) return;
-    float *ws = reinterpret_cast<float *>(a.workspace) +
-                (((size_t)b * a.H + h) * max_splits + split) * (size_t)ws_stride<D>();
-    for (int dd = threadIdx.x; dd < D; dd += blockDim.x) {
+    for (int e = threadIdx.x; e < GP * D; e += blockDim.x) {
+        const int g = e / D, dd = e % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w][g]);
         float L = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const float wgt = ex2_approx(sm.red_m[w] - M);
-                L += sm.red_l[w] * wgt;
-                O += sm.red_o[w][dd] * wgt;
+                const float wgt = ex2_approx(sm.red_m[w][g] - M);
+                L += sm.red_l[w][g] * wgt;
+                O += sm.red_o[w][g][dd] * wgt;
             }
         }
+        float *ws = reinterpret_cast<float *>(a.workspace) +
+                    (((size_t)b * a.H + qh0 + g) * max_splits + split) * (size_t)ws_stride<D>();
         ws[dd] = O;
         if (dd == 0) {
             ws[D] = M;
@@ -322,16 +348,28 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, i
     if (dd == 0 && a.lse) a.lse[row] = any ? kLn2 * (M + __log2f(L)) : -INFINITY;
 }
 
+template <int D, int GP>
+cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
+    const size_t smem = sizeof(DecodeSmem<D, GP>);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_split_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int gsplit = (a.H / a.Hkv) / GP;  // CTAs per key/value head
+    dim3 g1(max_splits, a.Hkv * gsplit, a.B);
+    decode_split_kernel<D, GP><<<g1, kWarps * 32, smem, stream>>>(a, max_splits, a.Hkv, gsplit);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     const int max_splits = (a.max_pages * kPS + kDecodeChunkTokens - 1) / kDecodeChunkTokens;
-    const size_t smem = sizeof(DecodeSmem<D>);
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    dim3 g1(max_splits, a.H, a.B);
-    decode_split_kernel<D><<<g1, kWarps * 32, smem, stream>>>(a, max_splits);
-    e = cudaGetLastError();
+    // query heads per CTA: the largest of 8, 4, 2, 1 dividing the group size
+    const int group = a.H / a.Hkv;
+    cudaError_t e;
+    if (group % 8 == 0) e = launch_decode_g<D, 8>(a, max_splits, stream);
+    else if (group % 4 == 0) e = launch_decode_g<D, 4>(a, max_splits, stream);
+    else if (group % 2 == 0) e = launch_decode_g<D, 2>(a, max_splits, stream);
+    else e = launch_decode_g<D, 1>(a, max_splits, stream);
     if (e != cudaSuccess) return e;
     dim3 g2(a.H, a.B);
     decode_combine_kernel<D><<<g2, D, 0, stream>>>(a, max_splits);
@@ -411,4 +449,33 @@ cudaError_t launch_decode_noalloc(const DecodeArgs &a_in, cudaStream_t stream) {
     return launch_decode(a, stream);
 }
 
+}  // namespace attn
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded-wait machinery: one warp waits on an mbarrier that
+// nothing ever arrives on.  The wait gives up after its time limit, raises the
+// device status word (site 250) and the kernel returns; the context stays usable.
+namespace attn {
+namespace {
+__global__ void selftest_wait_kernel(int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        WaitCtx wc{&abort_flag, status};
+        (void)mbar_wait(&bar, 0, wc, 250);
+    }
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(int *status, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
+}
 }  // namespace attn

@@ -17,6 +17,7 @@ struct PrefillArgs {
     int *status;             // device status word [2]
     int B, H, Nq, Nkv, d, causal;
     float scale;
+    int Hkv;                 // key/value heads (H for multi-head; H % Hkv == 0)
 };
 
 struct DecodeArgs {
@@ -28,6 +29,7 @@ struct DecodeArgs {
     int *status;
     int B, H, d, page_size, max_pages, num_pages;
     float scale;
+    int Hkv;  // key/value heads of the cache (H for multi-head; H % Hkv == 0)
 };
 
 // Encodes the TMA descriptors and launches the prefill kernel.
@@ -43,6 +45,9 @@ size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size)
 // (no workspace from the caller); see decode.cu.
 cudaError_t launch_decode_noalloc(const DecodeArgs &a, cudaStream_t stream);
 size_t decode_noalloc_scratch_bytes();
+
+// One block that waits on an mbarrier nobody arrives on (exercises the bounded waits).
+cudaError_t launch_selftest_wait(int *status, cudaStream_t stream);
 
 // Tokens per split of the paged decode.
 constexpr int kDecodeChunkTokens = 512;

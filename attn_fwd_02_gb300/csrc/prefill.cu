@@ -66,6 +66,7 @@ struct PrefillParams {
     const int32_t *kv_lens;
     int *status;
     int B, H, Nq, Nkv, causal, n_units;  // n_units = ceil(Nq / 256) per (b, h)
+    int Hkv, group;                      // key/value heads; query heads per key/value head
     int heads_per_chunk;                 // heads whose K/V share L2 at a time (see the CTA order)
     float scale_log2;
 };
@@ -103,7 +104,7 @@ __device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_
 // ------------------------------------------------------------------ producer
 template <int D>
 __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const CUtensorMap *tmK,
-                             const CUtensorMap *tmV, int bh, int q0, int n_all, WaitCtx wc) {
+                             const CUtensorMap *tmV, int bh, int bh_kv, int q0, int n_all, WaitCtx wc) {
     constexpr int kBoxes = D / 64;
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
@@ -123,12 +124,12 @@ __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const C
         if (has_k) {
 #pragma unroll
             for (int i = 0; i < kBoxes; ++i)
-                tma_load_3d(sm.k[slot] + i * (kBN * 64), tmK, &sm.u_full[slot], i * 64, u * kBN, bh);
+                tma_load_3d(sm.k[slot] + i * (kBN * 64), tmK, &sm.u_full[slot], i * 64, u * kBN, bh_kv);
         }
         if (has_v) {
 #pragma unroll
             for (int i = 0; i < kBoxes; ++i)
-                tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh);
+                tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh_kv);
         }
         ++fills;
     }
@@ -404,6 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int level = in_chunk / heads;  // 0 = heaviest unit of a head
     const int bh = h0 + in_chunk % heads;
     const int unit = p.n_units - 1 - level;
+    // key/value head of this query head (grouped-query attention; = bh for multi-head)
+    const int bh_kv = (bh / p.H) * p.Hkv + (bh % p.H) / p.group;
     const int b = bh / p.H;
     const int q0 = unit * kRowsPerCta;
     int kv_end = p.Nkv;
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 8) {
         setmaxnreg_dec<kRegsOther>();
         if (warp == kProducerWarp) {
-            if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, q0, n_all, wc);
+            if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, bh_kv, q0, n_all, wc);
         } else if (warp == kMmaWarp) {
             if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
         }
@@ -494,9 +497,9 @@ bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D) {
 template <int D>
 cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
-    const int BH = a.B * a.H;
-    if (!encode_qkv_map(&tq, a.q, BH, a.Nq, D) || !encode_qkv_map(&tk, a.k, BH, a.Nkv, D) ||
-        !encode_qkv_map(&tv, a.v, BH, a.Nkv, D))
+    const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
+    if (!encode_qkv_map(&tq, a.q, BH, a.Nq, D) || !encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D) ||
+        !encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D))
         return cudaErrorInvalidValue;
     PrefillParams p;
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
@@ -508,11 +511,13 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.Nq = a.Nq;
     p.Nkv = a.Nkv;
     p.causal = a.causal;
+    p.Hkv = a.Hkv;
+    p.group = a.H / a.Hkv;
     p.n_units = (a.Nq + kRowsPerCta - 1) / kRowsPerCta;
     {
         // about 48 MB of K/V per chunk: two chunks (the one finishing, the one starting) fit
-        // in the 126 MB L2 together
-        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0;
+        // in the 126 MB L2 together.  Query heads of one group share their K/V.
+        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0 / p.group;
         int hpc = (int)(48.0e6 / kv_bytes_per_head);
         p.heads_per_chunk = hpc < 1 ? 1 : (hpc > BH ? BH : hpc);
     }

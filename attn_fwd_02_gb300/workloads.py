@@ -40,10 +40,15 @@ class PrefillShape:
     kv_len_range: tuple[int, int] | None = None  # inclusive [lo, hi]; None = all keys valid
     seed: int = 0
     softmax_scale: float | None = None  # None = 1/sqrt(d)
+    kv_heads: int | None = None  # None = H (multi-head); fewer = grouped-query attention
 
     @property
     def scale(self) -> float:
         return self.softmax_scale if self.softmax_scale is not None else 1.0 / math.sqrt(self.d)
+
+    @property
+    def Hkv(self) -> int:
+        return self.H if self.kv_heads is None else self.kv_heads
 
 
 @dataclasses.dataclass(frozen=True)
@@ -83,12 +88,14 @@ PREFILL_WORKLOADS = (TILE_128x64, ENCODER_PAD, DECODER_CAUSAL, LONG_CAUSAL)
 
 
 def prefill_inputs(shape: PrefillShape):
-    """Return dict(q, k, v, kv_lens) as CPU tensors (bf16 / int32 or None)."""
+    """Return dict(q, k, v, kv_lens) as CPU tensors (bf16 / int32 or None).
+    K and V have shape.kv_heads heads (grouped-query attention) when it is set."""
     g = torch.Generator().manual_seed(shape.seed)
     B, H, Nq, Nkv, d = shape.B, shape.H, shape.Nq, shape.Nkv, shape.d
+    Hkv = shape.Hkv
     q = (torch.randn(B, H, Nq, d, generator=g) * shape.value_scale).to(torch.bfloat16)
-    k = (torch.randn(B, H, Nkv, d, generator=g) * shape.value_scale).to(torch.bfloat16)
-    v = (torch.randn(B, H, Nkv, d, generator=g) * shape.value_scale).to(torch.bfloat16)
+    k = (torch.randn(B, Hkv, Nkv, d, generator=g) * shape.value_scale).to(torch.bfloat16)
+    v = (torch.randn(B, Hkv, Nkv, d, generator=g) * shape.value_scale).to(torch.bfloat16)
     kv_lens = None
     if shape.kv_len_range is not None:
         lo, hi = shape.kv_len_range
@@ -99,13 +106,17 @@ def prefill_inputs(shape: PrefillShape):
 POISON_VALUE = 3.0e4
 
 
-def decode_inputs(shape: DecodeShape, ctx_lens=None):
+def decode_inputs(shape: DecodeShape, ctx_lens=None, kv_heads=None):
     """Return dict(q, k_pages, v_pages, page_table, ctx_lens) as CPU tensors.
 
     ``ctx_lens`` (optional list) overrides the drawn context lengths (for edge cases).
-    The poison page is the last physical page."""
+    ``kv_heads`` (optional) gives the cache fewer heads than the query (grouped-query
+    attention; shape.H must be a multiple of it).  The poison page is the last physical page."""
     g = torch.Generator().manual_seed(shape.seed)
     B, H, d, ps = shape.B, shape.H, shape.d, shape.page_size
+    Hkv = H if kv_heads is None else kv_heads
+    if H % Hkv:
+        raise ValueError("query heads must be a multiple of the cache heads")
     lo, hi = shape.ctx_range
     drawn = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64)
     cl = drawn if ctx_lens is None else torch.tensor(list(ctx_lens), dtype=torch.int64)
@@ -121,8 +132,8 @@ def decode_inputs(shape: DecodeShape, ctx_lens=None):
         table[b, :n] = perm[off:off + n]
         off += n
     num_pages = used + 1
-    k = torch.randn(num_pages, H, ps, d, generator=g).to(torch.bfloat16)
-    v = torch.randn(num_pages, H, ps, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(num_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(num_pages, Hkv, ps, d, generator=g).to(torch.bfloat16)
     k[poison] = POISON_VALUE
     v[poison] = POISON_VALUE
     for b, c in enumerate(cl.tolist()):

@@ -96,6 +96,18 @@ int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o, float *
                    const int32_t *kv_lens, attn_stream_t stream);
 
 /*
+ * Prefill forward with grouped-query (or multi-query) attention: Hq query heads
+ * share Hkv key/value heads, query head h reading key/value head h / (Hq / Hkv)
+ * (the MHA / GQA / MQA variants compared in the llm-kernel-lib README's
+ * attention ablation).  q, o [B, Hq, Nq, d]; k, v [B, Hkv, Nkv, d]; lse
+ * [B, Hq, Nq]; Hq % Hkv == 0 (else ATTN_ERR_INVALID_ARG).  Hkv == Hq is
+ * attn_fwd_kvlen.  Other arguments as attn_fwd_kvlen.
+ */
+int attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal, float scale,
+                 const int32_t *kv_lens, attn_stream_t stream);
+
+/*
  * Bytes of device workspace paged_attn_decode needs for these sizes (0 on
  * invalid sizes).  The caller allocates it (16-byte aligned) and may reuse it
  * across calls on the same stream; calls that overlap on the GPU need
@@ -122,6 +134,20 @@ int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages,
                       void *o, float *lse, int B, int H, int d, int max_pages_per_seq,
                       int num_pages, float scale, void *workspace, size_t workspace_bytes,
                       attn_stream_t stream);
+
+/*
+ * Paged decode with grouped-query attention: the cache has Hkv heads
+ * (k_pages, v_pages [num_pages, Hkv, page_size, d]) shared by the H query heads
+ * (q, o [B, H, d]; lse [B, H]); query head h reads cache head h / (H / Hkv), and
+ * each cache page is read once for all the query heads that share it.  H % Hkv
+ * must be 0.  The workspace is sized by paged_attn_decode_workspace_size(B, H,
+ * ...) with H the number of query heads.  Other arguments as paged_attn_decode.
+ */
+int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                          void *o, float *lse, int B, int H, int Hkv, int d, int max_pages_per_seq,
+                          int num_pages, float scale, void *workspace, size_t workspace_bytes,
+                          attn_stream_t stream);
 
 /*
  * paged_attn_decode for callers that cannot allocate device memory.  The pages
@@ -155,6 +181,16 @@ int paged_attn_decode_noalloc(const void *q, const void *k_pages, const void *v_
  * the last check, or ATTN_ERR_CUDA if the synchronisation itself failed.
  */
 int attn_check_device_status(attn_stream_t stream);
+
+/*
+ * Self-test of the failure detection: launches one block whose only thread waits
+ * on an mbarrier that nothing arrives on.  The wait gives up after its limit
+ * (about two seconds), records ATTN_ERR_DEVICE_TIMEOUT in the device status word
+ * and the kernel returns normally, so the CUDA context stays usable.  The next
+ * attn_check_device_status() on this stream returns ATTN_ERR_DEVICE_TIMEOUT.
+ * Returns ATTN_OK if the launch succeeded.
+ */
+int attn_selftest_bounded_wait(attn_stream_t stream);
 
 /* Static, human-readable text for a status code. */
 const char *attn_status_string(int status);

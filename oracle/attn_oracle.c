@@ -104,12 +104,18 @@ static int key_valid(int i, int j, int Nq, int Nkv, int kv_len, int causal) {
     return 1;
 }
 
-/* Rows selected by flat index r = (b*H + h)*Nq + i.  o_rows [nrows,d], lse_rows [nrows]. */
-int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                         const int32_t *kv_lens, int B, int H, int Nq, int Nkv, int d,
-                         int causal, double scale, const int64_t *rows, int64_t nrows,
-                         double *o_rows, double *lse_rows, int nthreads) {
-    if (B <= 0 || H <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0 || nrows < 0) return 1;
+/* Grouped-query form (grouped-query / multi-query attention, the variants compared in the
+ * llm-kernel-lib README's attention ablation): Hq query heads share Hkv key/value heads,
+ * query head h reading key/value head h / (Hq / Hkv).  q [B,Hq,Nq,d], k/v [B,Hkv,Nkv,d].
+ * Rows are selected by flat index r = (b*Hq + h)*Nq + i.  o_rows [nrows,d], lse_rows [nrows].
+ * Hkv == Hq is ordinary multi-head attention. */
+int oracle_attn_gqa_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const int32_t *kv_lens, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                             int causal, double scale, const int64_t *rows, int64_t nrows,
+                             double *o_rows, double *lse_rows, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || Nkv <= 0 || d <= 0 || nrows < 0)
+        return 1;
+    const int group = Hq / Hkv;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #else
@@ -127,17 +133,18 @@ int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v
 #pragma omp for schedule(dynamic, 4)
             for (int64_t t = 0; t < nrows; ++t) {
                 int64_t r = rows[t];
-                if (r < 0 || r >= (int64_t)B * H * Nq) {
+                if (r < 0 || r >= (int64_t)B * Hq * Nq) {
 #pragma omp atomic write
                     err = 1;
                     continue;
                 }
                 int i = (int)(r % Nq);
                 int64_t bh = r / Nq;
-                int b = (int)(bh / H);
+                int b = (int)(bh / Hq), h = (int)(bh % Hq);
+                int64_t bhkv = (int64_t)b * Hkv + h / group;
                 int kv_len = kv_lens ? kv_lens[b] : Nkv;
                 for (int j = 0; j < Nkv; ++j) valid[j] = (unsigned char)key_valid(i, j, Nq, Nkv, kv_len, causal);
-                attend_row(q + (size_t)r * d, k + (size_t)bh * Nkv * d, v + (size_t)bh * Nkv * d,
+                attend_row(q + (size_t)r * d, k + (size_t)bhkv * Nkv * d, v + (size_t)bhkv * Nkv * d,
                            valid, Nkv, d, scale, srow, o_rows + (size_t)t * d, lse_rows + t);
             }
         }
@@ -145,6 +152,15 @@ int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v
         free(valid);
     }
     return err;
+}
+
+/* Rows selected by flat index r = (b*H + h)*Nq + i (multi-head: Hkv = H). */
+int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const int32_t *kv_lens, int B, int H, int Nq, int Nkv, int d,
+                         int causal, double scale, const int64_t *rows, int64_t nrows,
+                         double *o_rows, double *lse_rows, int nthreads) {
+    return oracle_attn_gqa_rows_f64(q, k, v, kv_lens, B, H, H, Nq, Nkv, d, causal, scale, rows, nrows,
+                                    o_rows, lse_rows, nthreads);
 }
 
 /* Every row: o [B,H,Nq,d], lse [B,H,Nq]. */
@@ -162,12 +178,16 @@ int oracle_attn_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return err;
 }
 
-/* Paged decode: o [B,H,d], lse [B,H]. */
-int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
-                            const int32_t *page_table, const int32_t *ctx_lens, int page_size,
-                            int B, int H, int d, int max_pages, int num_pages, double scale,
-                            double *o, double *lse, int nthreads) {
-    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0) return 1;
+/* Paged decode, grouped-query form: q [B,Hq,d]; k_pages/v_pages [num_pages,Hkv,page_size,d];
+ * query head h reads key/value head h / (Hq / Hkv).  o [B,Hq,d], lse [B,Hq]. */
+int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                                const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                                int B, int Hq, int Hkv, int d, int max_pages, int num_pages, double scale,
+                                double *o, double *lse, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 || max_pages <= 0 ||
+        num_pages <= 0)
+        return 1;
+    const int H = Hq, group = Hq / Hkv;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #else
@@ -200,7 +220,7 @@ int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const ui
                 for (int t = 0; t < n; ++t) {
                     int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
                     if (pg < 0 || pg >= num_pages) { bad = 1; break; }
-                    size_t src = (((size_t)pg * H + h) * page_size + (size_t)(t % page_size)) * d;
+                    size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
                     memcpy(kc + (size_t)t * d, k_pages + src, sizeof(uint16_t) * (size_t)d);
                     memcpy(vc + (size_t)t * d, v_pages + src, sizeof(uint16_t) * (size_t)d);
                 }
@@ -220,6 +240,15 @@ int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const ui
         free(valid);
     }
     return err;
+}
+
+/* Paged decode, multi-head (Hkv = H): o [B,H,d], lse [B,H]. */
+int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                            const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                            int B, int H, int d, int max_pages, int num_pages, double scale,
+                            double *o, double *lse, int nthreads) {
+    return oracle_paged_decode_gqa_f64(q, k_pages, v_pages, page_table, ctx_lens, page_size, B, H, H, d,
+                                       max_pages, num_pages, scale, o, lse, nthreads);
 }
 
 /* Number of threads OpenMP would use (for reporting the CPU baseline's cores). */

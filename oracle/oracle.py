@@ -67,6 +67,12 @@ def _load():
             lib.oracle_paged_decode_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I,
                                                     ctypes.c_double, P, P, I]
             lib.oracle_num_threads.argtypes = [I]
+            lib.oracle_attn_gqa_rows_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+                                                     P, ctypes.c_int64, P, P, I]
+            lib.oracle_paged_decode_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I,
+                                                        ctypes.c_double, P, P, I]
+            lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
+            lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
             for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
                       lib.oracle_paged_decode_f64, lib.oracle_num_threads):
                 f.restype = ctypes.c_int
@@ -171,4 +177,44 @@ def paged_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nthrea
                                           nthreads)
     if err:
         raise RuntimeError(f"oracle_paged_decode_f64 failed ({err})")
+    return o, lse
+
+
+def attn_fwd_gqa(q, k, v, causal: bool, scale: float, kv_lens=None, nthreads: int = 0):
+    """Grouped-query prefill: q [B,Hq,Nq,d], k/v [B,Hkv,Nkv,d] bf16, Hq % Hkv == 0; query head h
+    reads key/value head h // (Hq // Hkv).  Returns (O [B,Hq,Nq,d], LSE [B,Hq,Nq]) in float64."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    B, Hq, Nq, d = qb.shape
+    Hkv, Nkv = kb.shape[1], kb.shape[2]
+    if kb.shape != (B, Hkv, Nkv, d) or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    kl = _i32(kv_lens)
+    rows = np.arange(B * Hq * Nq, dtype=np.int64)
+    o = np.empty((B * Hq * Nq, d), np.float64)
+    lse = np.empty((B * Hq * Nq,), np.float64)
+    err = _load().oracle_attn_gqa_rows_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(kl), B, Hq, Hkv, Nq, Nkv, d,
+                                           int(bool(causal)), float(scale), _ptr(rows), len(rows), _ptr(o),
+                                           _ptr(lse), nthreads)
+    if err:
+        raise RuntimeError(f"oracle_attn_gqa_rows_f64 failed ({err})")
+    return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
+
+
+def paged_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nthreads: int = 0):
+    """Grouped-query paged decode: q [B,Hq,d]; k_pages/v_pages [P,Hkv,page_size,d].
+    Returns (O [B,Hq,d], LSE [B,Hq]) in float64."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k_pages), bf16_bits(v_pages)
+    B, Hq, d = qb.shape
+    P, Hkv, ps, dk = kb.shape
+    if dk != d or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    pt = _i32(page_table)
+    cl = _i32(ctx_lens)
+    o = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    err = _load().oracle_paged_decode_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(cl), ps, B, Hq,
+                                              Hkv, d, pt.shape[1], P, float(scale), _ptr(o), _ptr(lse),
+                                              nthreads)
+    if err:
+        raise RuntimeError(f"oracle_paged_decode_gqa_f64 failed ({err})")
     return o, lse

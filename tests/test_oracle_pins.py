@@ -325,3 +325,75 @@ def test_planted_mistakes_are_caught(oracle_mod, tmp_path):
         assert np.allclose(good_l, ref_l.numpy(), atol=1e-12)
         caught = (not np.allclose(o, ref.numpy(), atol=1e-9)) or (not np.allclose(l, ref_l.numpy(), atol=1e-9))
         assert caught, f"planted mistake {name} not caught"
+
+
+# ----------------------------------------------------------------------------- grouped-query
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (6, 1), (4, 4)])
+def test_gqa_equals_mha_on_repeated_kv(oracle_mod, Hq, Hkv):
+    # grouped-query attention shares each K/V head among Hq/Hkv consecutive query heads:
+    # it must equal multi-head attention on K/V repeated along the head axis
+    B, N, d = 2, 33, 16
+    q = rand_bf16((B, Hq, N, d), 50)
+    k = rand_bf16((B, Hkv, N, d), 51)
+    v = rand_bf16((B, Hkv, N, d), 52)
+    kl = np.array([33, 20], np.int32)
+    rep = Hq // Hkv
+    for causal in (False, True):
+        o, lse = oracle_mod.attn_fwd_gqa(q, k, v, causal, 0.25, kv_lens=kl)
+        om, lm = oracle_mod.attn_fwd(q, k.repeat_interleave(rep, dim=1).contiguous(),
+                                     v.repeat_interleave(rep, dim=1).contiguous(), causal, 0.25, kv_lens=kl)
+        np.testing.assert_array_equal(o, om)
+        np.testing.assert_array_equal(lse, lm)
+
+
+def test_gqa_against_torch_sdpa_fp64(oracle_mod):
+    B, Hq, Hkv, N, d = 2, 8, 2, 29, 32
+    q, k, v = rand_bf16((B, Hq, N, d), 53), rand_bf16((B, Hkv, N, d), 54), rand_bf16((B, Hkv, N, d), 55)
+    o, lse = oracle_mod.attn_fwd_gqa(q, k, v, True, 0.2)
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, is_causal=True, scale=0.2, enable_gqa=True)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_paged_gqa_equals_contiguous_gqa(oracle_mod):
+    shape = workloads.DecodeShape("t", 3, 8, 16, (1, 70), page_size=16, seed=9)
+    inp = workloads.decode_inputs(shape, ctx_lens=[5, 70, 33], kv_heads=2)
+    o, lse = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                         inp["ctx_lens"], 0.3)
+    ps = 16
+    for b, n in enumerate(inp["ctx_lens"].tolist()):
+        pages = inp["page_table"][b, : (n + ps - 1) // ps].long()
+        kc = inp["k_pages"][pages].permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+        vc = inp["v_pages"][pages].permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+        oc, lc = oracle_mod.attn_fwd_gqa(inp["q"][b][None, :, None].contiguous(), kc[None].contiguous(),
+                                         vc[None].contiguous(), False, 0.3)
+        np.testing.assert_array_equal(o[b], oc[0, :, 0])
+        np.testing.assert_array_equal(lse[b], lc[0, :, 0])
+
+
+def test_planted_gqa_head_mapping_mistake_is_caught(oracle_mod, tmp_path):
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle_mod.__file__), "attn_oracle.c")).read()
+    a = "int64_t bhkv = (int64_t)b * Hkv + h / group;"
+    assert a in src
+    path = tmp_path / "m.c"
+    path.write_text(src.replace(a, "int64_t bhkv = (int64_t)b * Hkv + h % Hkv;", 1))
+    so = tmp_path / "m.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-o", str(so), str(path), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_attn_gqa_rows_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, P, ctypes.c_int64,
+                                             P, P, I]
+    B, Hq, Hkv, N, d = 1, 8, 2, 12, 16
+    q, k, v = rand_bf16((B, Hq, N, d), 56), rand_bf16((B, Hkv, N, d), 57), rand_bf16((B, Hkv, N, d), 58)
+    rows = np.arange(B * Hq * N, dtype=np.int64)
+    o = np.empty((len(rows), d))
+    l = np.empty(len(rows))
+    qb, kb, vb = (oracle_mod.bf16_bits(t) for t in (q, k, v))
+    lib.oracle_attn_gqa_rows_f64(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, None, B, Hq, Hkv, N, N, d, 0,
+                                 0.25, rows.ctypes.data, len(rows), o.ctypes.data, l.ctypes.data, 1)
+    qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, scale=0.25, enable_gqa=True)
+    assert not np.allclose(o.reshape(B, Hq, N, d), ref.numpy(), atol=1e-6)
