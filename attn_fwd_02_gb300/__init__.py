@@ -17,5 +17,7 @@ from .binding import (  # noqa: F401
     paged_attn_decode,
     paged_attn_decode_gqa,
     paged_attn_decode_noalloc,
+    paged_attn_prefill,
+    paged_kv_append,
     paged_attn_decode_workspace_size,
 )

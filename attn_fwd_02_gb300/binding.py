@@ -34,6 +34,8 @@ SIGNATURES = {
     "paged_attn_decode": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P, Z, P]),
     "paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P]),
     "paged_attn_decode_gqa": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
+    "paged_attn_prefill": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P]),
+    "paged_kv_append": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, P]),
     "attn_check_device_status": (I, [P]),
     "attn_selftest_bounded_wait": (I, [P]),
     "attn_status_string": (ctypes.c_char_p, [I]),
@@ -285,6 +287,57 @@ def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: 
         _dptr(lse), B, H, d, page_table.shape[1], num_pages, float(scale), _stream_ptr(stream))
     _check("paged_attn_decode_noalloc", st)
     return out, lse
+
+
+def paged_attn_prefill(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, scale: float | None = None,
+                       out=None, lse=None, return_lse: bool = True, stream=None):
+    """Chunked prefill over the paged cache: q [B,H,Nq,d] are the last Nq of the ctx_lens[b]
+    cached tokens of each sequence; k_pages/v_pages [P,Hkv,page_size,d]; page_table
+    [B,max_pages] int32; ctx_lens [B] int32 (all CUDA).  Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 4)
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, Nq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages must be [num_pages, Hkv, page_size, d] matching q")
+    if page_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    st = load_library().paged_attn_prefill(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table),
+                                           _dptr(ctx_lens), page_size, _dptr(out), _dptr(lse), B, H, Hkv, Nq, d,
+                                           page_table.shape[1], num_pages, int(bool(causal)), float(scale),
+                                           _stream_ptr(stream))
+    _check("paged_attn_prefill", st)
+    return out, lse
+
+
+def paged_kv_append(k_new, v_new, k_pages, v_pages, page_table, start_pos, stream=None) -> None:
+    """Write new tokens' K/V ([B,Hkv,Nnew,d] bf16) into the pages at positions start_pos[b] + t."""
+    import torch
+    _require(k_new, "k_new", torch.bfloat16, 4)
+    _require(v_new, "v_new", torch.bfloat16, 4)
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(start_pos, "start_pos", torch.int32, 1)
+    B, Hkv, Nnew, d = k_new.shape
+    num_pages, Hk, page_size, dk = k_pages.shape
+    if (Hk, dk) != (Hkv, d) or tuple(v_new.shape) != tuple(k_new.shape) or tuple(v_pages.shape) != tuple(
+            k_pages.shape):
+        raise ValueError("shape mismatch between new K/V and the pages")
+    st = load_library().paged_kv_append(_dptr(k_new), _dptr(v_new), _dptr(k_pages), _dptr(v_pages),
+                                        _dptr(page_table), _dptr(start_pos), page_size, B, Hkv, Nnew, d,
+                                        page_table.shape[1], num_pages, _stream_ptr(stream))
+    _check("paged_kv_append", st)
 
 
 def attn_selftest_bounded_wait(stream=None) -> None:

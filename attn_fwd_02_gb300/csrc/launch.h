@@ -18,6 +18,11 @@ struct PrefillArgs {
     int B, H, Nq, Nkv, d, causal;
     float scale;
     int Hkv;                 // key/value heads (H for multi-head; H % Hkv == 0)
+    // paged mode: k, v are [num_pages, Hkv, 16, d] pages through page_table [B, max_pages];
+    // ctx_lens[b] cached tokens, the queries being the last Nq of them; Nkv = capacity
+    int paged = 0;
+    const int32_t *page_table = nullptr, *ctx_lens = nullptr;
+    int max_pages = 0, num_pages = 0;
 };
 
 struct DecodeArgs {
@@ -34,6 +39,12 @@ struct DecodeArgs {
 
 // Encodes the TMA descriptors and launches the prefill kernel.
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Writes new tokens' K/V into their pages (token t of sequence b goes to position
+// start_pos[b] + t).  Positions past the table's capacity are skipped.
+cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                             const int32_t *page_table, const int32_t *start_pos, int B, int Hkv, int Nnew, int d,
+                             int max_pages, int num_pages, cudaStream_t stream);
 
 // Launches the split kernel and the combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

@@ -59,6 +59,7 @@ constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 bo
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr int kPageTokens = 16;            // tokens per page of the paged KV cache
 
 struct PrefillParams {
     __nv_bfloat16 *o;
@@ -67,6 +68,11 @@ struct PrefillParams {
     int *status;
     int B, H, Nq, Nkv, causal, n_units;  // n_units = ceil(Nq / 256) per (b, h)
     int Hkv, group;                      // key/value heads; query heads per key/value head
+    // paged mode (chunked prefill into a paged KV cache): K/V come from 16-token pages
+    // [num_pages, Hkv, 16, d] found through page_table [B, max_pages]; sequence b holds
+    // ctx_lens[b] tokens and the queries are its last Nq positions
+    const int32_t *page_table, *ctx_lens;
+    int paged, max_pages, num_pages;
     int heads_per_chunk;                 // heads whose K/V share L2 at a time (see the CTA order)
     float scale_log2;
 };
@@ -93,18 +99,24 @@ struct alignas(1024) PrefillSmem {
     int abort_flag;
 };
 
+// Cached tokens of sequence b in paged mode (clamped to the table's capacity).
+__device__ __forceinline__ int kv_end_of(const PrefillParams &p, int b) {
+    return min(max(p.ctx_lens[b], 0), p.max_pages * kPageTokens);
+}
+
 // Key tiles query tile t of this CTA must visit: keys < limit can be valid for some of its rows.
-__device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_end) {
+__device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_end, int delta) {
     if (qs >= p.Nq) return 0;  // no rows in this tile (ragged end)
     int limit = kv_end;
-    if (p.causal) limit = min(limit, min(qs + kBM, p.Nq) + (p.Nkv - p.Nq));
+    if (p.causal) limit = min(limit, min(qs + kBM, p.Nq) + delta);
     return limit > 0 ? (limit + kBN - 1) / kBN : 0;
 }
 
 // ------------------------------------------------------------------ producer
 template <int D>
-__device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const CUtensorMap *tmK,
-                             const CUtensorMap *tmV, int bh, int bh_kv, int q0, int n_all, WaitCtx wc) {
+__device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
+                             const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int bh, int bh_kv, int q0,
+                             int n_all, WaitCtx wc) {
     constexpr int kBoxes = D / 64;
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
@@ -115,21 +127,66 @@ __device__ void run_producer(PrefillSmem<D> &sm, const CUtensorMap *tmQ, const C
 #pragma unroll
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
+    // paged mode: pool row (page * Hkv + head) of each page of a tile; pages past the
+    // sequence's last page, or with an id outside the pool, get an out-of-range row, which
+    // TMA reads as zeros
+    constexpr int kTilePages = kBN / kPageTokens;
+    const int kvh = bh_kv % p.Hkv;
+    const int pages_used = p.paged ? (kv_end_of(p, b) + kPageTokens - 1) / kPageTokens : 0;
+    // raw page ids (-1 past the last page); they are only read when the tile is loaded, one
+    // unit later, so the global loads stay in flight across the ring wait
+    auto fetch_rows = [&](int tile, int (&ids)[kTilePages]) {
+#pragma unroll
+        for (int pg = 0; pg < kTilePages; ++pg) {
+            const int lp = tile * kTilePages + pg;
+            ids[pg] = lp < pages_used ? p.page_table[(size_t)b * p.max_pages + lp] : -1;
+        }
+    };
+    auto load_tile = [&](__nv_bfloat16 *dst, const CUtensorMap *map, uint64_t *bar, const int (&ids)[kTilePages]) {
+#pragma unroll
+        for (int pg = 0; pg < kTilePages; ++pg) {
+            const int id = ids[pg];
+            const int row = (id >= 0 && id < p.num_pages) ? id * p.Hkv + kvh : p.num_pages * p.Hkv;
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i)
+                tma_load_3d(dst + i * (kBN * 64) + pg * (kPageTokens * 64), map, bar, i * 64, 0, row);
+        }
+    };
+    int rows_prev[kTilePages], rows_cur[kTilePages], rows_next[kTilePages];
+#pragma unroll
+    for (int pg = 0; pg < kTilePages; ++pg) rows_prev[pg] = rows_cur[pg] = rows_next[pg] = 0;
+    if (p.paged) fetch_rows(0, rows_next);
+
     int fills = 0;
     for (int u = 0; u <= n_all; ++u) {
         const int slot = u % kStages, use = u / kStages;
         if (use > 0 && !mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 1)) break;
         const bool has_k = u < n_all, has_v = u > 0;
         mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kBoxBytes);
-        if (has_k) {
+        if (!p.paged) {
+            if (has_k) {
 #pragma unroll
-            for (int i = 0; i < kBoxes; ++i)
-                tma_load_3d(sm.k[slot] + i * (kBN * 64), tmK, &sm.u_full[slot], i * 64, u * kBN, bh_kv);
-        }
-        if (has_v) {
+                for (int i = 0; i < kBoxes; ++i)
+                    tma_load_3d(sm.k[slot] + i * (kBN * 64), tmK, &sm.u_full[slot], i * 64, u * kBN, bh_kv);
+            }
+            if (has_v) {
 #pragma unroll
-            for (int i = 0; i < kBoxes; ++i)
-                tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh_kv);
+                for (int i = 0; i < kBoxes; ++i)
+                    tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh_kv);
+            }
+        } else {
+            // a 128-key tile is 8 pages of 16 keys: one 16-row box per page and 64-column
+            // block, stacked in the tile's 128-byte-swizzled rows.  K(u) uses the pages of
+            // tile u, V(u-1) those of tile u-1 (already looked up for K(u-1)); tile u+1's page
+            // ids are fetched here, one unit ahead of their use.
+#pragma unroll
+            for (int pg = 0; pg < kTilePages; ++pg) {
+                rows_prev[pg] = rows_cur[pg];
+                rows_cur[pg] = rows_next[pg];
+            }
+            if (u + 1 < n_all) fetch_rows(u + 1, rows_next);
+            if (has_k) load_tile(sm.k[slot], tmK, &sm.u_full[slot], rows_cur);
+            if (has_v) load_tile(sm.v[slot], tmV, &sm.u_full[slot], rows_prev);
         }
         ++fills;
     }
@@ -270,7 +327,7 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t t
 
 template <int D>
 __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t tmem, int t, int bh, int q0,
-                            int n_tiles, int kv_end, WaitCtx wc) {
+                            int n_tiles, int kv_end, int delta, WaitCtx wc) {
     const int r = threadIdx.x & 127;  // query row in the tile = TMEM lane
     const int wq = (threadIdx.x >> 5) & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
@@ -278,7 +335,6 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     const uint32_t tO = lane_base + 256 + (uint32_t)(t * D);
     const int qs = q0 + t * kBM;  // first row of this tile
     const int row = qs + r;
-    const int delta = p.Nkv - p.Nq;
     const float c = p.scale_log2;
     const uint64_t c2 = f32x2_pack(c, c);
 
@@ -409,11 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh_kv = (bh / p.H) * p.Hkv + (bh % p.H) / p.group;
     const int b = bh / p.H;
     const int q0 = unit * kRowsPerCta;
-    int kv_end = p.Nkv;
-    if (p.kv_lens) kv_end = min(max(p.kv_lens[b], 0), p.Nkv);
+    // keys of this sequence and the causal offset (query i sits at key position i + delta)
+    int kv_end, delta;
+    if (p.paged) {
+        kv_end = kv_end_of(p, b);
+        delta = kv_end - p.Nq;
+    } else {
+        kv_end = p.kv_lens ? min(max(p.kv_lens[b], 0), p.Nkv) : p.Nkv;
+        delta = p.Nkv - p.Nq;
+    }
     int n[kQTiles];
 #pragma unroll
-    for (int t = 0; t < kQTiles; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end);
+    for (int t = 0; t < kQTiles; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end, delta);
     const int n_all = max(n[0], n[1]);
 
     if (threadIdx.x == 0) {
@@ -444,14 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 8) {
         setmaxnreg_dec<kRegsOther>();
         if (warp == kProducerWarp) {
-            if (lane == 0 && n_all > 0) run_producer<D>(sm, &tmQ, &tmK, &tmV, bh, bh_kv, q0, n_all, wc);
+            if (lane == 0 && n_all > 0) run_producer<D>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
         } else if (warp == kMmaWarp) {
             if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
         }
     } else {
         setmaxnreg_inc<kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
-        run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, wc);
+        run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
     }
 
     tc_fence_before_sync();
@@ -481,12 +544,12 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // [BH, N, D] bf16 viewed as a 3-D tensor (innermost first), boxes of 64 x 128 x 1, 128-byte swizzle.
-bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D) {
+bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, int box_rows = 128) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -498,9 +561,13 @@ template <int D>
 cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
-    if (!encode_qkv_map(&tq, a.q, BH, a.Nq, D) || !encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D) ||
-        !encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D))
-        return cudaErrorInvalidValue;
+    bool ok_maps = encode_qkv_map(&tq, a.q, BH, a.Nq, D);
+    if (a.paged)  // pages [num_pages * Hkv] of 16 x D, one 16-row box per page
+        ok_maps = ok_maps && encode_qkv_map(&tk, a.k, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens) &&
+                  encode_qkv_map(&tv, a.v, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens);
+    else
+        ok_maps = ok_maps && encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D) && encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D);
+    if (!ok_maps) return cudaErrorInvalidValue;
     PrefillParams p;
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
@@ -513,11 +580,16 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.causal = a.causal;
     p.Hkv = a.Hkv;
     p.group = a.H / a.Hkv;
+    p.paged = a.paged;
+    p.page_table = a.page_table;
+    p.ctx_lens = a.ctx_lens;
+    p.max_pages = a.max_pages;
+    p.num_pages = a.num_pages;
     p.n_units = (a.Nq + kRowsPerCta - 1) / kRowsPerCta;
     {
         // about 48 MB of K/V per chunk: two chunks (the one finishing, the one starting) fit
         // in the 126 MB L2 together.  Query heads of one group share their K/V.
-        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0 / p.group;
+        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0 / p.group;  // Nkv: capacity when paged
         int hpc = (int)(48.0e6 / kv_bytes_per_head);
         p.heads_per_chunk = hpc < 1 ? 1 : (hpc > BH ? BH : hpc);
     }

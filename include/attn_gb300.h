@@ -150,6 +150,42 @@ int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_page
                           attn_stream_t stream);
 
 /*
+ * Chunked prefill over the paged KV cache (a prefill step writing into, then
+ * attending over, a KV cache kept in pages: inference-kernel-cookbook README,
+ * recipes 02 and 03).  Sequence b holds ctx_lens[b] tokens (device int32 [B],
+ * clamped to [0, max_pages_per_seq * page_size]) in its pages; the Nq queries
+ * q[b, :, i] are its LAST Nq positions (ctx_lens[b] - Nq + i), so with causal = 1
+ * query i sees keys j <= i + ctx_lens[b] - Nq (bottom-right), and every query sees
+ * only keys j < ctx_lens[b].  The new tokens' K/V must already be in the pages
+ * (paged_kv_append).
+ *   q, o [B, H, Nq, d] bf16; lse [B, H, Nq] fp32 (may be NULL)
+ *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16; page_table [B, max_pages_per_seq]
+ *   H % Hkv == 0 (grouped-query heads as attn_fwd_gqa); page_size 16; d in {64, 128}.
+ * Page ids outside [0, num_pages) read as zero keys/values (their scores still count
+ * for positions < ctx_lens[b]).  Runs on the same tcgen05 pipeline as attn_fwd, with
+ * each 128-key tile gathered page by page through TMA.
+ */
+int paged_attn_prefill(const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                       void *o, float *lse, int B, int H, int Hkv, int Nq, int d,
+                       int max_pages_per_seq, int num_pages, int causal, float scale,
+                       attn_stream_t stream);
+
+/*
+ * Appends the K/V of Nnew new tokens to the paged cache: token t of sequence b
+ * goes to position p = start_pos[b] + t, i.e. page page_table[b][p / page_size],
+ * slot p % page_size, for every key/value head.
+ *   k_new, v_new [B, Hkv, Nnew, d] bf16; k_pages, v_pages [num_pages, Hkv, page_size, d]
+ *   start_pos [B] int32 (device; tokens already in the cache before this append)
+ * Positions past max_pages_per_seq * page_size and page ids outside [0, num_pages)
+ * are skipped (nothing written).  The caller reserves the pages in the table.
+ */
+int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                    const int32_t *page_table, const int32_t *start_pos, int page_size,
+                    int B, int Hkv, int Nnew, int d, int max_pages_per_seq, int num_pages,
+                    attn_stream_t stream);
+
+/*
  * paged_attn_decode for callers that cannot allocate device memory.  The pages
  * describe no such variant; it exists for callers such as code running inside
  * a memory pool or allocator callback (where a nested cudaMalloc is not

@@ -242,6 +242,75 @@ int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, cons
     return err;
 }
 
+/* Chunked prefill over the paged cache (prefill into a KV cache, inference-kernel-cookbook
+ * README recipes 02-03; KV-cache append path of the Kernel-Inference-Engine README's
+ * roadmap): sequence b has ctx_lens[b] cached tokens in its pages, the last Nq of which are
+ * the new queries q[b, :, i] at positions ctx_lens[b] - Nq + i.  Query i sees keys
+ * j < ctx_lens[b] and, if causal, j <= i + ctx_lens[b] - Nq (bottom-right).  Pages are
+ * gathered into a contiguous cache and the plain definition applied per row.
+ * q [B,Hq,Nq,d]; k_pages/v_pages [num_pages,Hkv,page_size,d]; o [B,Hq,Nq,d]; lse [B,Hq,Nq]. */
+int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                                 const int32_t *page_table, const int32_t *ctx_lens, int page_size, int B,
+                                 int Hq, int Hkv, int Nq, int d, int max_pages, int num_pages, int causal,
+                                 double scale, double *o, double *lse, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || d <= 0 || page_size <= 0 ||
+        max_pages <= 0 || num_pages <= 0)
+        return 1;
+    const int group = Hq / Hkv;
+    const int cap = max_pages * page_size;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        uint16_t *kc = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)cap * d);
+        uint16_t *vc = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)cap * d);
+        double *srow = (double *)malloc(sizeof(double) * (size_t)cap);
+        unsigned char *valid = (unsigned char *)malloc((size_t)cap);
+        if (!kc || !vc || !srow || !valid) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+                int b = (int)(bh / Hq), h = (int)(bh % Hq);
+                int n = ctx_lens[b];
+                if (n < 0 || n > cap) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                int bad = 0;
+                for (int t = 0; t < n; ++t) {
+                    int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
+                    if (pg < 0 || pg >= num_pages) { bad = 1; break; }
+                    size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
+                    memcpy(kc + (size_t)t * d, k_pages + src, sizeof(uint16_t) * (size_t)d);
+                    memcpy(vc + (size_t)t * d, v_pages + src, sizeof(uint16_t) * (size_t)d);
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                for (int i = 0; i < Nq; ++i) {
+                    for (int j = 0; j < n; ++j) valid[j] = (unsigned char)key_valid(i, j, Nq, n, n, causal);
+                    size_t r = (size_t)bh * Nq + i;
+                    attend_row(q + r * d, kc, vc, valid, n, d, scale, srow, o + r * d, lse + r);
+                }
+            }
+        }
+        free(kc);
+        free(vc);
+        free(srow);
+        free(valid);
+    }
+    return err;
+}
+
 /* Paged decode, multi-head (Hkv = H): o [B,H,d], lse [B,H]. */
 int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                             const int32_t *page_table, const int32_t *ctx_lens, int page_size,

@@ -71,6 +71,9 @@ def _load():
                                                      P, ctypes.c_int64, P, P, I]
             lib.oracle_paged_decode_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I,
                                                         ctypes.c_double, P, P, I]
+            lib.oracle_paged_prefill_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I,
+                                                         ctypes.c_double, P, P, I]
+            lib.oracle_paged_prefill_gqa_f64.restype = ctypes.c_int
             lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
             lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
             for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
@@ -217,4 +220,25 @@ def paged_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nt
                                               nthreads)
     if err:
         raise RuntimeError(f"oracle_paged_decode_gqa_f64 failed ({err})")
+    return o, lse
+
+
+def paged_prefill_gqa(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, scale: float, nthreads: int = 0):
+    """Chunked prefill over the paged cache: q [B,Hq,Nq,d] are the last Nq of the ctx_lens[b]
+    cached tokens of sequence b (bottom-right causal); k_pages/v_pages [P,Hkv,page_size,d].
+    Returns (O [B,Hq,Nq,d], LSE [B,Hq,Nq]) in float64."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k_pages), bf16_bits(v_pages)
+    B, Hq, Nq, d = qb.shape
+    P, Hkv, ps, dk = kb.shape
+    if dk != d or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    pt = _i32(page_table)
+    cl = _i32(ctx_lens)
+    o = np.empty((B, Hq, Nq, d), np.float64)
+    lse = np.empty((B, Hq, Nq), np.float64)
+    err = _load().oracle_paged_prefill_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(cl), ps, B, Hq, Hkv,
+                                               Nq, d, pt.shape[1], P, int(bool(causal)), float(scale), _ptr(o),
+                                               _ptr(lse), nthreads)
+    if err:
+        raise RuntimeError(f"oracle_paged_prefill_gqa_f64 failed ({err})")
     return o, lse

@@ -397,3 +397,37 @@ def test_planted_gqa_head_mapping_mistake_is_caught(oracle_mod, tmp_path):
     qd, kd, vd = (t.to(torch.float64) for t in (q, k, v))
     ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, scale=0.25, enable_gqa=True)
     assert not np.allclose(o.reshape(B, Hq, N, d), ref.numpy(), atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- paged prefill
+
+def test_paged_prefill_equals_contiguous_bottom_right(oracle_mod):
+    # chunked prefill over the paged cache == the contiguous prefill definition (bottom-right
+    # causal, Nkv = ctx_len) run per sequence on the gathered cache
+    shape = workloads.DecodeShape("t", 3, 4, 16, (1, 90), page_size=16, seed=11)
+    inp = workloads.decode_inputs(shape, ctx_lens=[40, 90, 23], kv_heads=2)
+    Nq = 20
+    q = rand_bf16((3, 4, Nq, 16), 60)
+    for causal in (False, True):
+        o, lse = oracle_mod.paged_prefill_gqa(q, inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                              inp["ctx_lens"], causal, 0.3)
+        ps = 16
+        for b, n in enumerate(inp["ctx_lens"].tolist()):
+            pages = inp["page_table"][b, : (n + ps - 1) // ps].long()
+            kc = inp["k_pages"][pages].permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+            vc = inp["v_pages"][pages].permute(1, 0, 2, 3).reshape(2, -1, 16)[:, :n]
+            oc, lc = oracle_mod.attn_fwd_gqa(q[b:b + 1], kc[None].contiguous(), vc[None].contiguous(), causal, 0.3)
+            np.testing.assert_array_equal(o[b], oc[0])
+            np.testing.assert_array_equal(lse[b], lc[0])
+
+
+def test_paged_prefill_single_query_is_decode(oracle_mod):
+    shape = workloads.DecodeShape("t", 4, 4, 32, (1, 64), page_size=16, seed=12)
+    inp = workloads.decode_inputs(shape, ctx_lens=[1, 64, 17, 33])
+    q1 = inp["q"][:, :, None].contiguous()
+    o, lse = oracle_mod.paged_prefill_gqa(q1, inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                          True, 0.2)
+    od, ld = oracle_mod.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                     0.2)
+    np.testing.assert_array_equal(o[:, :, 0], od)
+    np.testing.assert_array_equal(lse[:, :, 0], ld)
