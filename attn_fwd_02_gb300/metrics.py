@@ -34,11 +34,30 @@ def prefill_bytes(B: int, H: int, Nq: int, Nkv: int, d: int, elem: int = 2, lse:
     return qo + kv + (4.0 * B * H * Nq if lse else 0.0)
 
 
-def decode_bytes(H: int, d: int, ctx_lens, page_size: int, elem: int = 2, lse: bool = True) -> float:
-    """K and V of every cached token once, q and o once, LSE fp32, page-table entries used."""
+def decode_bytes(H: int, d: int, ctx_lens, page_size: int, elem: int = 2, lse: bool = True,
+                 kv_heads: int | None = None) -> float:
+    """K and V of every cached token once (kv_heads cache heads, default H), q and o once,
+    LSE fp32, page-table entries used."""
     ctx = [int(x) for x in ctx_lens]
     B = len(ctx)
-    kv = 2.0 * H * d * elem * float(sum(ctx))
+    Hkv = H if kv_heads is None else kv_heads
+    kv = 2.0 * Hkv * d * elem * float(sum(ctx))
     qo = 2.0 * B * H * d * elem
     pt = 4.0 * float(sum(-(-c // page_size) for c in ctx))
     return kv + qo + pt + (4.0 * B * H if lse else 0.0)
+
+
+def paged_prefill_flops(H: int, Nq: int, d: int, ctx_lens, causal: bool = True) -> float:
+    """FLOPs of a chunked prefill whose Nq queries are the last Nq of ctx_b cached tokens:
+    4*d per (query, visible key); with the bottom-right causal mask query i sees
+    ctx_b - Nq + i + 1 keys, else ctx_b."""
+    total = 0.0
+    for c in (int(x) for x in ctx_lens):
+        if causal:
+            # sum over i of (c - Nq + i + 1), counting only positive terms
+            first = c - Nq + 1
+            keys = sum(max(0, first + i) for i in range(Nq))
+        else:
+            keys = Nq * c
+        total += 4.0 * H * d * keys
+    return total

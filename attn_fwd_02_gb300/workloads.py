@@ -80,6 +80,18 @@ LONG_CAUSAL = PrefillShape("long-context causal B2 H32 N8192 d128 inputs x0.5",
 PAGED_DECODE = DecodeShape("paged decode B32 H32 d128 ctx U[512,8192] page16",
                            32, 32, 128, (512, 8192), 16, seed=1005)
 
+# Grouped-query paged decode (32 query heads over 8 cache heads) on the same lengths.
+PAGED_DECODE_GQA = DecodeShape("paged decode GQA B32 Hq32 Hkv8 d128 ctx U[512,8192] page16",
+                               32, 32, 128, (512, 8192), 16, seed=1007)
+PAGED_DECODE_GQA_KV_HEADS = 8
+
+# Chunked prefill over the paged cache: 1024 new tokens per sequence on top of a cache of
+# 1024..8192 tokens (the chunk included), 32 query heads over 8 cache heads.
+PAGED_PREFILL = DecodeShape("chunked prefill B8 Hq32 Hkv8 d128 Nq1024 ctx U[1024,8192] page16",
+                            8, 32, 128, (1024, 8192), 16, seed=1008)
+PAGED_PREFILL_KV_HEADS = 8
+PAGED_PREFILL_NQ = 1024
+
 # A quarter-size paged decode (same lengths distribution) for multi-pass profiler captures.
 PAGED_DECODE_SMALL = DecodeShape("paged decode B8 H32 d128 ctx U[512,8192] page16",
                                  8, 32, 128, (512, 8192), 16, seed=1006)

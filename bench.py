@@ -230,9 +230,10 @@ class PrefillCase:
 
 
 class DecodeCase:
-    def __init__(self, shape, torch, A):
+    def __init__(self, shape, torch, A, kv_heads=None):
         self.shape, self.A = shape, A
-        inp = workloads.decode_inputs(shape)
+        self.kv_heads = kv_heads
+        inp = workloads.decode_inputs(shape, kv_heads=kv_heads)
         self.host = {k: v.pin_memory() for k, v in inp.items()}
         self.dev = {k: v.cuda() for k, v in inp.items()}
         d = self.dev
@@ -242,7 +243,7 @@ class DecodeCase:
                                                   shape.page_size)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
         self.ctx = [int(x) for x in inp["ctx_lens"]]
-        self.bytes = metrics.decode_bytes(shape.H, shape.d, self.ctx, shape.page_size)
+        self.bytes = metrics.decode_bytes(shape.H, shape.d, self.ctx, shape.page_size, kv_heads=kv_heads)
         self.launches = 2
         self.o_host = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
         self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
@@ -251,8 +252,9 @@ class DecodeCase:
 
     def run(self):
         d = self.dev
-        self.A.paged_attn_decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"],
-                                 self.shape.scale, out=self.o, lse=self.lse, workspace=self.ws)
+        fn = self.A.paged_attn_decode if self.kv_heads is None else self.A.paged_attn_decode_gqa
+        fn(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"], self.shape.scale, out=self.o,
+           lse=self.lse, workspace=self.ws)
 
     def run_e2e(self):
         for k, v in self.host.items():
@@ -260,6 +262,28 @@ class DecodeCase:
         self.run()
         self.o_host.copy_(self.o, non_blocking=True)
         self.lse_host.copy_(self.lse, non_blocking=True)
+
+
+class PagedPrefillCase:
+    """Chunked prefill over the paged cache (queries = the last Nq cached positions)."""
+
+    def __init__(self, shape, kv_heads, nq, torch, A):
+        self.shape, self.A, self.Nq = shape, A, nq
+        inp = workloads.decode_inputs(shape, kv_heads=kv_heads)
+        g = torch.Generator().manual_seed(shape.seed + 1)
+        q = torch.randn(shape.B, shape.H, nq, shape.d, generator=g).to(torch.bfloat16)
+        self.dev = {k: v.cuda() for k, v in inp.items()}
+        self.q = q.cuda()
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device="cuda")
+        self.ctx = [int(x) for x in inp["ctx_lens"]]
+        self.flops = metrics.paged_prefill_flops(shape.H, nq, shape.d, self.ctx, causal=True)
+        self.launches = 1
+
+    def run(self):
+        d = self.dev
+        self.A.paged_attn_prefill(self.q, d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"], True,
+                                  self.shape.scale, out=self.o, lse=self.lse)
 
 
 def time_parts(torch, parts, steps, warmup, world, sampler=None):
@@ -335,10 +359,16 @@ def gpu_arm(args):
         pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
         dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
         parts = [pre, dec]
-    elif args.workload in ("decode", "decode_small"):
-        shape = workloads.PAGED_DECODE if args.workload == "decode" else workloads.PAGED_DECODE_SMALL
-        pre, dec = None, DecodeCase(shape, torch, A)
+    elif args.workload in ("decode", "decode_small", "decode_gqa"):
+        if args.workload == "decode_gqa":
+            dec = DecodeCase(workloads.PAGED_DECODE_GQA, torch, A, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
+        else:
+            shape = workloads.PAGED_DECODE if args.workload == "decode" else workloads.PAGED_DECODE_SMALL
+            dec = DecodeCase(shape, torch, A)
+        pre = None
         parts = [dec]
+    elif args.workload == "prefill_paged":
+        return paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind)
     else:
         pre, dec = PrefillCase(PREFILL_BY_NAME[args.workload], torch, A), None
         parts = [pre]
@@ -406,6 +436,42 @@ def gpu_arm(args):
         out["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pre, dec, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
+    """Chunked prefill over the paged cache, timed alone (not part of the default step)."""
+    case = PagedPrefillCase(workloads.PAGED_PREFILL, workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ,
+                            torch, A)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    region_ms, part_ms = time_parts(torch, [case], args.steps, args.warmup, world, sampler)
+    clocks = sampler.stop() if sampler else None
+    if A.attn_check_device_status() != 0:
+        raise RuntimeError("device status error after the timed region")
+    ms = part_ms[0]
+    achieved = case.flops / (ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    s = case.shape
+    out = {"metric": METRIC, "value": round(job_rate(case.flops, world, ms, 1e12), 2), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(region_ms / args.steps, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded torch.randn -> bf16)",
+           "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel (paged)",
+                        "peak_source": f"{peak_kind} bf16_tflops"},
+           "config": {"workload": s.name, "B": s.B, "H": s.H, "Hkv": workloads.PAGED_PREFILL_KV_HEADS, "d": s.d,
+                      "Nq": case.Nq, "ctx_total": sum(case.ctx), "flops_per_call": case.flops,
+                      "ms_per_call": round(ms, 4), "l2": "inputs larger than L2 (no flush)"},
+           "gpu_launches": case.launches * args.steps}
+    if clocks is not None:
+        out["clocks"] = clocks
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -518,7 +584,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["default", "decode", "decode_small", *PREFILL_BY_NAME], default="default")
+    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "prefill_paged",
+                                           *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

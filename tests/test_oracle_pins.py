@@ -431,3 +431,13 @@ def test_paged_prefill_single_query_is_decode(oracle_mod):
                                      0.2)
     np.testing.assert_array_equal(o[:, :, 0], od)
     np.testing.assert_array_equal(lse[:, :, 0], ld)
+
+
+def test_paged_prefill_flop_count_closed_form():
+    from attn_fwd_02_gb300.metrics import paged_prefill_flops
+    # Nq == ctx (no earlier cache): query i sees i + 1 keys -> 4*d*H*N(N+1)/2
+    assert paged_prefill_flops(3, 10, 8, [10]) == 4 * 8 * 3 * 55
+    # Nq = 1 is one decode row over all ctx keys
+    assert paged_prefill_flops(2, 1, 16, [7, 9]) == 4 * 16 * 2 * (7 + 9)
+    # non-causal: every query sees every cached key
+    assert paged_prefill_flops(1, 4, 2, [6], causal=False) == 4 * 2 * 4 * 6
