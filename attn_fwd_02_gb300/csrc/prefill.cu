@@ -9,8 +9,9 @@
 // memory, and K/V tiles wholly above the causal diagonal (or past the
 // key-padding length) are never visited.
 //
-// GB300 mapping.  One CTA = one (batch, head) and 256 query rows held as two
-// 128-row tiles Q0, Q1 that share every K/V tile.  12 warps (three warpgroups):
+// GB300 mapping (d = 128; d = 64 uses one query tile per CTA and two CTAs per SM, see Cfg).
+// One CTA = one (batch, head) and 256 query rows held as two 128-row tiles Q0, Q1 that share
+// every K/V tile.  12 warps (three warpgroups):
 //   warps 0-3  softmax warpgroup 0 (rows of Q0), warps 4-7  softmax warpgroup 1
 //              (rows of Q1).  Thread r of a warpgroup owns query row r = TMEM
 //              lane r: it loads its 128 scores from TMEM, masks, takes the row
@@ -43,18 +44,33 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
-constexpr int kQTiles = 2;
-constexpr int kRowsPerCta = kBM * kQTiles;
-constexpr int kThreads = 384;
-// Register split: launched at 168 per thread (384 x 168 = 64512 in the block's pool); the
-// producer/MMA warpgroup drops to 64 and each softmax warpgroup rises to 216:
+// Shape of the CTA per head dimension.
+//   d = 128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 12 warps with a
+//            per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
+//   d = 64:  one query tile per CTA, 6 warps, two CTAs per SM: at d = 64 a tile needs 256 TMEM
+//            columns (S 128 | O 64 | P 64) and 80 KB of shared memory, and two co-resident CTAs
+//            overlap each other's serial chains (Q load, first S, softmax, PV, epilogue), which
+//            dominate the short units of small problems.
+template <int D> struct Cfg;
+template <> struct Cfg<128> {
+    static constexpr int QT = 2, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr bool kSplitRegs = true;
+};
+template <> struct Cfg<64> {
+    static constexpr int QT = 1, kThreads = 192, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 2;
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr bool kSplitRegs = false;
+};
+static_assert(Cfg<64>::QT * (128 + 64 + 64) <= (int)Cfg<64>::kTmemCols, "d=64 TMEM layout");
+static_assert(Cfg<128>::QT * (128 + 128) <= (int)Cfg<128>::kTmemCols, "d=128 TMEM layout");
+constexpr int kQTilesMax = 2;
+// Register split (d = 128): launched at 168 per thread (384 x 168 = 64512 in the block's
+// pool); the producer/MMA warpgroup drops to 64 and each softmax warpgroup rises to 216:
 // 128 x (64 + 216 + 216) = 63488 <= 64512, and per SM sub-partition (one warp of each
 // warpgroup) 32 x 496 <= 16384 registers.
 constexpr uint32_t kRegsSoftmax = 216;
 constexpr uint32_t kRegsOther = 64;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -86,14 +102,16 @@ constexpr int kStages = 2;
 
 template <int D>
 struct alignas(1024) PrefillSmem {
-    __nv_bfloat16 q[kQTiles][kBM * D];     // D/64 boxes each
+    __nv_bfloat16 q[Cfg<D>::QT][kBM * D];  // D/64 boxes each
     __nv_bfloat16 k[kStages][kBN * D];     // D/64 boxes each
     __nv_bfloat16 v[kStages][kBN * D];     // D/64 boxes each
     uint64_t q_full;
     uint64_t u_full[kStages], u_empty[kStages];
-    uint64_t s_full[kQTiles];
-    uint64_t p_full[kQTiles];
-    uint64_t o_done[kQTiles];
+    uint64_t s_full[kQTilesMax];
+    uint64_t p_full[kQTilesMax];
+    uint64_t o_done[kQTilesMax];
+    uint64_t s_free[kQTilesMax];   // separate-P pipeline: the softmax has read S_t
+    uint64_t pv_done[kQTilesMax];  // separate-P pipeline: PV_t finished with P_t and O_t
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -102,6 +120,21 @@ struct alignas(1024) PrefillSmem {
 // Cached tokens of sequence b in paged mode (clamped to the table's capacity).
 __device__ __forceinline__ int kv_end_of(const PrefillParams &p, int b) {
     return min(max(p.ctx_lens[b], 0), p.max_pages * kPageTokens);
+}
+
+// At d = 64 the TMEM has room for P next to S and O (S0|S1|O0|O1|P0|P1 = 128+128+64+64+64+64
+// columns), so P gets its own columns and S_t(j+1) can be issued as soon as the softmax has
+// read S_t(j), before PV_t(j): the next scores are ready when the softmax finishes a tile.
+// At d = 128 the 512 columns hold exactly S0|S1|O0|O1 and P is written over its scores.
+template <int D> struct SeparateP { static constexpr bool value = (D == 64); };
+
+// TMEM columns: S_t at 128 t; O_t after all S buffers; P_t after all O accumulators when it
+// has its own columns, else over the first 64 columns of S_t.
+template <int D> __device__ __forceinline__ uint32_t o_col(int t) {
+    return (uint32_t)(Cfg<D>::QT * kBN + t * D);
+}
+template <int D> __device__ __forceinline__ uint32_t p_col(int t) {
+    return SeparateP<D>::value ? (uint32_t)(Cfg<D>::QT * (kBN + D) + t * 64) : (uint32_t)(t * kBN);
 }
 
 // Key tiles query tile t of this CTA must visit: keys < limit can be valid for some of its rows.
@@ -121,9 +154,9 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
-    mbar_arrive_expect_tx(&sm.q_full, kQTiles * kBoxes * kBoxBytes);
+    mbar_arrive_expect_tx(&sm.q_full, Cfg<D>::QT * kBoxes * kBoxBytes);
 #pragma unroll
-    for (int t = 0; t < kQTiles; ++t)
+    for (int t = 0; t < Cfg<D>::QT; ++t)
 #pragma unroll
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
@@ -201,7 +234,7 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
 
 // ------------------------------------------------------------------ MMA issuer
 template <int D>
-__device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTiles], int n_all, WaitCtx wc) {
+__device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
 
@@ -221,8 +254,8 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
     // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
     auto issue_PV = [&](int t, int j) {
         const uint32_t v_addr = smem_u32(sm.v[(j + 1) % kStages]);
-        const uint32_t tP = tmem + (uint32_t)(t * kBN);
-        const uint32_t tO = tmem + 256 + (uint32_t)(t * D);
+        const uint32_t tP = tmem + p_col<D>(t);
+        const uint32_t tO = tmem + o_col<D>(t);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
             tc_mma_ts(tO, tP + (uint32_t)(kk * 8), sdesc_sw128(v_addr + (uint32_t)(kk * 16 * 128), kBoxBytes, 1024),
@@ -236,14 +269,35 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
     bool ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.u_full[0], 0, wc, 10);
     if (ok) {
         tc_fence_after_sync();
-        for (int t = 0; t < kQTiles; ++t)
+        for (int t = 0; t < Cfg<D>::QT; ++t)
             if (n[t] > 0) issue_S(t, 0);
         tc_commit(&sm.u_empty[0]);
         for (int j = 0; j < n_all && ok; ++j) {
             const int u = j + 1;  // unit with V(j) and K(j+1)
             ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13);
             if (!ok) break;
-            for (int t = 0; t < kQTiles; ++t) {
+            if constexpr (SeparateP<D>::value) {
+                // both S_t(j+1) first (a buffer is free once its softmax has read S_t(j)), then
+                // both PV_t(j): the softmax warpgroups find their next scores ready
+                for (int t = 0; t < Cfg<D>::QT && ok; ++t) {
+                    if (j + 1 < n[t]) {
+                        if (!(ok = mbar_wait(&sm.s_free[t], (uint32_t)(j & 1), wc, 17 + t))) break;
+                        tc_fence_after_sync();
+                        issue_S(t, j + 1);
+                    }
+                }
+                for (int t = 0; t < Cfg<D>::QT && ok; ++t) {
+                    if (j < n[t]) {
+                        if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
+                        tc_fence_after_sync();
+                        issue_PV(t, j);
+                        tc_commit(&sm.pv_done[t]);
+                        if (j == n[t] - 1) tc_commit(&sm.o_done[t]);
+                    }
+                }
+            }
+            // P over S: PV_t(j) must be issued before S_t(j+1) overwrites its buffer
+            for (int t = 0; t < Cfg<D>::QT && !SeparateP<D>::value; ++t) {
                 if (j < n[t]) {
                     if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
                     tc_fence_after_sync();
@@ -332,7 +386,8 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     const int wq = (threadIdx.x >> 5) & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t tS = lane_base + (uint32_t)(t * kBN);
-    const uint32_t tO = lane_base + 256 + (uint32_t)(t * D);
+    const uint32_t tO = lane_base + o_col<D>(t);
+    const uint32_t tP = lane_base + p_col<D>(t);
     const int qs = q0 + t * kBM;  // first row of this tile
     const int row = qs + r;
     const float c = p.scale_log2;
@@ -370,6 +425,11 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             tmem_wait_ld(s[h][0]);
             tmem_wait_ld(s[h][1]);
         }
+        if constexpr (SeparateP<D>::value) {
+            // the scores are in registers: the MMA issuer may compute S_t(j+1) into the buffer
+            tc_fence_before_sync();
+            mbar_arrive(&sm.s_free[t]);
+        }
         if (need_mask) {
             mask_chunks(s[0], nvalid);
             mask_chunks(s[1], nvalid - 64);
@@ -390,8 +450,21 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
         // expects): keys 0-63 -> columns 0-31, keys 64-127 -> columns 32-63, over scores
         // already read into registers.
         uint64_t rs2[4] = {0, 0, 0, 0};
-        exp_store(s[0], tS, c2, negm2, rs2);
-        exp_store(s[1], tS + 32, c2, negm2, rs2);
+        if constexpr (SeparateP<D>::value) {
+            // P_t and O_t are free once PV_t(j-1) has completed
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done[t], (uint32_t)((j - 1) & 1), wc, 28 + t))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+            }
+            exp_store(s[0], tP, c2, negm2, rs2);
+            exp_store(s[1], tP + 32, c2, negm2, rs2);
+        } else {
+            exp_store(s[0], tS, c2, negm2, rs2);
+            exp_store(s[1], tS + 32, c2, negm2, rs2);
+        }
         {
             const uint64_t t01 = f32x2_add(rs2[0], rs2[1]);
             const uint64_t t23 = f32x2_add(rs2[2], rs2[3]);
@@ -400,7 +473,8 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             l += a0 + a1;
         }
 
-        // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled)
+        // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled (P over S), or
+        // pv_done was waited for above (separate P)
         if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<D>(tO, alpha);
         tmem_wait_st();
         tc_fence_before_sync();
@@ -439,7 +513,7 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -464,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key/value head of this query head (grouped-query attention; = bh for multi-head)
     const int bh_kv = (bh / p.H) * p.Hkv + (bh % p.H) / p.group;
     const int b = bh / p.H;
-    const int q0 = unit * kRowsPerCta;
+    const int q0 = unit * (kBM * Cfg<D>::QT);
     // keys of this sequence and the causal offset (query i sits at key position i + delta)
     int kv_end, delta;
     if (p.paged) {
@@ -474,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv_end = p.kv_lens ? min(max(p.kv_lens[b], 0), p.Nkv) : p.Nkv;
         delta = p.Nkv - p.Nq;
     }
-    int n[kQTiles];
+    int n[kQTilesMax] = {0, 0};
 #pragma unroll
-    for (int t = 0; t < kQTiles; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end, delta);
+    for (int t = 0; t < Cfg<D>::QT; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end, delta);
     const int n_all = max(n[0], n[1]);
 
     if (threadIdx.x == 0) {
@@ -485,17 +559,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.u_full[s], 1);
             mbar_init(&sm.u_empty[s], 1);
         }
-        for (int t = 0; t < kQTiles; ++t) {
+        for (int t = 0; t < Cfg<D>::QT; ++t) {
             mbar_init(&sm.s_full[t], 1);
             mbar_init(&sm.p_full[t], kBM);
             mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.s_free[t], kBM);
+            mbar_init(&sm.pv_done[t], 1);
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (warp == Cfg<D>::kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, Cfg<D>::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -504,24 +580,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     WaitCtx wc{&sm.abort_flag, p.status};
 
-    if (warp >= 8) {
-        setmaxnreg_dec<kRegsOther>();
-        if (warp == kProducerWarp) {
+    if (warp >= 4 * Cfg<D>::QT) {
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<kRegsOther>();
+        if (warp == Cfg<D>::kProducerWarp) {
             if (lane == 0 && n_all > 0) run_producer<D>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
-        } else if (warp == kMmaWarp) {
+        } else if (warp == Cfg<D>::kMmaWarp) {
             if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
         }
     } else {
-        setmaxnreg_inc<kRegsSoftmax>();
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
         run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == Cfg<D>::kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, Cfg<D>::kTmemCols);
     }
 }
 
@@ -585,7 +661,7 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.ctx_lens = a.ctx_lens;
     p.max_pages = a.max_pages;
     p.num_pages = a.num_pages;
-    p.n_units = (a.Nq + kRowsPerCta - 1) / kRowsPerCta;
+    p.n_units = (a.Nq + kBM * Cfg<D>::QT - 1) / (kBM * Cfg<D>::QT);
     {
         // about 48 MB of K/V per chunk: two chunks (the one finishing, the one starting) fit
         // in the 126 MB L2 together.  Query heads of one group share their K/V.
@@ -598,7 +674,7 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)p.n_units * BH);
-    prefill_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
