@@ -56,6 +56,8 @@ def library_path() -> str:
 def load_library():
     """Load the CUDA library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             path = library_path()

@@ -61,6 +61,47 @@ int prefill_checks(const void *q, const void *k, const void *v, void *o, float *
 
 }  // namespace
 
+namespace attn {
+
+cudaError_t current_sm_count(int *sms) {
+    static int cache[kMaxDevices];  // 0 = unknown
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (cache[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cache[dev] = n;
+    }
+    *sms = cache[dev];
+    return cudaSuccess;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes) {
+    struct Entry {
+        const void *fn;
+        int dev;
+        int bytes;
+    };
+    static Entry done[256];
+    static int n_done = 0;
+    static std::mutex mu;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].fn == kernel && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (n_done < 256) done[n_done++] = Entry{kernel, dev, bytes};
+    return cudaSuccess;
+}
+
+}  // namespace attn
+
 ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
                           int Hkv, int Nq, int Nkv, int d, int causal, float scale, const int32_t *kv_lens,
                           attn_stream_t stream) {

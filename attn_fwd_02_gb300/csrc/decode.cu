@@ -351,8 +351,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, i
 template <int D, int GP>
 cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
     const size_t smem = sizeof(DecodeSmem<D, GP>);
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_split_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_split_kernel<D, GP>), (int)smem);
     if (e != cudaSuccess) return e;
     const int gsplit = (a.H / a.Hkv) / GP;  // CTAs per key/value head
     dim3 g1(max_splits, a.Hkv * gsplit, a.B);

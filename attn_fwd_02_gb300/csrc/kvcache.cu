@@ -45,9 +45,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
                              const int32_t *page_table, const int32_t *start_pos, int B, int Hkv, int Nnew, int d,
                              int max_pages, int num_pages, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0;
+    cudaError_t e = current_sm_count(&sms);
     if (e != cudaSuccess) return e;
     const long long total = (long long)B * Hkv * Nnew * (d * 2 / 16);
     const long long want = (total + 255) / 256;

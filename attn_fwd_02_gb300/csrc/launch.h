@@ -37,6 +37,12 @@ struct DecodeArgs {
     int Hkv;  // key/value heads of the cache (H for multi-head; H % Hkv == 0)
 };
 
+// Per-device facts looked up once (host-side caches shared by the launchers): the SM count
+// of the current device, and a kernel's dynamic shared-memory opt-in (set once per
+// function and device; cudaFuncSetAttribute is not free on every call).
+cudaError_t current_sm_count(int *sms);
+cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes);
+
 // Encodes the TMA descriptors and launches the prefill kernel.
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 

@@ -671,7 +671,7 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     }
     p.scale_log2 = a.scale * kLog2e;
     const size_t smem = sizeof(PrefillSmem<D>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<D>), (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)p.n_units * BH);
     prefill_kernel<D><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);

@@ -286,24 +286,56 @@ class PagedPrefillCase:
                                   self.shape.scale, out=self.o, lse=self.lse)
 
 
-def time_parts(torch, parts, steps, warmup, world, sampler=None):
+L2_BYTES = 129e6
+FLUSH_BYTES = 512 << 20
+
+
+def step_flushes_l2(parts) -> bool:
+    """Flush L2 between steps when one step's inputs would otherwise stay resident in it."""
+    return sum(getattr(p, "bytes", 0) for p in parts) < 2 * L2_BYTES
+
+
+def time_parts(torch, parts, steps, warmup, world, sampler=None, graphs=False):
     """Warm up, then time `steps` steps; each step runs every part once.  Returns the
-    region time (max over ranks) and each part's mean per-call device time (ms)."""
+    region time (max over ranks) and each part's mean per-call device time (ms).
+
+    With graphs, each part's call (all its kernels) is captured once into a CUDA graph
+    after the warm-up and the timed steps replay the graphs: the host's per-call launch
+    cost, which exceeds the device time of the smallest workloads, stays out of the
+    device-throughput figure (the end-to-end figure keeps it)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for p in parts:
             p.run()
     barrier_sync(world)
+    runners = [p.run for p in parts]
+    if graphs:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        captured = []
+        for p in parts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                p.run()
+            captured.append(g)
+        stream.wait_stream(side)
+        runners = [g.replay for g in captured]
+        for r in runners:  # one untimed replay each
+            r()
+        barrier_sync(world)
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
            for _ in range(steps)]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if step_flushes_l2(parts) else None
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.mark(True)
     t0.record(stream)
     for s in range(steps):
-        for i, p in enumerate(parts):
+        if flush is not None:  # outside the per-call events; inside the step's region time
+            flush.zero_()
+        for i, run in enumerate(runners):
             evs[s][i][0].record(stream)
-            p.run()
+            run()
             evs[s][i][1].record(stream)
     t1.record(stream)
     barrier_sync(world)
@@ -377,7 +409,7 @@ def gpu_arm(args):
     if sampler:
         sampler.start()
         time.sleep(0.5)
-    region_ms, part_ms = time_parts(torch, parts, args.steps, args.warmup, world, sampler)
+    region_ms, part_ms = time_parts(torch, parts, args.steps, args.warmup, world, sampler, graphs=args.graphs)
     clocks = sampler.stop() if sampler else None
     status = A.attn_check_device_status()
     if status != 0:
@@ -388,7 +420,10 @@ def gpu_arm(args):
     out = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(region_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded torch.randn -> bf16)"}
-    cfg = {"l2": "inputs larger than L2 (no flush)", "parallelism": "replicas" if world > 1 else "single GPU"}
+    cfg = {"l2": "L2 flushed between steps (512 MiB write, outside the per-call events)"
+           if step_flushes_l2(parts) else "inputs larger than L2 (no flush)",
+           "parallelism": "replicas" if world > 1 else "single GPU",
+           "launch": "CUDA graph replay per call (captured through the API)" if args.graphs else "direct calls"}
     launches = 0
     if pre is not None:
         i = parts.index(pre)
@@ -451,7 +486,7 @@ def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
     if sampler:
         sampler.start()
         time.sleep(0.5)
-    region_ms, part_ms = time_parts(torch, [case], args.steps, args.warmup, world, sampler)
+    region_ms, part_ms = time_parts(torch, [case], args.steps, args.warmup, world, sampler, graphs=args.graphs)
     clocks = sampler.stop() if sampler else None
     if A.attn_check_device_status() != 0:
         raise RuntimeError("device status error after the timed region")
@@ -588,6 +623,7 @@ def main():
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graphs", action="store_true", help="time CUDA graph replays of each call instead of direct calls")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always
     if args.impl == "reference":
