@@ -46,6 +46,8 @@
  *   q [B,H,Nq,d], k/v [B,H,Nkv,d], o [B,H,Nq,d] (fp64), lse [B,H,Nq] (fp64)
  *   paged: q [B,H,d]; k_pages/v_pages [num_pages,H,page_size,d];
  *          page_table [B,max_pages] int32; ctx_lens [B] int32
+ *
+ * The backward (gradients of the same definition) is at the end of the file.
  */
 #include <math.h>
 #include <stdint.h>
@@ -318,6 +320,138 @@ int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const ui
                             double *o, double *lse, int nthreads) {
     return oracle_paged_decode_gqa_f64(q, k_pages, v_pages, page_table, ctx_lens, page_size, B, H, H, d,
                                        max_pages, num_pages, scale, o, lse, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * Backward pass.  The gpu-inference blog, section 02 ("FlashAttention-2 in Triton"), trains with
+ * a backward that recomputes the probabilities from the forward's saved log-sum-exp and splits
+ * the work into a row-wise D preprocessing pass, a dK/dV pass and a dQ pass.  What that backward
+ * reaches is the exact gradient of the definition above for an upstream gradient dO of O, which
+ * this oracle writes out directly (no tiling, no saved statistics; everything recomputed):
+ *
+ *   P_ij  = exp(s_ij - m_i) / l_i  for j in J_i, 0 otherwise        (the forward's softmax row)
+ *   dV_j  = sum_i P_ij dO_i                                          (O = P V)
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij                                         (= dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)                                       (softmax Jacobian)
+ *   dQ_i  = scale sum_j dS_ij k_j,     dK_j = scale sum_i dS_ij q_i  (s = scale q . k)
+ *
+ * Grouped-query form: key/value head g is read by query heads g*group .. g*group+group-1, so its
+ * dK and dV sum over those heads.  A row with no valid key has P = 0: it adds nothing and its dQ
+ * is 0.  Inputs are fp64 here (the Python wrapper widens bf16 exactly) so that the same function
+ * also serves finite-difference checks with perturbations bf16 cannot hold.  Optional outputs o,
+ * lse (the forward of these fp64 inputs) and Drow may be NULL.
+ * q, dout, dq [B,Hq,Nq,d]; k, v, dk, dv [B,Hkv,Nkv,d]; o [B,Hq,Nq,d]; lse, Drow [B,Hq,Nq].
+ */
+int oracle_attn_bwd_gqa_f64(const double *q, const double *k, const double *v, const double *dout,
+                            const int32_t *kv_lens, int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                            int causal, double scale, double *dq, double *dk, double *dv,
+                            double *o, double *lse, double *Drow, int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || Nkv <= 0 || d <= 0) return 1;
+    const int group = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *P = (double *)malloc(sizeof(double) * (size_t)Nkv);
+        double *dP = (double *)malloc(sizeof(double) * (size_t)Nkv);
+        unsigned char *valid = (unsigned char *)malloc((size_t)Nkv);
+        if (!P || !dP || !valid) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+            /* one (batch, key/value head) per iteration: it owns dK/dV of that head */
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bg = 0; bg < (int64_t)B * Hkv; ++bg) {
+                const int b = (int)(bg / Hkv), g = (int)(bg % Hkv);
+                const double *kb = k + (size_t)bg * Nkv * d;
+                const double *vb = v + (size_t)bg * Nkv * d;
+                double *dkb = dk + (size_t)bg * Nkv * d;
+                double *dvb = dv + (size_t)bg * Nkv * d;
+                for (size_t x = 0; x < (size_t)Nkv * d; ++x) dkb[x] = dvb[x] = 0.0;
+                const int kv_len = kv_lens ? kv_lens[b] : Nkv;
+                for (int hh = 0; hh < group; ++hh) {
+                    const int h = g * group + hh;
+                    for (int i = 0; i < Nq; ++i) {
+                        const size_t r = ((size_t)b * Hq + h) * Nq + i;
+                        const double *qi = q + r * d, *doi = dout + r * d;
+                        double *dqi = dq + r * d;
+                        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+                        /* the forward's softmax row, three passes */
+                        double m = -INFINITY;
+                        int any = 0;
+                        for (int j = 0; j < Nkv; ++j) {
+                            valid[j] = (unsigned char)key_valid(i, j, Nq, Nkv, kv_len, causal);
+                            if (!valid[j]) continue;
+                            double dot = 0.0;
+                            for (int c = 0; c < d; ++c) dot += qi[c] * kb[(size_t)j * d + c];
+                            P[j] = scale * dot;
+                            if (!any || P[j] > m) m = P[j];
+                            any = 1;
+                        }
+                        if (!any) {
+                            if (o) for (int c = 0; c < d; ++c) o[r * d + c] = 0.0;
+                            if (lse) lse[r] = -INFINITY;
+                            if (Drow) Drow[r] = 0.0;
+                            continue;
+                        }
+                        double l = 0.0;
+                        for (int j = 0; j < Nkv; ++j)
+                            if (valid[j]) l += exp(P[j] - m);
+                        for (int j = 0; j < Nkv; ++j) P[j] = valid[j] ? exp(P[j] - m) / l : 0.0;
+                        if (o) {
+                            for (int c = 0; c < d; ++c) o[r * d + c] = 0.0;
+                            for (int j = 0; j < Nkv; ++j)
+                                if (valid[j])
+                                    for (int c = 0; c < d; ++c) o[r * d + c] += P[j] * vb[(size_t)j * d + c];
+                        }
+                        if (lse) lse[r] = m + log(l);
+                        /* dP and the row term D */
+                        double Di = 0.0;
+                        for (int j = 0; j < Nkv; ++j) {
+                            if (!valid[j]) continue;
+                            double dot = 0.0;
+                            for (int c = 0; c < d; ++c) dot += doi[c] * vb[(size_t)j * d + c];
+                            dP[j] = dot;
+                            Di += P[j] * dot;
+                        }
+                        if (Drow) Drow[r] = Di;
+                        /* dS, then the three products */
+                        for (int j = 0; j < Nkv; ++j) {
+                            if (!valid[j]) continue;
+                            const double dS = P[j] * (dP[j] - Di);
+                            for (int c = 0; c < d; ++c) {
+                                dqi[c] += scale * dS * kb[(size_t)j * d + c];
+                                dkb[(size_t)j * d + c] += scale * dS * qi[c];
+                                dvb[(size_t)j * d + c] += P[j] * doi[c];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dP);
+        free(valid);
+    }
+    return err;
+}
+
+/* The backward's preprocessing step as the method computes it: D_i = dO_i . O_i from the stored
+ * (bf16) forward output.  o, dout [nrows, d] bf16 bit patterns; Drow [nrows]. */
+int oracle_bwd_rowdot_f64(const uint16_t *o, const uint16_t *dout, int64_t nrows, int d, double *Drow) {
+    if (nrows < 0 || d <= 0) return 1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += bf16_to_f64(dout[(size_t)r * d + c]) * bf16_to_f64(o[(size_t)r * d + c]);
+        Drow[r] = acc;
+    }
+    return 0;
 }
 
 /* Number of threads OpenMP would use (for reporting the CPU baseline's cores). */

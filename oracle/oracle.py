@@ -21,6 +21,11 @@ pages to reach exactly this result without materialising the score matrix
 recipe 01).  The paged form gathers pages through the page table into a
 contiguous cache and applies the same definition (inference-kernel-cookbook
 README, recipe 03 "Paged Attention").
+
+The backward is the exact gradient of that definition for an upstream gradient
+dO (gpu-inference blog, section 02: D preprocessing, dK/dV and dQ passes):
+dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij, dS = P * (dP - D),
+dQ = scale dS K, dK = scale dS^T Q.
 """
 from __future__ import annotations
 
@@ -74,6 +79,11 @@ def _load():
             lib.oracle_paged_prefill_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                                          ctypes.c_double, P, P, I]
             lib.oracle_paged_prefill_gqa_f64.restype = ctypes.c_int
+            lib.oracle_attn_bwd_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
+                                                    P, P, P, P, P, P, I]
+            lib.oracle_attn_bwd_gqa_f64.restype = ctypes.c_int
+            lib.oracle_bwd_rowdot_f64.argtypes = [P, P, ctypes.c_int64, I, P]
+            lib.oracle_bwd_rowdot_f64.restype = ctypes.c_int
             lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
             lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
             for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
@@ -242,3 +252,51 @@ def paged_prefill_gqa(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, s
     if err:
         raise RuntimeError(f"oracle_paged_prefill_gqa_f64 failed ({err})")
     return o, lse
+
+
+def _f64(x) -> np.ndarray:
+    """float64 copy of a bf16 tensor (exact widening) or of a float array."""
+    if isinstance(x, np.ndarray) and x.dtype != np.uint16:
+        return np.ascontiguousarray(x, dtype=np.float64)
+    if not isinstance(x, np.ndarray):
+        import torch
+        if x.dtype != torch.bfloat16:
+            return np.ascontiguousarray(x.detach().cpu().to(torch.float64).numpy())
+    return np.ascontiguousarray(bf16_to_f64(x))
+
+
+def attn_bwd_gqa(q, k, v, dout, causal: bool, scale: float, kv_lens=None, nthreads: int = 0):
+    """Gradients of exact attention for upstream gradient dout.  q, dout [B,Hq,Nq,d]; k, v
+    [B,Hkv,Nkv,d]; bf16 tensors are widened exactly, float inputs are taken as they are (finite
+    differences).  Returns a dict of float64 arrays: dq, dk, dv, and the forward o, lse and the
+    row term D = rowsum(P * dP) of the same inputs."""
+    qd, kd, vd, dod = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Nq, d = qd.shape
+    Hkv, Nkv = kd.shape[1], kd.shape[2]
+    if kd.shape != (B, Hkv, Nkv, d) or vd.shape != kd.shape or dod.shape != qd.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    kl = _i32(kv_lens)
+    out = {n: np.empty(qd.shape, np.float64) for n in ("dq", "o")}
+    out.update({n: np.empty(kd.shape, np.float64) for n in ("dk", "dv")})
+    out.update({n: np.empty((B, Hq, Nq), np.float64) for n in ("lse", "D")})
+    err = _load().oracle_attn_bwd_gqa_f64(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dod), _ptr(kl), B, Hq, Hkv, Nq, Nkv,
+                                          d, int(bool(causal)), float(scale), _ptr(out["dq"]), _ptr(out["dk"]),
+                                          _ptr(out["dv"]), _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["D"]),
+                                          nthreads)
+    if err:
+        raise RuntimeError(f"oracle_attn_bwd_gqa_f64 failed ({err})")
+    return out
+
+
+def bwd_rowdot(o, dout):
+    """The backward's preprocessing term D_i = dO_i . O_i from bf16 o, dout [..., d]; float64 [...]."""
+    ob, db = bf16_bits(o), bf16_bits(dout)
+    if ob.shape != db.shape:
+        raise ValueError("shape mismatch")
+    d = ob.shape[-1]
+    n = ob.size // d
+    D = np.empty((n,), np.float64)
+    err = _load().oracle_bwd_rowdot_f64(_ptr(ob), _ptr(db), n, d, _ptr(D))
+    if err:
+        raise RuntimeError("oracle_bwd_rowdot_f64 failed")
+    return D.reshape(ob.shape[:-1])
