@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) exact attention forward: FlashAttention-style prefill and paged-KV decode.
+"""GB300 (sm_103a) exact attention: FlashAttention-style prefill (forward and backward) and paged-KV decode.
 
 The compute path is the CUDA shared library built from ``csrc/`` (C-ABI declared in
 ``include/attn_gb300.h``).  ``binding`` marshals torch tensors into that ABI; it has no
@@ -6,6 +6,8 @@ fallback: if the library is missing, every call raises.
 """
 from .binding import (  # noqa: F401
     AttnError,
+    attn_bwd,
+    attn_bwd_workspace_size,
     attn_check_device_status,
     attn_selftest_bounded_wait,
     attn_fwd,

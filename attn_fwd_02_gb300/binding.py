@@ -36,6 +36,8 @@ SIGNATURES = {
     "paged_attn_decode_gqa": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
     "paged_attn_prefill": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P]),
     "paged_kv_append": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, P]),
+    "attn_bwd_workspace_size": (Z, [I, I, I]),
+    "attn_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, Z, P]),
     "attn_check_device_status": (I, [P]),
     "attn_selftest_bounded_wait": (I, [P]),
     "attn_status_string": (ctypes.c_char_p, [I]),
@@ -157,6 +159,44 @@ def attn_fwd_gqa(q, k, v, causal: bool, scale: float | None = None, kv_lens=None
                                      d, int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
     _check("attn_fwd_gqa", st)
     return out, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Nq: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, Hq, Nq))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, kv_lens=None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd_gqa: q, o, dout [B,Hq,Nq,d] and k, v [B,Hkv,Nkv,d] bf16 CUDA tensors,
+    lse [B,Hq,Nq] fp32 from the forward; causal, scale and kv_lens as in the forward call.
+    Returns (dq, dk, dv) bf16.  The workspace (uint8, attn_bwd_workspace_size bytes) ends up
+    holding the row term D [B,Hq,Nq] fp32."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _require(t, n, torch.bfloat16, 4)
+    _require(lse, "lse", torch.float32, 3)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nkv, d) or tuple(v.shape) != (B, Hkv, Nkv, d):
+        raise ValueError("k and v must be [B, Hkv, Nkv, d] matching q")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("o and dout must match q, lse must be [B, Hq, Nq]")
+    if kv_lens is not None:
+        _require(kv_lens, "kv_lens", torch.int32, 1)
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    lib = load_library()
+    need = int(lib.attn_bwd_workspace_size(B, Hq, Nq))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = lib.attn_bwd(_dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse), _dptr(dout), _dptr(dq), _dptr(dk),
+                      _dptr(dv), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), float(scale), _dptr(kv_lens),
+                      _dptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("attn_bwd", st)
+    return dq, dk, dv
 
 
 def attn_fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=None,

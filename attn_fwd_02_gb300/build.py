@@ -24,7 +24,7 @@ ROOT = os.path.dirname(HERE)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden,-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["abi.cu", "prefill.cu", "decode.cu", "kvcache.cu"]
+SOURCES = ["abi.cu", "prefill.cu", "decode.cu", "kvcache.cu", "backward.cu"]
 
 
 def nvcc() -> str:

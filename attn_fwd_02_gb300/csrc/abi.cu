@@ -100,6 +100,38 @@ cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes) {
     return cudaSuccess;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [BH, N, D] bf16 viewed as a 3-D tensor (innermost first), boxes of 64 x 128 x 1, 128-byte swizzle.
+bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace attn
 
 ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
@@ -124,6 +156,31 @@ ATTN_API int attn_fwd_kvlen(const void *q, const void *k, const void *v, void *o
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
                       int Nkv, int d, int causal, float scale, attn_stream_t stream) {
     return attn_fwd_kvlen(q, k, v, o, lse, B, H, Nq, Nkv, d, causal, scale, nullptr, stream);
+}
+
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq) { return attn::bwd_workspace_bytes(B, Hq, Nq); }
+
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                      void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal,
+                      float scale, const int32_t *kv_lens, void *workspace, size_t workspace_bytes,
+                      attn_stream_t stream) {
+    if (!o || !lse || !dout || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    // q, k, v, dq and the sizes get the forward's checks (dq in the place of o)
+    int st = prefill_checks(q, k, v, dq, nullptr, B, Hq, Hkv, Nq, Nkv, d, causal, scale, kv_lens);
+    if (st != ATTN_OK) return st;
+    const uint64_t kv_ctas = ((uint64_t)Nkv + 127) / 128 * (uint64_t)B * (uint64_t)Hkv;
+    if (kv_ctas > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
+        return ATTN_ERR_MISALIGNED;
+    const size_t need = attn::bwd_workspace_bytes(B, Hq, Nq);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    int *status = nullptr;
+    st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::BwdArgs a{q,  k,  v,      o, dout, lse, dq, dk, dv, static_cast<float *>(workspace), kv_lens, status,
+                    B,  Hq, Hkv, Nq, Nkv, d, causal, scale};
+    cudaError_t e = attn::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 ATTN_API int paged_attn_prefill(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,

@@ -37,14 +37,33 @@ struct DecodeArgs {
     int Hkv;  // key/value heads of the cache (H for multi-head; H % Hkv == 0)
 };
 
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dout;  // q, o, dout [B,Hq,Nq,d]; k, v [B,Hkv,Nkv,d] (bf16)
+    const float *lse;                  // [B,Hq,Nq], natural log, from the forward
+    void *dq, *dk, *dv;                // bf16 outputs, shaped like q, k, v
+    float *dterm;                      // workspace: the row term D [B,Hq,Nq]
+    const int32_t *kv_lens;            // may be null
+    int *status;
+    int B, Hq, Hkv, Nq, Nkv, d, causal;
+    float scale;
+};
+
 // Per-device facts looked up once (host-side caches shared by the launchers): the SM count
 // of the current device, and a kernel's dynamic shared-memory opt-in (set once per
 // function and device; cudaFuncSetAttribute is not free on every call).
 cudaError_t current_sm_count(int *sms);
 cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes);
 
+// TMA descriptor of a bf16 [BH, N, D] tensor viewed as 3-D (innermost first) with boxes of
+// 64 x box_rows x 1 and the 128-byte swizzle; rows past N read as zeros.
+bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, int box_rows = 128);
+
 // Encodes the TMA descriptors and launches the prefill kernel.
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Backward: the row term D, then the dK/dV kernel and the dQ kernel.
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream);
+size_t bwd_workspace_bytes(int B, int Hq, int Nq);
 
 // Writes new tokens' K/V into their pages (token t of sequence b goes to position
 // start_pos[b] + t).  Positions past the table's capacity are skipped.

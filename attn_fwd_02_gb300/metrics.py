@@ -18,6 +18,17 @@ def prefill_flops(B: int, H: int, Nq: int, Nkv: int, d: int, causal: bool) -> fl
     return f / 2.0 if causal else f
 
 
+def backward_flops(B: int, H: int, Nq: int, Nkv: int, d: int, causal: bool) -> float:
+    """Backward FLOPs by the usual accounting: five Nq x Nkv x d products (S, dP, dV, dK, dQ)
+    against the forward's two, i.e. 2.5 x prefill_flops.  The dQ kernel recomputes S and dP,
+    so the tensor cores execute 3.5 x prefill_flops (backward_flops_executed)."""
+    return 2.5 * prefill_flops(B, H, Nq, Nkv, d, causal)
+
+
+def backward_flops_executed(B: int, H: int, Nq: int, Nkv: int, d: int, causal: bool) -> float:
+    return 3.5 * prefill_flops(B, H, Nq, Nkv, d, causal)
+
+
 def prefill_flops_kvlen(H: int, Nq: int, d: int, kv_lens) -> float:
     """FLOPs actually required with key padding: 4*H*Nq*d*sum_b(kv_len_b) (non-causal)."""
     return 4.0 * H * Nq * d * float(sum(int(x) for x in kv_lens))

@@ -115,6 +115,13 @@ def prefill_inputs(shape: PrefillShape):
     return dict(q=q, k=k, v=v, kv_lens=kv_lens)
 
 
+def backward_upstream(shape: PrefillShape):
+    """Seeded upstream gradient dO [B, H, Nq, d] (bf16, standard normal) for the backward of a
+    prefill workload; its own seed (shape.seed + 500), so the forward's inputs are unchanged."""
+    g = torch.Generator().manual_seed(shape.seed + 500)
+    return torch.randn(shape.B, shape.H, shape.Nq, shape.d, generator=g).to(torch.bfloat16)
+
+
 POISON_VALUE = 3.0e4
 
 

@@ -295,6 +295,93 @@ def step_flushes_l2(parts) -> bool:
     return sum(getattr(p, "bytes", 0) for p in parts) < 2 * L2_BYTES
 
 
+class BackwardCase:
+    """Backward of a prefill workload (the forward runs once, untimed, for O and LSE)."""
+
+    def __init__(self, shape, torch, A):
+        self.shape, self.A = shape, A
+        inp = workloads.prefill_inputs(shape)
+        do = workloads.backward_upstream(shape)
+        q, k, v = inp["q"], inp["k"], inp["v"]
+        self.dev = {"q": q.cuda(), "k": k.cuda(), "v": v.cuda(), "do": do.cuda()}
+        d = self.dev
+        o, lse = A.attn_fwd(d["q"], d["k"], d["v"], shape.causal, shape.scale)
+        d["o"], d["lse"] = o, lse
+        self.host = {n: t.cpu().pin_memory() for n, t in d.items()}
+        self.dq, self.dk, self.dv = (torch.empty_like(d[n]) for n in ("q", "k", "v"))
+        self.ws = torch.empty(max(A.attn_bwd_workspace_size(shape.B, shape.H, shape.Nq), 16), dtype=torch.uint8,
+                              device="cuda")
+        s = shape
+        self.flops = metrics.backward_flops(s.B, s.H, s.Nq, s.Nkv, s.d, s.causal)
+        self.flops_executed = metrics.backward_flops_executed(s.B, s.H, s.Nq, s.Nkv, s.d, s.causal)
+        # read q, k, v, o, dO once, LSE; write dQ, dK, dV and D
+        qkv = 2.0 * s.B * s.H * s.Nq * s.d
+        self.bytes = 8 * qkv + 8.0 * s.B * s.H * s.Nq
+        self.launches = 3
+        self.dq_host, self.dk_host, self.dv_host = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                                                    for t in (self.dq, self.dk, self.dv))
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.dq, self.dk, self.dv))
+
+    def run(self):
+        d, s = self.dev, self.shape
+        self.A.attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], s.causal, s.scale, dq=self.dq,
+                        dk=self.dk, dv=self.dv, workspace=self.ws)
+
+    def run_e2e(self):
+        for n, t in self.host.items():
+            self.dev[n].copy_(t, non_blocking=True)
+        self.run()
+        self.dq_host.copy_(self.dq, non_blocking=True)
+        self.dk_host.copy_(self.dk, non_blocking=True)
+        self.dv_host.copy_(self.dv, non_blocking=True)
+
+
+def backward_arm(args, torch, A, rank, world, peaks, peak_kind):
+    """Backward of the long-context causal prefill, timed alone (not part of the default step)."""
+    case = BackwardCase(workloads.LONG_CAUSAL, torch, A)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    region_ms, part_ms = time_parts(torch, [case], args.steps, args.warmup, world, sampler, graphs=args.graphs)
+    clocks = sampler.stop() if sampler else None
+    if A.attn_check_device_status() != 0:
+        raise RuntimeError("device status error after the timed region")
+    ms = part_ms[0]
+    achieved = case.flops / (ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    e2e_ms = time_e2e(torch, case, max(3, min(args.steps, 10)), 1, world)
+    s = case.shape
+    out = {"metric": METRIC, "value": round(job_rate(case.flops, world, ms, 1e12), 2), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(region_ms / args.steps, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded torch.randn -> bf16)",
+           "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(achieved / peak, 4), "traffic": None,
+                        "kernel": "attn_bwd (row term + dK/dV + dQ kernels)",
+                        "executed_tflops": round(case.flops_executed / (ms * 1e-3) / 1e12, 2),
+                        "peak_source": f"{peak_kind} bf16_tflops"},
+           "e2e": {"value": round(job_rate(case.flops, world, e2e_ms, 1e12), 2), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": int(case.h2d_bytes), "d2h_bytes_per_step": int(case.d2h_bytes),
+                   "ms_per_step": round(e2e_ms, 3)},
+           "config": {"workload": "backward of " + s.name, "B": s.B, "H": s.H, "Nq": s.Nq, "Nkv": s.Nkv, "d": s.d,
+                      "causal": s.causal, "flops_per_call": case.flops, "flops_executed_per_call": case.flops_executed,
+                      "flops_accounting": "5 products of the forward's size (2.5 x forward); the dQ kernel recomputes "
+                                          "S and dP (3.5 x forward executed)",
+                      "ms_per_call": round(ms, 4), "l2": "inputs larger than L2 (no flush)",
+                      "launch": "CUDA graph replay per call (captured through the API)" if args.graphs
+                      else "direct calls"},
+           "gpu_launches": case.launches * args.steps}
+    if clocks is not None:
+        out["clocks"] = clocks
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def time_parts(torch, parts, steps, warmup, world, sampler=None, graphs=False):
     """Warm up, then time `steps` steps; each step runs every part once.  Returns the
     region time (max over ranks) and each part's mean per-call device time (ms).
@@ -401,6 +488,8 @@ def gpu_arm(args):
         parts = [dec]
     elif args.workload == "prefill_paged":
         return paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind)
+    elif args.workload == "backward":
+        return backward_arm(args, torch, A, rank, world, peaks, peak_kind)
     else:
         pre, dec = PrefillCase(PREFILL_BY_NAME[args.workload], torch, A), None
         parts = [pre]
@@ -619,7 +708,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "prefill_paged",
+    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "prefill_paged", "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

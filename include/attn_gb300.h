@@ -1,7 +1,7 @@
 /*
  * attn_gb300.h -- C ABI of the GB300 (sm_103a) exact-attention library.
  *
- * Two operations, both exact scaled-dot-product attention computed the
+ * Exact scaled-dot-product attention computed the
  * FlashAttention way (K/V streamed in tiles past a resident Q tile, running
  * max m and normaliser l, accumulator rescaled by exp(m_old - m_new), the
  * score matrix never written to memory):
@@ -14,6 +14,9 @@
  *       padding mask before the softmax); llm-kernel-lib README, kernel 1
  *       (causal tile skipping); Kernel-Inference-Engine README, the tile-loop
  *       flowchart (Q tile held, K/V tiles streamed, normalise and store).
+ *
+ *   attn_bwd -- the backward of the prefill forward (dQ, dK, dV from the
+ *       saved log-sum-exp; gpu-inference blog, section 02).
  *
  *   paged_attn_decode -- one query token per sequence attending over a KV
  *       cache split into fixed-size pages reached through a page table; the
@@ -184,6 +187,34 @@ int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v
                     const int32_t *page_table, const int32_t *start_pos, int page_size,
                     int B, int Hkv, int Nnew, int d, int max_pages_per_seq, int num_pages,
                     attn_stream_t stream);
+
+/*
+ * Backward of attn_fwd_gqa: gradients of the loss with respect to q, k and v
+ * given its gradient dout with respect to the forward output.  The method
+ * (gpu-inference blog, section 02 "FlashAttention-2 in Triton"): the
+ * probabilities are recomputed tile by tile from the forward's log-sum-exp
+ * instead of being stored, and the work is three kernels -- the row term
+ * D_i = dO_i . O_i, a dK/dV kernel and a dQ kernel.  With P_ij = exp(s_ij -
+ * LSE_i) on the valid keys (0 elsewhere), dP = dO V^T and dS = P * (dP - D):
+ *   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K;
+ * for grouped-query heads dK and dV of a key/value head sum over the query
+ * heads that read it.  A row with no valid key contributes nothing.
+ *   q, o, dout, dq [B, Hq, Nq, d] bf16    k, v, dk, dv [B, Hkv, Nkv, d] bf16
+ *   lse [B, Hq, Nq] fp32: the forward's log-sum-exp (natural log), required
+ *   o: the forward's output for these inputs (used only for D)
+ *   kv_lens, causal, scale, Hq % Hkv == 0: exactly as in the forward call
+ *   workspace: device scratch of at least attn_bwd_workspace_size(B, Hq, Nq)
+ *       bytes, 16-byte aligned; it holds D [B, Hq, Nq] fp32 when the call ends.
+ * dq, dk and dv are fully written (rows past a sequence's key length get zero
+ * dk/dv).  Products run on bf16 operands with fp32 accumulation: P and dS are
+ * rounded to bf16 before they multiply dO, Q and K.  d in {64, 128}.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Nq,
+             int Nkv, int d, int causal, float scale, const int32_t *kv_lens, void *workspace,
+             size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * paged_attn_decode for callers that cannot allocate device memory.  The pages

@@ -88,6 +88,30 @@ def test_prefill_argument_checks(lib):
     assert lib.attn_fwd(None, ALIGNED, ALIGNED, ALIGNED, None, 1, 1, 1, 1, 64, 0, 0.1, None) == 1
 
 
+def call_bwd(lib, q=ALIGNED, k=ALIGNED, v=ALIGNED, o=ALIGNED, lse=ALIGNED, do=ALIGNED, dq=ALIGNED, dk=ALIGNED,
+             dv=ALIGNED, B=1, Hq=2, Hkv=1, Nq=128, Nkv=128, d=64, causal=1, scale=0.125, kv_lens=None, ws=ALIGNED,
+             wsb=1 << 20):
+    return lib.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, Nq, Nkv, d, causal, scale, kv_lens, ws, wsb,
+                        None)
+
+
+def test_backward_argument_checks(lib):
+    assert lib.attn_bwd_workspace_size(2, 4, 100) == 2 * 4 * 100 * 4 + 256 - (2 * 4 * 100 * 4) % 256
+    assert lib.attn_bwd_workspace_size(0, 4, 100) == 0
+    for name in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"):
+        assert call_bwd(lib, **{name: None}) == 1, name
+    assert call_bwd(lib, Hkv=3) == 1
+    assert call_bwd(lib, causal=5) == 1
+    assert call_bwd(lib, scale=float("nan")) == 1
+    assert call_bwd(lib, d=96) == 2
+    for name in ("q", "o", "do", "dq", "dk", "dv"):
+        assert call_bwd(lib, **{name: ALIGNED + 8}) == 3, name
+    assert call_bwd(lib, lse=ALIGNED + 2) == 3
+    assert call_bwd(lib, ws=None) == 4
+    assert call_bwd(lib, ws=ALIGNED + 4) == 4
+    assert call_bwd(lib, wsb=lib.attn_bwd_workspace_size(1, 2, 128) - 1) == 4
+
+
 def call_dec(lib, q=ALIGNED, kp=ALIGNED, vp=ALIGNED, pt=ALIGNED, cl=ALIGNED, ps=16, o=ALIGNED, lse=None,
              B=2, H=2, d=128, maxp=4, npages=8, scale=0.1, ws=ALIGNED, wsb=1 << 20):
     return lib.paged_attn_decode(q, kp, vp, pt, cl, ps, o, lse, B, H, d, maxp, npages, scale, ws, wsb, None)
