@@ -40,6 +40,10 @@ int device_setup(int **status_out) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Head dims of the prefill kernels (forward, paged prefill, KV append): the set the
+// Kernel-Inference-Engine README instantiates its attention kernel for.  Decode and the
+// backward take 64 and 128.
+bool prefill_head_dim(int d) { return d == 32 || d == 64 || d == 80 || d == 96 || d == 128; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int prefill_checks(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
@@ -49,7 +53,7 @@ int prefill_checks(const void *q, const void *k, const void *v, void *o, float *
     if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;  // finite, positive
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!prefill_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
     // grid = ceil(Nq/128) * B * H CTAs and 32-bit TMA coordinates
     const uint64_t bh = (uint64_t)B * (uint64_t)H;
     const uint64_t ctas = ((uint64_t)Nq + 127) / 128 * bh;
@@ -168,6 +172,7 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
     // q, k, v, dq and the sizes get the forward's checks (dq in the place of o)
     int st = prefill_checks(q, k, v, dq, nullptr, B, Hq, Hkv, Nq, Nkv, d, causal, scale, kv_lens);
     if (st != ATTN_OK) return st;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     const uint64_t kv_ctas = ((uint64_t)Nkv + 127) / 128 * (uint64_t)B * (uint64_t)Hkv;
     if (kv_ctas > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))
@@ -215,7 +220,7 @@ ATTN_API int paged_kv_append(const void *k_new, const void *v_new, void *k_pages
     if (!k_new || !v_new || !k_pages || !v_pages || !page_table || !start_pos) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hkv <= 0 || Nnew <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
         return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!prefill_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
     if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
     if ((uint64_t)max_pages_per_seq * 16 > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
@@ -320,7 +325,7 @@ ATTN_API const char *attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or oversized dimension, bad scale)";
-        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128, page size 16, device sm_103)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 32, 64, 80, 96 or 128 for prefill, 64 or 128 for decode and backward; page size 16; device sm_103)";
         case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment)";
         case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size()";
         case ATTN_ERR_CUDA: return "CUDA runtime error or launch failure";

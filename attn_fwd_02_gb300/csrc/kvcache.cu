@@ -6,7 +6,7 @@
 // Cache"; the "KV-cache append path" on the Kernel-Inference-Engine README's roadmap).
 // Token t of sequence b lands at position pos = start_pos[b] + t: page
 // page_table[b][pos / 16], slot pos % 16, for every key/value head.  Pure data movement:
-// 16 threads copy one d-element row with 16-byte accesses (d = 128) or 8 threads (d = 64).
+// d/8 threads copy one d-element row with 16-byte accesses (d a multiple of 8).
 #include "launch.h"
 #include "sm103_ptx.cuh"
 
@@ -15,18 +15,16 @@ namespace {
 
 constexpr int kPS = 16;
 
-template <int D>
 __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict__ k_new,
                                                         const uint4 *__restrict__ v_new, uint4 *k_pages,
                                                         uint4 *v_pages, const int32_t *__restrict__ page_table,
                                                         const int32_t *__restrict__ start_pos, int B, int Hkv,
-                                                        int Nnew, int max_pages, int num_pages) {
-    constexpr int kVecPerRow = D * 2 / 16;  // 16-byte vectors per row
-    const long long total = (long long)B * Hkv * Nnew * kVecPerRow;
+                                                        int Nnew, int vec_per_row, int max_pages, int num_pages) {
+    const long long total = (long long)B * Hkv * Nnew * vec_per_row;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
-        const int vec = (int)(e % kVecPerRow);
-        const long long row = e / kVecPerRow;  // (b * Hkv + h) * Nnew + t
+        const int vec = (int)(e % vec_per_row);
+        const long long row = e / vec_per_row;  // (b * Hkv + h) * Nnew + t
         const int t = (int)(row % Nnew);
         const int bh = (int)(row / Nnew);
         const int b = bh / Hkv, h = bh % Hkv;
@@ -34,7 +32,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
         if (pos >= max_pages * kPS) continue;  // past the table's capacity
         const int phys = page_table[(size_t)b * max_pages + pos / kPS];
         if (phys < 0 || phys >= num_pages) continue;
-        const size_t dst = (((size_t)phys * Hkv + h) * kPS + (pos % kPS)) * kVecPerRow + vec;
+        const size_t dst = (((size_t)phys * Hkv + h) * kPS + (pos % kPS)) * vec_per_row + vec;
         k_pages[dst] = k_new[e];
         v_pages[dst] = v_new[e];
     }
@@ -52,14 +50,9 @@ cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_pages
     const long long want = (total + 255) / 256;
     const int grid = (int)(want < (long long)sms * 16 ? want : (long long)sms * 16);
     if (grid <= 0) return cudaSuccess;
-    if (d == 128)
-        kv_append_kernel<128><<<grid, 256, 0, stream>>>(
-            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_pages),
-            static_cast<uint4 *>(v_pages), page_table, start_pos, B, Hkv, Nnew, max_pages, num_pages);
-    else
-        kv_append_kernel<64><<<grid, 256, 0, stream>>>(
-            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_pages),
-            static_cast<uint4 *>(v_pages), page_table, start_pos, B, Hkv, Nnew, max_pages, num_pages);
+    kv_append_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+                                               static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages), page_table,
+                                               start_pos, B, Hkv, Nnew, d * 2 / 16, max_pages, num_pages);
     return cudaGetLastError();
 }
 

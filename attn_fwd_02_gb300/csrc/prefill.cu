@@ -43,20 +43,26 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
-// Shape of the CTA per head dimension.
-//   d = 128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 12 warps with a
-//            per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
-//   d = 64:  one query tile per CTA, 6 warps, two CTAs per SM: at d = 64 a tile needs 256 TMEM
-//            columns (S 128 | O 64 | P 64) and 80 KB of shared memory, and two co-resident CTAs
-//            overlap each other's serial chains (Q load, first S, softmax, PV, epilogue), which
-//            dominate the short units of small problems.
-template <int D> struct Cfg;
-template <> struct Cfg<128> {
+// Head dims 32, 64, 80, 96 and 128 (the set the Kernel-Inference-Engine README instantiates its
+// attention kernel for).  Tiles are laid out at a padded width kPad<D> (64 up to d = 64, else
+// 128) in 64-column boxes; TMA fills the columns past d with zeros, the S product runs over d/16
+// k-steps and the PV product has N = d, so the padding costs shared memory but no tensor work.
+template <int D> constexpr int kPad = D <= 64 ? 64 : 128;
+// Shape of the CTA per padded head dimension.
+//   128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 12 warps with a
+//        per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
+//   64:  one query tile per CTA, 6 warps, two CTAs per SM: at d = 64 a tile needs 256 TMEM
+//        columns (S 128 | O 64 | P 64) and 80 KB of shared memory, and two co-resident CTAs
+//        overlap each other's serial chains (Q load, first S, softmax, PV, epilogue), which
+//        dominate the short units of small problems.
+template <int P> struct CfgPad;
+template <int D> struct Cfg : CfgPad<kPad<D>> {};
+template <> struct CfgPad<128> {
     static constexpr int QT = 2, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr bool kSplitRegs = true;
 };
-template <> struct Cfg<64> {
+template <> struct CfgPad<64> {
     static constexpr int QT = 1, kThreads = 192, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 2;
     static constexpr uint32_t kTmemCols = 256;
     static constexpr bool kSplitRegs = false;
@@ -101,9 +107,9 @@ constexpr int kStages = 2;
 
 template <int D>
 struct alignas(1024) PrefillSmem {
-    __nv_bfloat16 q[Cfg<D>::QT][kBM * D];  // D/64 boxes each
-    __nv_bfloat16 k[kStages][kBN * D];     // D/64 boxes each
-    __nv_bfloat16 v[kStages][kBN * D];     // D/64 boxes each
+    __nv_bfloat16 q[Cfg<D>::QT][kBM * kPad<D>];  // kPad/64 boxes each
+    __nv_bfloat16 k[kStages][kBN * kPad<D>];     // kPad/64 boxes each
+    __nv_bfloat16 v[kStages][kBN * kPad<D>];     // kPad/64 boxes each
     uint64_t q_full;
     uint64_t u_full[kStages], u_empty[kStages];
     uint64_t s_full[kQTilesMax];
@@ -125,15 +131,15 @@ __device__ __forceinline__ int kv_end_of(const PrefillParams &p, int b) {
 // columns), so P gets its own columns and S_t(j+1) can be issued as soon as the softmax has
 // read S_t(j), before PV_t(j): the next scores are ready when the softmax finishes a tile.
 // At d = 128 the 512 columns hold exactly S0|S1|O0|O1 and P is written over its scores.
-template <int D> struct SeparateP { static constexpr bool value = (D == 64); };
+template <int D> struct SeparateP { static constexpr bool value = (kPad<D> == 64); };
 
 // TMEM columns: S_t at 128 t; O_t after all S buffers; P_t after all O accumulators when it
 // has its own columns, else over the first 64 columns of S_t.
 template <int D> __device__ __forceinline__ uint32_t o_col(int t) {
-    return (uint32_t)(Cfg<D>::QT * kBN + t * D);
+    return (uint32_t)(Cfg<D>::QT * kBN + t * kPad<D>);
 }
 template <int D> __device__ __forceinline__ uint32_t p_col(int t) {
-    return SeparateP<D>::value ? (uint32_t)(Cfg<D>::QT * (kBN + D) + t * 64) : (uint32_t)(t * kBN);
+    return SeparateP<D>::value ? (uint32_t)(Cfg<D>::QT * (kBN + kPad<D>) + t * 64) : (uint32_t)(t * kBN);
 }
 
 // Key tiles query tile t of this CTA must visit: keys < limit can be valid for some of its rows.
@@ -149,7 +155,7 @@ template <int D>
 __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
                              const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int bh, int bh_kv, int q0,
                              int n_all, WaitCtx wc) {
-    constexpr int kBoxes = D / 64;
+    constexpr int kBoxes = kPad<D> / 64;
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
@@ -508,6 +514,24 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
     }
+    if constexpr (D % 32 != 0) {  // d = 80: the last 16 columns
+        constexpr int c0 = D / 32 * 32;
+        uint32_t ov[16];
+        if (n_tiles > 0) {
+            tmem_ld16(tO + c0, ov);
+            tmem_wait_ld16(ov);
+        }
+        if (store) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                pk[i] = have ? pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l)
+                             : 0u;
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    }
     if (store && p.lse) p.lse[(size_t)bh * p.Nq + row] = have ? kLn2 * (m_ref + __log2f(l)) : -INFINITY;
 }
 
@@ -648,8 +672,14 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
-    if (a.d == 128) return launch_prefill_d<128>(a, stream);
-    return launch_prefill_d<64>(a, stream);
+    switch (a.d) {
+        case 32: return launch_prefill_d<32>(a, stream);
+        case 64: return launch_prefill_d<64>(a, stream);
+        case 80: return launch_prefill_d<80>(a, stream);
+        case 96: return launch_prefill_d<96>(a, stream);
+        case 128: return launch_prefill_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace attn

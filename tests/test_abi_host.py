@@ -79,8 +79,9 @@ def test_prefill_argument_checks(lib):
     assert call_fwd(lib, scale=-1.0) == 1
     assert call_fwd(lib, scale=float("nan")) == 1
     assert call_fwd(lib, scale=float("inf")) == 1
-    assert call_fwd(lib, d=96) == 2
-    assert call_fwd(lib, d=32) == 2
+    assert call_fwd(lib, d=48) == 2
+    assert call_fwd(lib, d=16) == 2
+    assert call_fwd(lib, d=192) == 2
     assert call_fwd(lib, q=ALIGNED + 8) == 3
     assert call_fwd(lib, o=ALIGNED + 2) == 3
     assert call_fwd(lib, lse=ALIGNED + 2) == 3
@@ -104,6 +105,7 @@ def test_backward_argument_checks(lib):
     assert call_bwd(lib, causal=5) == 1
     assert call_bwd(lib, scale=float("nan")) == 1
     assert call_bwd(lib, d=96) == 2
+    assert call_bwd(lib, d=48) == 2
     for name in ("q", "o", "do", "dq", "dk", "dv"):
         assert call_bwd(lib, **{name: ALIGNED + 8}) == 3, name
     assert call_bwd(lib, lse=ALIGNED + 2) == 3
