@@ -454,6 +454,141 @@ int oracle_bwd_rowdot_f64(const uint16_t *o, const uint16_t *dout, int64_t nrows
     return 0;
 }
 
+/* ------------------------------------------------------------------------------------------
+ * FP8 (E4M3) key/value cache.  The NanoInfer README's roadmap names FP8 e4m3 storage (Hopper and
+ * later, cuda_fp8.h) as the successor of INT8 with the quantisation math unchanged; applied to the
+ * attention path that is a KV cache stored as e4m3 codes with one scale per tensor:
+ *   value(code) = e4m3(code) * scale,
+ *   code(x)     = e4m3 rounding of fp32(x) * fp32(1/scale), to nearest with ties to even,
+ *                 saturating at the largest finite magnitude (448).
+ * E4M3 (the OCP FP8 "E4M3" format): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 holds the subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so the
+ * largest finite value is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_value(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 code to y (ties to the even code, i.e. mantissa bit 0 clear), saturating:
+ * magnitudes above 448 give 448.  A brute-force search over the 127 non-negative finite codes,
+ * which saturates by construction (every candidate is finite). */
+uint8_t oracle_e4m3_code(float y) {
+    if (y != y) return 0x7F;
+    const double a = fabs((double)y);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)((y < 0 ? 0x80 : 0) | best);
+}
+
+/* codes[i] = code(fp32(x[i]) * inv_scale): x bf16 bit patterns, the product rounded to fp32. */
+int oracle_e4m3_quantize(const uint16_t *x, int64_t n, float inv_scale, uint8_t *codes) {
+    if (n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        const float y = (float)bf16_to_f64(x[i]) * inv_scale;
+        codes[i] = oracle_e4m3_code(y);
+    }
+    return 0;
+}
+
+/* One query row against n_keys fp64 keys/values (all valid): the three passes of attend_row. */
+static void attend_row_f64kv(const uint16_t *qrow, const double *kb, const double *vb, int n_keys, int d,
+                             double scale, double *srow, double *out, double *lse_out) {
+    double m = -INFINITY;
+    for (int j = 0; j < n_keys; ++j) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_to_f64(qrow[c]) * kb[(size_t)j * d + c];
+        srow[j] = scale * dot;
+        if (j == 0 || srow[j] > m) m = srow[j];
+    }
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    if (n_keys == 0) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int j = 0; j < n_keys; ++j) l += exp(srow[j] - m);
+    for (int j = 0; j < n_keys; ++j) {
+        const double p = exp(srow[j] - m) / l;
+        for (int c = 0; c < d; ++c) out[c] += p * vb[(size_t)j * d + c];
+    }
+    *lse_out = m + log(l);
+}
+
+/* Paged decode over an e4m3 cache: as oracle_paged_decode_gqa_f64 with k_pages/v_pages holding
+ * e4m3 codes [num_pages, Hkv, page_size, d]; each cached value is e4m3(code) * k_scale (keys) or
+ * * v_scale (values), dequantised exactly in fp64 before the plain definition is applied. */
+int oracle_paged_decode_fp8_gqa_f64(const uint16_t *q, const uint8_t *k_pages, const uint8_t *v_pages,
+                                    double k_scale, double v_scale, const int32_t *page_table,
+                                    const int32_t *ctx_lens, int page_size, int B, int Hq, int Hkv, int d,
+                                    int max_pages, int num_pages, double scale, double *o, double *lse,
+                                    int nthreads) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 || max_pages <= 0 ||
+        num_pages <= 0)
+        return 1;
+    const int group = Hq / Hkv;
+    const int cap = max_pages * page_size;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *kc = (double *)malloc(sizeof(double) * (size_t)cap * d);
+        double *vc = (double *)malloc(sizeof(double) * (size_t)cap * d);
+        double *srow = (double *)malloc(sizeof(double) * (size_t)cap);
+        if (!kc || !vc || !srow) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+                const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+                const int n = ctx_lens[b];
+                if (n < 0 || n > cap) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                int bad = 0;
+                for (int t = 0; t < n && !bad; ++t) {
+                    const int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
+                    if (pg < 0 || pg >= num_pages) {
+                        bad = 1;
+                        break;
+                    }
+                    const size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
+                    for (int c = 0; c < d; ++c) {
+                        kc[(size_t)t * d + c] = oracle_e4m3_value(k_pages[src + c]) * k_scale;
+                        vc[(size_t)t * d + c] = oracle_e4m3_value(v_pages[src + c]) * v_scale;
+                    }
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                attend_row_f64kv(q + (size_t)bh * d, kc, vc, n, d, scale, srow, o + (size_t)bh * d, lse + bh);
+            }
+        }
+        free(kc);
+        free(vc);
+        free(srow);
+    }
+    return err;
+}
+
 /* Number of threads OpenMP would use (for reporting the CPU baseline's cores). */
 int oracle_num_threads(int nthreads) {
 #ifdef _OPENMP

@@ -84,6 +84,15 @@ def _load():
             lib.oracle_attn_bwd_gqa_f64.restype = ctypes.c_int
             lib.oracle_bwd_rowdot_f64.argtypes = [P, P, ctypes.c_int64, I, P]
             lib.oracle_bwd_rowdot_f64.restype = ctypes.c_int
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_code.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_code.restype = ctypes.c_uint8
+            lib.oracle_e4m3_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_float, P]
+            lib.oracle_e4m3_quantize.restype = ctypes.c_int
+            lib.oracle_paged_decode_fp8_gqa_f64.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P, P, I, I,
+                                                            I, I, I, I, I, ctypes.c_double, P, P, I]
+            lib.oracle_paged_decode_fp8_gqa_f64.restype = ctypes.c_int
             lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
             lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
             for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
@@ -300,3 +309,56 @@ def bwd_rowdot(o, dout):
     if err:
         raise RuntimeError("oracle_bwd_rowdot_f64 failed")
     return D.reshape(ob.shape[:-1])
+
+
+def e4m3_values() -> np.ndarray:
+    """float64 value of each of the 256 e4m3 codes (NaN for the two NaN codes)."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_value(c) for c in range(256)], np.float64)
+
+
+def e4m3_code(y: float) -> int:
+    """Nearest e4m3 code (ties to even, saturating at 448) of one fp32 value."""
+    return int(_load().oracle_e4m3_code(float(np.float32(y))))
+
+
+def e4m3_quantize(x, scale: float) -> np.ndarray:
+    """e4m3 codes (uint8, same shape) of bf16 x under a per-tensor scale:
+    code(fp32(x) * fp32(1 / scale))."""
+    xb = bf16_bits(x)
+    codes = np.empty(xb.shape, np.uint8)
+    inv = np.float32(1.0) / np.float32(scale)
+    err = _load().oracle_e4m3_quantize(_ptr(xb), xb.size, float(inv), _ptr(codes))
+    if err:
+        raise RuntimeError("oracle_e4m3_quantize failed")
+    return codes
+
+
+def _u8(x) -> np.ndarray:
+    if not isinstance(x, np.ndarray):
+        x = x.detach().cpu().numpy()
+    if x.dtype != np.uint8:
+        raise TypeError("e4m3 codes must be uint8")
+    return np.ascontiguousarray(x)
+
+
+def paged_decode_fp8_gqa(q, k_codes, v_codes, k_scale: float, v_scale: float, page_table, ctx_lens, scale: float,
+                         nthreads: int = 0):
+    """Paged decode over an e4m3 cache (codes uint8 [P,Hkv,page_size,d]; value = e4m3 * scale).
+    Returns (O [B,Hq,d], LSE [B,Hq]) in float64."""
+    qb = bf16_bits(q)
+    kb, vb = _u8(k_codes), _u8(v_codes)
+    B, Hq, d = qb.shape
+    P, Hkv, ps, dk = kb.shape
+    if dk != d or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    pt = _i32(page_table)
+    cl = _i32(ctx_lens)
+    o = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    err = _load().oracle_paged_decode_fp8_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), float(k_scale), float(v_scale),
+                                                  _ptr(pt), _ptr(cl), ps, B, Hq, Hkv, d, pt.shape[1], P, float(scale),
+                                                  _ptr(o), _ptr(lse), nthreads)
+    if err:
+        raise RuntimeError(f"oracle_paged_decode_fp8_gqa_f64 failed ({err})")
+    return o, lse
