@@ -473,7 +473,7 @@ double oracle_e4m3_value(uint8_t code) {
 }
 
 /* Nearest e4m3 code to y (ties to the even code, i.e. mantissa bit 0 clear), saturating:
- * magnitudes above 448 give 448.  A brute-force search over the 127 non-negative finite codes,
+ * magnitudes above 448 give 448.  The sign bit is y's (E4M3 has a signed zero: -0 -> 0x80).  A brute-force search over the 127 non-negative finite codes,
  * which saturates by construction (every candidate is finite). */
 uint8_t oracle_e4m3_code(float y) {
     if (y != y) return 0x7F;
@@ -487,7 +487,7 @@ uint8_t oracle_e4m3_code(float y) {
             best_err = err;
         }
     }
-    return (uint8_t)((y < 0 ? 0x80 : 0) | best);
+    return (uint8_t)((signbit(y) ? 0x80 : 0) | best);  /* the sign is kept, -0 included */
 }
 
 /* codes[i] = code(fp32(x[i]) * inv_scale): x bf16 bit patterns, the product rounded to fp32. */

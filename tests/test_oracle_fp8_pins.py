@@ -61,6 +61,9 @@ def test_e4m3_rounding_is_nearest_ties_even_saturating(oracle_mod):
         assert err[c & 0x7F] == err.min()
         assert (c >> 7) == (1 if y < 0 else 0) or (c & 0x7F) == 0
     assert oracle_mod.e4m3_code(1e9) == 0x7E and oracle_mod.e4m3_code(-500.0) == 0xFE
+    # signed zero: -0 and negatives that round to zero keep the sign bit
+    assert oracle_mod.e4m3_code(-0.0) == 0x80 and oracle_mod.e4m3_code(-1e-6) == 0x80
+    assert oracle_mod.e4m3_code(0.0) == 0x00
 
 
 def test_quantize_applies_the_fp32_inverse_scale(oracle_mod):
@@ -113,7 +116,7 @@ def test_planted_fp8_mistakes_are_caught(oracle_mod, tmp_path):
         "bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
         "subnormal_2^-10": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
         "ties_odd": ("(c & 1) == 0)", "(c & 1) == 1)"),
-        "sign_dropped": ("return (uint8_t)((y < 0 ? 0x80 : 0) | best);", "return (uint8_t)best;"),
+        "sign_dropped": ("return (uint8_t)((signbit(y) ? 0x80 : 0) | best);", "return (uint8_t)best;"),
     }
     for name, (a, b) in mutants.items():
         assert a in src, name
