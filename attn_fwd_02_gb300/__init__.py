@@ -14,12 +14,15 @@ from .binding import (  # noqa: F401
     attn_fwd_gqa,
     attn_fwd_kvlen,
     attn_status_string,
+    kv_quantize_fp8,
     library_path,
     load_library,
     paged_attn_decode,
+    paged_attn_decode_fp8,
     paged_attn_decode_gqa,
     paged_attn_decode_noalloc,
     paged_attn_prefill,
     paged_kv_append,
+    paged_kv_append_fp8,
     paged_attn_decode_workspace_size,
 )

@@ -37,6 +37,9 @@ SIGNATURES = {
     "paged_attn_prefill": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P]),
     "paged_kv_append": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, P]),
     "attn_bwd_workspace_size": (Z, [I, I, I]),
+    "paged_attn_decode_fp8": (I, [P, P, P, F, F, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
+    "kv_quantize_fp8": (I, [P, P, Z, F, P]),
+    "paged_kv_append_fp8": (I, [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, P]),
     "attn_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, Z, P]),
     "attn_check_device_status": (I, [P]),
     "attn_selftest_bounded_wait": (I, [P]),
@@ -158,6 +161,75 @@ def attn_fwd_gqa(q, k, v, causal: bool, scale: float | None = None, kv_lens=None
     st = load_library().attn_fwd_gqa(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, Hq, Hkv, Nq, Nkv,
                                      d, int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
     _check("attn_fwd_gqa", st)
+    return out, lse
+
+
+def kv_quantize_fp8(x, scale: float, out=None, stream=None):
+    """bf16 CUDA tensor -> uint8 e4m3 codes of the same shape under a per-tensor scale
+    (value = e4m3(code) * scale; code = nearest-even e4m3 of fp32(x) * fp32(1/scale), saturating)."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous bf16 CUDA tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    st = load_library().kv_quantize_fp8(_dptr(x), _dptr(out), x.numel(), float(scale), _stream_ptr(stream))
+    _check("kv_quantize_fp8", st)
+    return out
+
+
+def paged_kv_append_fp8(k_new, v_new, k_pages, v_pages, k_scale: float, v_scale: float, page_table, start_pos,
+                        stream=None):
+    """paged_kv_append into an e4m3 cache (k_pages/v_pages uint8 [P,Hkv,16,d]); new K/V bf16
+    [B,Hkv,Nnew,d] are converted with the cache's scales."""
+    import torch
+    _require(k_new, "k_new", torch.bfloat16, 4)
+    _require(v_new, "v_new", torch.bfloat16, 4)
+    _require(k_pages, "k_pages", torch.uint8, 4)
+    _require(v_pages, "v_pages", torch.uint8, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(start_pos, "start_pos", torch.int32, 1)
+    B, Hkv, Nnew, d = k_new.shape
+    P, Hk, ps, dk = k_pages.shape
+    if (Hk, dk) != (Hkv, d) or tuple(v_new.shape) != tuple(k_new.shape) or tuple(v_pages.shape) != tuple(
+            k_pages.shape):
+        raise ValueError("shape mismatch between new K/V and the pages")
+    st = load_library().paged_kv_append_fp8(_dptr(k_new), _dptr(v_new), _dptr(k_pages), _dptr(v_pages),
+                                            float(k_scale), float(v_scale), _dptr(page_table), _dptr(start_pos), ps,
+                                            B, Hkv, Nnew, d, page_table.shape[1], P, _stream_ptr(stream))
+    _check("paged_kv_append_fp8", st)
+
+
+def paged_attn_decode_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float, page_table, ctx_lens,
+                          scale: float | None = None, out=None, lse=None, workspace=None, return_lse: bool = True,
+                          stream=None):
+    """Paged decode over an e4m3 cache: q [B,H,d] bf16; k_pages/v_pages uint8 codes [P,Hkv,16,d]
+    with per-tensor scales.  Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_pages, "k_pages", torch.uint8, 4)
+    _require(v_pages, "v_pages", torch.uint8, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, d = q.shape
+    P, Hkv, ps, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages and v_pages must be [num_pages, Hkv, page_size, d]")
+    if scale is None:
+        scale = d ** -0.5
+    max_pages = page_table.shape[1]
+    lib = load_library()
+    need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, ps))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    st = lib.paged_attn_decode_fp8(_dptr(q), _dptr(k_pages), _dptr(v_pages), float(k_scale), float(v_scale),
+                                   _dptr(page_table), _dptr(ctx_lens), ps, _dptr(out), _dptr(lse), B, H, Hkv, d,
+                                   max_pages, P, float(scale), _dptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("paged_attn_decode_fp8", st)
     return out, lse
 
 

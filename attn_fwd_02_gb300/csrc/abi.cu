@@ -238,6 +238,84 @@ ATTN_API size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pa
     return attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
 }
 
+namespace {
+bool finite_positive(float x) { return x > 0.f && x < 3.0e38f; }
+
+int decode_checks(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                  const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
+                  int max_pages_per_seq, int num_pages, float scale, void *workspace, size_t workspace_bytes) {
+    if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;  // grid y/z limits
+    if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+    if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
+    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    return ATTN_OK;
+}
+}  // namespace
+
+ATTN_API int paged_attn_decode_fp8(const void *q, const void *k_pages, const void *v_pages, float k_scale,
+                                   float v_scale, const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                                   void *o, float *lse, int B, int H, int Hkv, int d, int max_pages_per_seq,
+                                   int num_pages, float scale, void *workspace, size_t workspace_bytes,
+                                   attn_stream_t stream) {
+    int st = decode_checks(q, k_pages, v_pages, page_table, ctx_lens, page_size, o, lse, B, H, Hkv, d,
+                           max_pages_per_seq, num_pages, scale, workspace, workspace_bytes);
+    if (st != ATTN_OK) return st;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return ATTN_ERR_INVALID_ARG;
+    int *status = nullptr;
+    st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, workspace, status, B, H, d, page_size,
+                       max_pages_per_seq, num_pages, scale, Hkv};
+    a.kv_fp8 = 1;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = attn::launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int kv_quantize_fp8(const void *src, void *dst, size_t n, float scale, attn_stream_t stream) {
+    if (!src || !dst || n == 0 || n % 8 != 0 || n > (1ull << 40)) return ATTN_ERR_INVALID_ARG;
+    if (!finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return ATTN_ERR_MISALIGNED;
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = attn::launch_kv_quantize_fp8(src, dst, n, 1.0f / scale, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+ATTN_API int paged_kv_append_fp8(const void *k_new, const void *v_new, void *k_pages, void *v_pages, float k_scale,
+                                 float v_scale, const int32_t *page_table, const int32_t *start_pos, int page_size,
+                                 int B, int Hkv, int Nnew, int d, int max_pages_per_seq, int num_pages,
+                                 attn_stream_t stream) {
+    if (!k_new || !v_new || !k_pages || !v_pages || !page_table || !start_pos) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hkv <= 0 || Nnew <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!finite_positive(k_scale) || !finite_positive(v_scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if ((uint64_t)max_pages_per_seq * 16 > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+        return ATTN_ERR_MISALIGNED;
+    if (!aligned4(page_table) || !aligned4(start_pos)) return ATTN_ERR_MISALIGNED;
+    int *status = nullptr;
+    int st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = attn::launch_kv_append_fp8(k_new, v_new, k_pages, v_pages, 1.0f / k_scale, 1.0f / v_scale,
+                                               page_table, start_pos, B, Hkv, Nnew, d, max_pages_per_seq, num_pages,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 ATTN_API int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_pages,
                                    const int32_t *page_table, const int32_t *ctx_lens, int page_size, void *o,
                                    float *lse, int B, int H, int Hkv, int d, int max_pages_per_seq, int num_pages,

@@ -19,6 +19,13 @@
 // Pass 2 (decode_combine_kernel): per (sequence, head), the partials of all
 // chunks merge with weights 2^(m_s - M):  L = sum l_s 2^(m_s-M),
 // O = sum O_s 2^(m_s-M) / L, LSE = ln2 * (M + log2 L).
+//
+// The cache holds bf16 values, or FP8 E4M3 codes with one scale per tensor (value =
+// e4m3 * scale; the FP8 e4m3 storage on the NanoInfer README's roadmap), which halves the
+// bytes a decode step reads.  The key scale folds into the query's score scale and the value
+// scale into the partial O, so the inner loops only widen codes to fp32.
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "launch.h"
@@ -28,16 +35,20 @@ namespace attn {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kSlots = 3;  // ring slots per warp
+// Ring slots per warp: 3 page blocks (4 KB each for bf16 at d = 128: 96 KB per CTA, 2 CTAs per
+// SM) or 2 for an e4m3 cache (2 KB blocks: 32 KB per CTA, 7 CTAs per SM).  Per byte the e4m3
+// decode does twice the arithmetic (one token is half the bytes), so it gains more from extra
+// warps than from bytes in flight per warp: measured 2 slots > 1 > 3 > 4 > 6.
+template <bool FP8> constexpr int kSlots = FP8 ? 2 : 3;
 constexpr int kPS = 16;    // page size (tokens)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D, int GP>
+template <int D, int GP, bool FP8>
 struct DecodeSmem {
-    // [warp][slot][0 = K, 1 = V][kPS * D] bf16; each block is 16-byte aligned
-    alignas(128) __nv_bfloat16 kv[kWarps][kSlots][2][kPS * D];
-    uint64_t full[kWarps][kSlots];
+    // [warp][slot][0 = K, 1 = V][kPS * D] elements (bf16, or e4m3 bytes); 16-byte aligned blocks
+    alignas(128) uint8_t kv[kWarps][kSlots<FP8>][2][kPS * D * (FP8 ? 1 : 2)];
+    uint64_t full[kWarps][kSlots<FP8>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
     float red_l[kWarps][GP];
@@ -79,6 +90,36 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL
         f[0] = __uint_as_float(u << 16);
         f[1] = __uint_as_float(u & 0xffff0000u);
     }
+}
+
+// Two e4m3 codes (low byte first) -> two fp32 values (exact: every e4m3 value is an fp16 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+// Load DPL consecutive e4m3 codes from shared memory as fp32 (unscaled).
+template <int DPL>
+__device__ __forceinline__ void load_e4m3(const uint8_t *p, float (&f)[DPL]) {
+    if constexpr (DPL == 4) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        const float2 a = e4m3x2_to_float2(u), b = e4m3x2_to_float2(u >> 16);
+        f[0] = a.x;
+        f[1] = a.y;
+        f[2] = b.x;
+        f[3] = b.y;
+    } else {
+        const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t *>(p));
+        f[0] = a.x;
+        f[1] = a.y;
+    }
+}
+
+// DPL consecutive cache elements of one row (bf16 or e4m3) as fp32.
+template <int DPL, bool FP8>
+__device__ __forceinline__ void load_kv(const uint8_t *row, int lane, float (&f)[DPL]) {
+    if constexpr (FP8) load_e4m3<DPL>(row + lane * DPL, f);
+    else load_bf16<DPL>(reinterpret_cast<const __nv_bfloat16 *>(row) + lane * DPL, f);
 }
 
 // Loads DPL consecutive bf16 of global memory (the query) as fp32 scaled by c.
@@ -146,13 +187,15 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
 // One CTA: one chunk of one sequence's cache for one key/value head, applied to GP query
 // heads that share that head (grouped-query attention; GP = 1 for multi-head attention).
 // Grid (chunks, Hkv * gsplit, B): blockIdx.y = kv_head * gsplit + group slice.
-template <int D, int GP>
+template <int D, int GP, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits, int Hkv,
                                                                    int gsplit) {
     constexpr int DPL = D / 32;  // head dims per lane
-    constexpr uint32_t kBlockBytes = kPS * D * 2;
+    constexpr int kElem = FP8 ? 1 : 2;
+    constexpr uint32_t kRowBytes = D * kElem;
+    constexpr uint32_t kBlockBytes = kPS * kRowBytes;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    DecodeSmem<D, GP> &sm = *reinterpret_cast<DecodeSmem<D, GP> *>(smem_raw);
+    DecodeSmem<D, GP, FP8> &sm = *reinterpret_cast<DecodeSmem<D, GP, FP8> *>(smem_raw);
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int kvh = (int)blockIdx.y / gsplit;
@@ -169,7 +212,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
 
     if (threadIdx.x == 0) {
         for (int w = 0; w < kWarps; ++w)
-            for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[w][s], 1);
+            for (int s = 0; s < kSlots<FP8>; ++s) mbar_init(&sm.full[w][s], 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -181,28 +224,29 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     if (lane < nk) my_pid = a.page_table[(size_t)b * a.max_pages + page0 + warp + kWarps * lane];
     const bool my_ok = (my_pid >= 0 && my_pid < a.num_pages);
 
-    const __nv_bfloat16 *kbase = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-    const __nv_bfloat16 *vbase = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(a.k_pages);
+    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(a.v_pages);
     auto issue = [&](int k) {
         const int pid = __shfl_sync(0xffffffffu, my_pid, k);
         const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
         if (lane == 0) {
-            uint64_t *bar = &sm.full[warp][k % kSlots];
+            uint64_t *bar = &sm.full[warp][k % kSlots<FP8>];
             if (ok) {
-                const size_t off = ((size_t)pid * Hkv + kvh) * (size_t)(kPS * D);
+                const size_t off = ((size_t)pid * Hkv + kvh) * (size_t)kBlockBytes;
                 mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
-                bulk_load(sm.kv[warp][k % kSlots][0], kbase + off, kBlockBytes, bar);
-                bulk_load(sm.kv[warp][k % kSlots][1], vbase + off, kBlockBytes, bar);
+                bulk_load(sm.kv[warp][k % kSlots<FP8>][0], kbase + off, kBlockBytes, bar);
+                bulk_load(sm.kv[warp][k % kSlots<FP8>][1], vbase + off, kBlockBytes, bar);
             } else {
                 mbar_arrive(bar);  // nothing to load: complete the phase so the consumer stays in step
             }
         }
     };
-    const int first = nk < kSlots ? nk : kSlots;
+    const int first = nk < kSlots<FP8> ? nk : kSlots<FP8>;
     for (int k = 0; k < first; ++k) issue(k);
 
-    // Queries, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k
-    const float c = a.scale * kLog2e;
+    // Queries, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k (times the key scale
+    // of an e4m3 cache, whose codes are then used as they are)
+    const float c = a.scale * kLog2e * (FP8 ? a.k_scale : 1.f);
     float qf[GP][DPL];
 #pragma unroll
     for (int g = 0; g < GP; ++g)
@@ -221,8 +265,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     int issued = first;
     bool failed = false;
     for (int k = 0; k < nk; ++k) {
-        const int slot = k % kSlots;
-        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSlots) & 1), wc, 100 + warp)) {
+        const int slot = k % kSlots<FP8>;
+        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSlots<FP8>) & 1), wc, 100 + warp)) {
             failed = true;
             break;
         }
@@ -230,12 +274,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
         const int ntok = min(kPS, tok1 - page_tok0);
         if (ok) {
-            const __nv_bfloat16 *Ks = sm.kv[warp][slot][0];
-            const __nv_bfloat16 *Vs = sm.kv[warp][slot][1];
+            const uint8_t *Ks = sm.kv[warp][slot][0];
+            const uint8_t *Vs = sm.kv[warp][slot][1];
             // this lane's DPL dims of the 16 keys, read once and used for every query head
             float kf[16][DPL];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) load_bf16<DPL>(Ks + t * D + lane * DPL, kf[t]);
+            for (int t = 0; t < 16; ++t) load_kv<DPL, FP8>(Ks + t * kRowBytes, lane, kf[t]);
             float p[GP];  // lane L: probability of token L >> 1, per query head
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
@@ -259,7 +303,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             }
             for (int t = 0; t < ntok; ++t) {
                 float vf[DPL];
-                load_bf16<DPL>(Vs + t * D + lane * DPL, vf);
+                load_kv<DPL, FP8>(Vs + t * kRowBytes, lane, vf);
 #pragma unroll
                 for (int g = 0; g < GP; ++g) {
                     const float pt = __shfl_sync(0xffffffffu, p[g], 2 * t);
@@ -271,8 +315,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         // the slot is free again: order this warp's reads before the next bulk write
         fence_proxy_async_smem();
         __syncwarp();
-        if (k + kSlots < nk) {
-            issue(k + kSlots);
+        if (k + kSlots<FP8> < nk) {
+            issue(k + kSlots<FP8>);
             ++issued;
         }
     }
@@ -280,8 +324,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         // drain this warp's copies still in flight (bounded) before the CTA exits
         WaitCtx drain{nullptr, a.status};
         for (int k = 0; k < issued; ++k) {
-            if (lane == 0 && k + kSlots >= issued)  // the last use of each slot
-                (void)mbar_wait(&sm.full[warp][k % kSlots], (uint32_t)((k / kSlots) & 1), drain, 199);
+            if (lane == 0 && k + kSlots<FP8> >= issued)  // the last use of each slot
+                (void)mbar_wait(&sm.full[warp][k % kSlots<FP8>], (uint32_t)((k / kSlots<FP8>) & 1), drain, 199);
         }
         __syncwarp();
     }
@@ -314,7 +358,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         }
         float *ws = reinterpret_cast<float *>(a.workspace) +
                     (((size_t)b * a.H + qh0 + g) * max_splits + split) * (size_t)ws_stride<D>();
-        ws[dd] = O;
+        ws[dd] = FP8 ? O * a.v_scale : O;
         if (dd == 0) {
             ws[D] = M;
             ws[D + 1] = L;
@@ -348,15 +392,22 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, i
     if (dd == 0 && a.lse) a.lse[row] = any ? kLn2 * (M + __log2f(L)) : -INFINITY;
 }
 
-template <int D, int GP>
+template <int D, int GP, bool FP8>
 cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
-    const size_t smem = sizeof(DecodeSmem<D, GP>);
-    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_split_kernel<D, GP>), (int)smem);
+    const size_t smem = sizeof(DecodeSmem<D, GP, FP8>);
+    cudaError_t e =
+        ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_split_kernel<D, GP, FP8>), (int)smem);
     if (e != cudaSuccess) return e;
     const int gsplit = (a.H / a.Hkv) / GP;  // CTAs per key/value head
     dim3 g1(max_splits, a.Hkv * gsplit, a.B);
-    decode_split_kernel<D, GP><<<g1, kWarps * 32, smem, stream>>>(a, max_splits, a.Hkv, gsplit);
+    decode_split_kernel<D, GP, FP8><<<g1, kWarps * 32, smem, stream>>>(a, max_splits, a.Hkv, gsplit);
     return cudaGetLastError();
+}
+
+template <int D, int GP>
+cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
+    return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, stream)
+                    : launch_decode_g<D, GP, false>(a, max_splits, stream);
 }
 
 template <int D>
@@ -365,10 +416,10 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     // query heads per CTA: the largest of 8, 4, 2, 1 dividing the group size
     const int group = a.H / a.Hkv;
     cudaError_t e;
-    if (group % 8 == 0) e = launch_decode_g<D, 8>(a, max_splits, stream);
-    else if (group % 4 == 0) e = launch_decode_g<D, 4>(a, max_splits, stream);
-    else if (group % 2 == 0) e = launch_decode_g<D, 2>(a, max_splits, stream);
-    else e = launch_decode_g<D, 1>(a, max_splits, stream);
+    if (group % 8 == 0) e = launch_decode_gk<D, 8>(a, max_splits, stream);
+    else if (group % 4 == 0) e = launch_decode_gk<D, 4>(a, max_splits, stream);
+    else if (group % 2 == 0) e = launch_decode_gk<D, 2>(a, max_splits, stream);
+    else e = launch_decode_gk<D, 1>(a, max_splits, stream);
     if (e != cudaSuccess) return e;
     dim3 g2(a.H, a.B);
     decode_combine_kernel<D><<<g2, D, 0, stream>>>(a, max_splits);

@@ -35,6 +35,9 @@ struct DecodeArgs {
     int B, H, d, page_size, max_pages, num_pages;
     float scale;
     int Hkv;  // key/value heads of the cache (H for multi-head; H % Hkv == 0)
+    // e4m3 cache: pages hold FP8 codes, value = e4m3(code) * k_scale (keys) or * v_scale (values)
+    int kv_fp8 = 0;
+    float k_scale = 1.f, v_scale = 1.f;
 };
 
 struct BwdArgs {
@@ -70,6 +73,15 @@ size_t bwd_workspace_bytes(int B, int Hq, int Nq);
 cudaError_t launch_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
                              const int32_t *page_table, const int32_t *start_pos, int B, int Hkv, int Nnew, int d,
                              int max_pages, int num_pages, cudaStream_t stream);
+
+// FP8 (E4M3) cache conversion: codes = e4m3_rn_satfinite(fp32(x) * inv_scale).
+//   kv_quantize_fp8: n contiguous bf16 elements -> n codes (n % 8 == 0).
+//   kv_append_fp8: as launch_kv_append, converting each new element on the way into the pages.
+cudaError_t launch_kv_quantize_fp8(const void *src, void *dst, size_t n, float inv_scale, cudaStream_t stream);
+cudaError_t launch_kv_append_fp8(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                                 float k_inv_scale, float v_inv_scale, const int32_t *page_table,
+                                 const int32_t *start_pos, int B, int Hkv, int Nnew, int d, int max_pages,
+                                 int num_pages, cudaStream_t stream);
 
 // Launches the split kernel and the combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

@@ -46,13 +46,14 @@ def prefill_bytes(B: int, H: int, Nq: int, Nkv: int, d: int, elem: int = 2, lse:
 
 
 def decode_bytes(H: int, d: int, ctx_lens, page_size: int, elem: int = 2, lse: bool = True,
-                 kv_heads: int | None = None) -> float:
-    """K and V of every cached token once (kv_heads cache heads, default H), q and o once,
-    LSE fp32, page-table entries used."""
+                 kv_heads: int | None = None, kv_elem: int | None = None) -> float:
+    """K and V of every cached token once (kv_heads cache heads, default H; kv_elem bytes per
+    cached element, default elem: 1 for an e4m3 cache), q and o once (elem bytes), LSE fp32,
+    page-table entries used."""
     ctx = [int(x) for x in ctx_lens]
     B = len(ctx)
     Hkv = H if kv_heads is None else kv_heads
-    kv = 2.0 * Hkv * d * elem * float(sum(ctx))
+    kv = 2.0 * Hkv * d * (elem if kv_elem is None else kv_elem) * float(sum(ctx))
     qo = 2.0 * B * H * d * elem
     pt = 4.0 * float(sum(-(-c // page_size) for c in ctx))
     return kv + qo + pt + (4.0 * B * H if lse else 0.0)

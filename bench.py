@@ -264,6 +264,28 @@ class DecodeCase:
         self.lse_host.copy_(self.lse, non_blocking=True)
 
 
+class DecodeFp8Case(DecodeCase):
+    """Paged decode over an e4m3 cache: the bf16 pages of the workload converted on the GPU
+    with kv_quantize_fp8 (per-tensor scale 6/448), then decoded with paged_attn_decode_fp8."""
+    SCALE = 6.0 / 448
+
+    def __init__(self, shape, torch, A, kv_heads=None):
+        super().__init__(shape, torch, A, kv_heads=kv_heads)
+        d = self.dev
+        for n in ("k_pages", "v_pages"):
+            codes = A.kv_quantize_fp8(d[n], self.SCALE)
+            d[n] = codes
+            self.host[n] = codes.cpu().pin_memory()
+        torch.cuda.synchronize()
+        self.bytes = metrics.decode_bytes(shape.H, shape.d, self.ctx, shape.page_size, kv_heads=kv_heads, kv_elem=1)
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
+
+    def run(self):
+        d = self.dev
+        self.A.paged_attn_decode_fp8(d["q"], d["k_pages"], d["v_pages"], self.SCALE, self.SCALE, d["page_table"],
+                                     d["ctx_lens"], self.shape.scale, out=self.o, lse=self.lse, workspace=self.ws)
+
+
 class PagedPrefillCase:
     """Chunked prefill over the paged cache (queries = the last Nq cached positions)."""
 
@@ -478,9 +500,11 @@ def gpu_arm(args):
         pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
         dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
         parts = [pre, dec]
-    elif args.workload in ("decode", "decode_small", "decode_gqa"):
+    elif args.workload in ("decode", "decode_small", "decode_gqa", "decode_fp8"):
         if args.workload == "decode_gqa":
             dec = DecodeCase(workloads.PAGED_DECODE_GQA, torch, A, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
+        elif args.workload == "decode_fp8":
+            dec = DecodeFp8Case(workloads.PAGED_DECODE, torch, A)
         else:
             shape = workloads.PAGED_DECODE if args.workload == "decode" else workloads.PAGED_DECODE_SMALL
             dec = DecodeCase(shape, torch, A)
@@ -545,6 +569,10 @@ def gpu_arm(args):
         s = dec.shape
         cfg["decode"] = {"workload": s.name, "B": s.B, "H": s.H, "d": s.d, "page_size": s.page_size,
                          "ctx_range": s.ctx_range, "ctx_total": sum(dec.ctx)}
+        if dec.kv_heads is not None:
+            cfg["decode"]["Hkv"] = dec.kv_heads
+        if isinstance(dec, DecodeFp8Case):
+            cfg["decode"]["kv_cache"] = f"e4m3 codes, per-tensor scale {dec.SCALE:.6g} (kv_quantize_fp8)"
         if pre is None:
             out["value"], out["unit"] = dec_obj["value"], "GB/s"
             out["roofline"] = dec_obj["roofline"]
@@ -640,10 +668,14 @@ def cpu_baseline(pre, dec, budget_s):
         out.update(value=round(flops / t / 1e12, 6), unit="TFLOP/s",
                    sample=f"{rows} seeded random query rows of {pre.shape.name} ({t:.1f} s of fp64 C, OpenMP)")
     if dec is not None:
-        inp = workloads.decode_inputs(dec.shape)
+        inp = workloads.decode_inputs(dec.shape, kv_heads=dec.kv_heads)
         t = time.perf_counter()
-        oracle.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
-                            dec.shape.scale)
+        if isinstance(dec, DecodeFp8Case):  # timing only: the codes the benchmark decodes
+            oracle.paged_decode_fp8_gqa(inp["q"], dec.host["k_pages"], dec.host["v_pages"], dec.SCALE, dec.SCALE,
+                                        inp["page_table"], inp["ctx_lens"], dec.shape.scale)
+        else:
+            oracle.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                    dec.shape.scale)
         t = time.perf_counter() - t
         dobj = {"value": round(dec.bytes / t / 1e9, 3), "unit": "GB/s",
                 "sample": f"the whole {dec.shape.name} ({t:.1f} s)"}
@@ -708,7 +740,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "prefill_paged", "backward",
+    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8",
+                                           "prefill_paged", "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

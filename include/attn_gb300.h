@@ -50,7 +50,9 @@
  *   - Every wait inside a kernel is bounded.  A wait that runs out sets a
  *     device status word (ATTN_ERR_DEVICE_TIMEOUT) and the kernel exits
  *     cleanly; attn_check_device_status() reports and clears it.
- *   - Supported: head dim d in {64, 128}; page_size 16.
+ *   - Supported: head dim d in {32, 64, 80, 96, 128} for the prefill entry
+ *     points (forward, paged prefill, KV append), {64, 128} for decode and the
+ *     backward; page_size 16.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -68,7 +70,7 @@ typedef struct CUstream_st *attn_stream_t;
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, size overflow */
-    ATTN_ERR_UNSUPPORTED = 2,     /* d not in {64,128}, page_size != 16, no sm_103 device */
+    ATTN_ERR_UNSUPPORTED = 2,     /* head dim not supported by the call, page_size != 16, no sm_103 device */
     ATTN_ERR_MISALIGNED = 3,      /* a tensor pointer not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,       /* workspace missing, misaligned or too small */
     ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call or launch failed */
@@ -187,6 +189,38 @@ int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v
                     const int32_t *page_table, const int32_t *start_pos, int page_size,
                     int B, int Hkv, int Nnew, int d, int max_pages_per_seq, int num_pages,
                     attn_stream_t stream);
+
+/*
+ * FP8 KV cache.  The NanoInfer README's roadmap names FP8 e4m3 storage (cuda_fp8.h
+ * __nv_fp8_e4m3) as the successor of INT8 with the quantisation math unchanged;
+ * here it is the storage of the paged KV cache, which halves the bytes a decode
+ * step reads.  A cache tensor holds E4M3 codes (1 sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits, no infinities, largest finite 448) with one scale per
+ * tensor:  value = e4m3(code) * scale.  Conversion from bf16:
+ *   code = e4m3 nearest-even rounding of fp32(x) * fp32(1 / scale), saturating at
+ *          +-448 (1 / scale is computed in fp32 on the host).
+ *
+ * paged_attn_decode_fp8: paged_attn_decode_gqa over an e4m3 cache (k_pages,
+ *   v_pages [num_pages, Hkv, page_size, d] uint8 codes; k_scale, v_scale > 0
+ *   and finite).  q, o, lse, the table, the workspace and the result are as in
+ *   paged_attn_decode_gqa, for the dequantised cache.
+ * kv_quantize_fp8: n contiguous bf16 elements of src -> n codes in dst (n a
+ *   multiple of 8; both 16-byte aligned).  Converts a whole bf16 page pool.
+ * paged_kv_append_fp8: paged_kv_append into an e4m3 cache, converting each new
+ *   element with the tensor's scale (d in {64, 128}).
+ */
+int paged_attn_decode_fp8(const void *q, const void *k_pages, const void *v_pages, float k_scale,
+                          float v_scale, const int32_t *page_table, const int32_t *ctx_lens,
+                          int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
+                          int max_pages_per_seq, int num_pages, float scale, void *workspace,
+                          size_t workspace_bytes, attn_stream_t stream);
+
+int kv_quantize_fp8(const void *src, void *dst, size_t n, float scale, attn_stream_t stream);
+
+int paged_kv_append_fp8(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
+                        float k_scale, float v_scale, const int32_t *page_table,
+                        const int32_t *start_pos, int page_size, int B, int Hkv, int Nnew, int d,
+                        int max_pages_per_seq, int num_pages, attn_stream_t stream);
 
 /*
  * Backward of attn_fwd_gqa: gradients of the loss with respect to q, k and v

@@ -490,13 +490,20 @@ uint8_t oracle_e4m3_code(float y) {
     return (uint8_t)((signbit(y) ? 0x80 : 0) | best);  /* the sign is kept, -0 included */
 }
 
-/* codes[i] = code(fp32(x[i]) * inv_scale): x bf16 bit patterns, the product rounded to fp32. */
+/* codes[i] = code(fp32(x[i]) * inv_scale): x bf16 bit patterns, the product rounded to fp32.
+ * The code depends only on x[i]'s bit pattern, so it is worked out once per pattern (65536
+ * calls of oracle_e4m3_code) and looked up. */
 int oracle_e4m3_quantize(const uint16_t *x, int64_t n, float inv_scale, uint8_t *codes) {
     if (n < 0) return 1;
-    for (int64_t i = 0; i < n; ++i) {
-        const float y = (float)bf16_to_f64(x[i]) * inv_scale;
-        codes[i] = oracle_e4m3_code(y);
+    uint8_t *table = (uint8_t *)malloc(65536);
+    if (!table) return 2;
+    for (int b = 0; b < 65536; ++b) {
+        const float y = (float)bf16_to_f64((uint16_t)b) * inv_scale;
+        table[b] = oracle_e4m3_code(y);
     }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) codes[i] = table[x[i]];
+    free(table);
     return 0;
 }
 

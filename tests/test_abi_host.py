@@ -114,6 +114,28 @@ def test_backward_argument_checks(lib):
     assert call_bwd(lib, wsb=lib.attn_bwd_workspace_size(1, 2, 128) - 1) == 4
 
 
+def test_fp8_argument_checks(lib):
+    q = ALIGNED
+    # decode over an e4m3 cache: the decode checks plus positive, finite cache scales
+    dec = lambda **kw: lib.paged_attn_decode_fp8(
+        kw.get("q", q), ALIGNED, ALIGNED, kw.get("ks", 0.1), kw.get("vs", 0.1), ALIGNED, ALIGNED, 16, ALIGNED, None,
+        2, kw.get("H", 2), kw.get("Hkv", 2), kw.get("d", 128), 4, 8, 0.1, kw.get("ws", ALIGNED), 1 << 20, None)
+    assert dec(q=None) == 1
+    assert dec(ks=0.0) == 1 and dec(vs=float("inf")) == 1 and dec(ks=float("nan")) == 1
+    assert dec(Hkv=3) == 1
+    assert dec(d=80) == 2
+    assert dec(q=ALIGNED + 4) == 3
+    assert dec(ws=None) == 4
+    assert lib.kv_quantize_fp8(None, ALIGNED, 64, 1.0, None) == 1
+    assert lib.kv_quantize_fp8(ALIGNED, ALIGNED, 12, 1.0, None) == 1  # not a multiple of 8
+    assert lib.kv_quantize_fp8(ALIGNED, ALIGNED, 64, -1.0, None) == 1
+    assert lib.kv_quantize_fp8(ALIGNED + 8, ALIGNED, 64, 1.0, None) == 3
+    app = lambda **kw: lib.paged_kv_append_fp8(ALIGNED, ALIGNED, ALIGNED, ALIGNED, kw.get("ks", 1.0), 1.0,
+                                               kw.get("pt", ALIGNED), ALIGNED, 16, 1, 1, 4, kw.get("d", 64), 4, 8,
+                                               None)
+    assert app(pt=None) == 1 and app(ks=0.0) == 1 and app(d=96) == 2
+
+
 def call_dec(lib, q=ALIGNED, kp=ALIGNED, vp=ALIGNED, pt=ALIGNED, cl=ALIGNED, ps=16, o=ALIGNED, lse=None,
              B=2, H=2, d=128, maxp=4, npages=8, scale=0.1, ws=ALIGNED, wsb=1 << 20):
     return lib.paged_attn_decode(q, kp, vp, pt, cl, ps, o, lse, B, H, d, maxp, npages, scale, ws, wsb, None)

@@ -1,0 +1,114 @@
+"""GPU parity for the FP8 (E4M3) KV cache: conversion bit-exact against the oracle's code table
+(every finite bf16 value, several scales), the FP8 KV append bit-exact against the oracle's
+quantisation and a direct scatter, and decode over e4m3 pages against the fp64 oracle (same
+tolerances as the bf16 decode: O max-abs <= 1e-2, mean-abs <= 1e-3, LSE abs <= 1e-3; the
+oracle dequantises the codes exactly, the kernel widens them exactly, so only fp32 arithmetic
+and the bf16 output separate the two)."""
+import numpy as np
+import pytest
+import torch
+
+from attn_fwd_02_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+O_MAX, O_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
+KV_SCALE = 6.0 / 448  # N(0,1) data: values beyond +-6 saturate
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attn_fwd_02_gb300 import binding, build
+    build.build()
+    return binding
+
+
+def all_finite_bf16():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = ((bits >> 7) & 0xFF) != 0xFF
+    return torch.from_numpy(bits[finite].view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("scale", [1.0, KV_SCALE, 0.37, 1e-3, 250.0])
+def test_quantize_every_finite_bf16_bit_exact(lib, oracle_mod, scale):
+    x = all_finite_bf16()
+    x = x[: x.numel() // 8 * 8].contiguous()
+    got = lib.kv_quantize_fp8(x.cuda(), scale)
+    torch.cuda.synchronize()
+    want = oracle_mod.e4m3_quantize(x, scale)
+    g = got.cpu().numpy()
+    bad = np.nonzero(g != want)[0]
+    assert bad.size == 0, f"{bad.size} codes differ, e.g. x={x[bad[0]].item()} got {g[bad[0]]:#x} want {want[bad[0]]:#x}"
+
+
+def test_append_fp8_bit_exact(lib, oracle_mod):
+    B, Hkv, d, Nnew = 3, 2, 128, 37
+    shape = workloads.DecodeShape("fp8 append", B, 4, d, (1, 400), seed=700)
+    inp = workloads.decode_inputs(shape, ctx_lens=[400, 100, 250], kv_heads=Hkv)
+    start = torch.tensor([363, 0, 213], dtype=torch.int32)
+    g = torch.Generator().manual_seed(701)
+    kn = torch.randn(B, Hkv, Nnew, d, generator=g).to(torch.bfloat16)
+    vn = (torch.randn(B, Hkv, Nnew, d, generator=g) * 3).to(torch.bfloat16)
+    ks, vs = KV_SCALE, 2 * KV_SCALE
+    kp = torch.from_numpy(oracle_mod.e4m3_quantize(inp["k_pages"], ks))
+    vp = torch.from_numpy(oracle_mod.e4m3_quantize(inp["v_pages"], vs))
+    kq = torch.from_numpy(oracle_mod.e4m3_quantize(kn, ks))
+    vq = torch.from_numpy(oracle_mod.e4m3_quantize(vn, vs))
+    kd, vd = kp.cuda(), vp.cuda()
+    for b in range(B):
+        for t in range(Nnew):
+            pos = int(start[b]) + t
+            pg = int(inp["page_table"][b, pos // 16])
+            kp[pg, :, pos % 16] = kq[b, :, t]
+            vp[pg, :, pos % 16] = vq[b, :, t]
+    lib.paged_kv_append_fp8(kn.cuda(), vn.cuda(), kd, vd, ks, vs, inp["page_table"].cuda(), start.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu(), kp) and torch.equal(vd.cpu(), vp)
+
+
+def run_fp8_decode(lib, oracle_mod, shape, ctx=None, kv_heads=None, ks=KV_SCALE, vs=KV_SCALE):
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=kv_heads)
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], ks)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], vs)
+    o = torch.full(inp["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(inp["q"].shape[:2], float("nan"), device="cuda")
+    lib.paged_attn_decode_fp8(inp["q"].cuda(), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(), ks, vs,
+                              inp["page_table"].cuda(), inp["ctx_lens"].cuda(), shape.scale, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_decode_fp8_gqa(inp["q"], kc, vc, ks, vs, inp["page_table"], inp["ctx_lens"],
+                                                     shape.scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    err = np.abs(og - o_ref)
+    assert np.isfinite(og).all() and err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.abs(lg - lse_ref).max() <= LSE_MAX
+    return err.max(), err.mean()
+
+
+CASES = [
+    # name, B, H, Hkv, d, ctx
+    ("d128 MHA ragged", 4, 4, 4, 128, [1, 17, 513, 2000]),
+    ("d64 MHA", 3, 2, 2, 64, [16, 1024, 777]),
+    ("d128 GQA 4", 3, 8, 2, 128, [5, 600, 1500]),
+    ("d64 MQA 8", 2, 8, 1, 64, [300, 1025]),
+    ("d128 GQA chunk edges", 2, 4, 1, 128, [512, 1536]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fp8_decode_vs_oracle(lib, oracle_mod, case):
+    name, B, H, Hkv, d, ctx = case
+    shape = workloads.DecodeShape(name, B, H, d, (1, max(ctx)), seed=710 + len(name))
+    run_fp8_decode(lib, oracle_mod, shape, ctx=ctx, kv_heads=Hkv)
+
+
+def test_fp8_decode_unequal_scales(lib, oracle_mod):
+    shape = workloads.DecodeShape("scales", 2, 4, 128, (1, 900), seed=720)
+    run_fp8_decode(lib, oracle_mod, shape, ctx=[900, 33], ks=0.02, vs=0.5)
+
+
+def test_fp8_decode_full_size(lib, oracle_mod):
+    # the paged-decode workload (B=32, H=32, d=128, ctx U[512,8192]) with its cache in e4m3
+    run_fp8_decode(lib, oracle_mod, workloads.PAGED_DECODE)

@@ -66,6 +66,20 @@ def test_e4m3_rounding_is_nearest_ties_even_saturating(oracle_mod):
     assert oracle_mod.e4m3_code(0.0) == 0x00
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.37, 6.0 / 448])
+def test_quantize_equals_code_of_the_scaled_value(oracle_mod, scale):
+    # the bulk quantiser is code(fp32(x) * fp32(1/scale)) for every finite bf16 x
+    bits = np.arange(0, 65536, 97, dtype=np.uint32).astype(np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    codes = oracle_mod.e4m3_quantize(x, scale)
+    inv = np.float32(1.0) / np.float32(scale)
+    xs = x.float().numpy()
+    with np.errstate(over="ignore"):  # products past the fp32 range become inf and saturate
+        for xi, c in zip(xs, codes):
+            assert c == oracle_mod.e4m3_code(np.float32(xi) * inv)
+
+
 def test_quantize_applies_the_fp32_inverse_scale(oracle_mod):
     x = torch.tensor([1.0, -2.0, 0.0078125, 100.0, 3.0e4]).to(torch.bfloat16)
     codes = oracle_mod.e4m3_quantize(x, 0.5)  # x * 2
