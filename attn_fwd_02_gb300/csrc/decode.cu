@@ -35,11 +35,13 @@ namespace attn {
 namespace {
 
 constexpr int kWarps = 4;
-// Ring slots per warp: 3 page blocks (4 KB each for bf16 at d = 128: 96 KB per CTA, 2 CTAs per
-// SM) or 2 for an e4m3 cache (2 KB blocks: 32 KB per CTA, 7 CTAs per SM).  Per byte the e4m3
-// decode does twice the arithmetic (one token is half the bytes), so it gains more from extra
-// warps than from bytes in flight per warp: measured 2 slots > 1 > 3 > 4 > 6.
-template <bool FP8> constexpr int kSlots = FP8 ? 2 : 3;
+// Ring slots per warp: 3 page blocks for a bf16 cache and one query head per CTA (4 KB each at
+// d = 128: 96 KB per CTA, 2 CTAs per SM); 2 when the arithmetic per byte is higher -- an e4m3
+// cache (half the bytes per token; 2 KB blocks, 32 KB per CTA, 7 CTAs per SM) or several query
+// heads per CTA (grouped-query) -- where extra warps help more than bytes in flight per warp.
+// Measured: e4m3 2 slots > 1 > 3 > 4 > 6; grouped-query bf16 2 slots 4.50 TB/s, 3 or 1 slots
+// 3.94 TB/s.
+template <bool FP8, int GP> constexpr int kSlotsFor = (FP8 || GP > 1) ? 2 : 3;
 constexpr int kPS = 16;    // page size (tokens)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -47,8 +49,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D, int GP, bool FP8>
 struct DecodeSmem {
     // [warp][slot][0 = K, 1 = V][kPS * D] elements (bf16, or e4m3 bytes); 16-byte aligned blocks
-    alignas(128) uint8_t kv[kWarps][kSlots<FP8>][2][kPS * D * (FP8 ? 1 : 2)];
-    uint64_t full[kWarps][kSlots<FP8>];
+    alignas(128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kPS * D * (FP8 ? 1 : 2)];
+    uint64_t full[kWarps][kSlotsFor<FP8, GP>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
     float red_l[kWarps][GP];
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
 
     if (threadIdx.x == 0) {
         for (int w = 0; w < kWarps; ++w)
-            for (int s = 0; s < kSlots<FP8>; ++s) mbar_init(&sm.full[w][s], 1);
+            for (int s = 0; s < kSlotsFor<FP8, GP>; ++s) mbar_init(&sm.full[w][s], 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -230,18 +232,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         const int pid = __shfl_sync(0xffffffffu, my_pid, k);
         const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
         if (lane == 0) {
-            uint64_t *bar = &sm.full[warp][k % kSlots<FP8>];
+            uint64_t *bar = &sm.full[warp][k % kSlotsFor<FP8, GP>];
             if (ok) {
                 const size_t off = ((size_t)pid * Hkv + kvh) * (size_t)kBlockBytes;
                 mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
-                bulk_load(sm.kv[warp][k % kSlots<FP8>][0], kbase + off, kBlockBytes, bar);
-                bulk_load(sm.kv[warp][k % kSlots<FP8>][1], vbase + off, kBlockBytes, bar);
+                bulk_load(sm.kv[warp][k % kSlotsFor<FP8, GP>][0], kbase + off, kBlockBytes, bar);
+                bulk_load(sm.kv[warp][k % kSlotsFor<FP8, GP>][1], vbase + off, kBlockBytes, bar);
             } else {
                 mbar_arrive(bar);  // nothing to load: complete the phase so the consumer stays in step
             }
         }
     };
-    const int first = nk < kSlots<FP8> ? nk : kSlots<FP8>;
+    const int first = nk < kSlotsFor<FP8, GP> ? nk : kSlotsFor<FP8, GP>;
     for (int k = 0; k < first; ++k) issue(k);
 
     // Queries, pre-scaled into the log2 domain: x = (scale * log2 e) * q.k (times the key scale
@@ -265,8 +267,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     int issued = first;
     bool failed = false;
     for (int k = 0; k < nk; ++k) {
-        const int slot = k % kSlots<FP8>;
-        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSlots<FP8>) & 1), wc, 100 + warp)) {
+        const int slot = k % kSlotsFor<FP8, GP>;
+        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSlotsFor<FP8, GP>) & 1), wc, 100 + warp)) {
             failed = true;
             break;
         }
@@ -315,8 +317,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         // the slot is free again: order this warp's reads before the next bulk write
         fence_proxy_async_smem();
         __syncwarp();
-        if (k + kSlots<FP8> < nk) {
-            issue(k + kSlots<FP8>);
+        if (k + kSlotsFor<FP8, GP> < nk) {
+            issue(k + kSlotsFor<FP8, GP>);
             ++issued;
         }
     }
@@ -324,8 +326,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         // drain this warp's copies still in flight (bounded) before the CTA exits
         WaitCtx drain{nullptr, a.status};
         for (int k = 0; k < issued; ++k) {
-            if (lane == 0 && k + kSlots<FP8> >= issued)  // the last use of each slot
-                (void)mbar_wait(&sm.full[warp][k % kSlots<FP8>], (uint32_t)((k / kSlots<FP8>) & 1), drain, 199);
+            if (lane == 0 && k + kSlotsFor<FP8, GP> >= issued)  // the last use of each slot
+                (void)mbar_wait(&sm.full[warp][k % kSlotsFor<FP8, GP>], (uint32_t)((k / kSlotsFor<FP8, GP>) & 1), drain, 199);
         }
         __syncwarp();
     }
