@@ -248,6 +248,7 @@ int decode_checks(const void *q, const void *k_pages, const void *v_pages, const
     if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
         return ATTN_ERR_INVALID_ARG;
     if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if ((uint64_t)num_pages * (uint64_t)Hkv > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;  // TMA rows
     if (!finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
@@ -320,21 +321,11 @@ ATTN_API int paged_attn_decode_gqa(const void *q, const void *k_pages, const voi
                                    const int32_t *page_table, const int32_t *ctx_lens, int page_size, void *o,
                                    float *lse, int B, int H, int Hkv, int d, int max_pages_per_seq, int num_pages,
                                    float scale, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
-    if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-    if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
-    if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;  // grid y/z limits
-    if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
-    if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
-    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    int st = decode_checks(q, k_pages, v_pages, page_table, ctx_lens, page_size, o, lse, B, H, Hkv, d,
+                           max_pages_per_seq, num_pages, scale, workspace, workspace_bytes);
+    if (st != ATTN_OK) return st;
     int *status = nullptr;
-    int st = device_setup(&status);
+    st = device_setup(&status);
     if (st != ATTN_OK) return st;
     attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, workspace, status, B, H, d, page_size,
                        max_pages_per_seq, num_pages, scale, Hkv};

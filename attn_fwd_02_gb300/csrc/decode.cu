@@ -49,7 +49,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D, int GP, bool FP8>
 struct DecodeSmem {
     // [warp][slot][0 = K, 1 = V][kPS * D] elements (bf16, or e4m3 bytes); 16-byte aligned blocks
-    alignas(128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kPS * D * (FP8 ? 1 : 2)];
+    // (1024-byte alignment for the swizzled TMA boxes of the grouped-query mma kernel)
+    alignas((!FP8 && GP > 1) ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kPS * D * (FP8 ? 1 : 2)];
     uint64_t full[kWarps][kSlotsFor<FP8, GP>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     constexpr int kElem = FP8 ? 1 : 2;
     constexpr uint32_t kRowBytes = D * kElem;
     constexpr uint32_t kBlockBytes = kPS * kRowBytes;
+    static_assert(FP8 || GP == 1, "bf16 grouped-query decode runs in decode_gqa_mma_kernel");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem<D, GP, FP8> &sm = *reinterpret_cast<DecodeSmem<D, GP, FP8> *>(smem_raw);
 
@@ -368,6 +370,286 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     }
 }
 
+// ------------------------------------------------------------------ grouped-query decode on mma
+// With GP query heads per key/value head the scalar kernel spends about 12 warp-instructions per
+// (token, query head) on dot products, shuffles and broadcasts, and becomes compute-bound.  Here
+// each warp runs the two products of a 16-token page on the tensor cores with mma.sync
+// (m16n8k16, bf16 -> fp32): S = Q K^T with the group's query heads as the M rows (padded to 16),
+// and O += P V with P taken straight from the score fragments (the C layout of two n8 tiles is
+// the A layout of one k16 step).  K and V fragments come from the page blocks in shared memory
+// through ldmatrix (transposed for V).  Softmax per row over the quad of lanes that holds it,
+// with the same lazy reference max as the prefill (O and l are rescaled only when a row max
+// grows by more than 2^8).  The page blocks arrive by TMA in 128-byte-swizzled boxes of 16 rows x
+// 64 columns (the 16-byte chunk c of row r sits at chunk c ^ (r & 7)), so the eight rows of every
+// ldmatrix read fall in different banks.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// d (+)= a b: a 16x16 bf16 (row-major fragment), b 16x8 bf16 (column-major fragment), d 16x8 fp32.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of the 16-byte chunk holding column col (a multiple of 8) of row r in a page block
+// stored as 128-byte-swizzled boxes of 16 rows x 64 bf16 columns.
+__device__ __forceinline__ uint32_t swz_off(int r, int col) {
+    return (uint32_t)((col >> 6) * (16 * 128) + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+template <int D, int GP>
+__global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                     const __grid_constant__ CUtensorMap tmV,
+                                                                     const DecodeArgs a, int max_splits, int Hkv,
+                                                                     int gsplit) {
+    static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
+    constexpr int kSl = kSlotsFor<false, GP>;
+    constexpr uint32_t kBlockBytes = kPS * D * 2;
+    constexpr int KS = D / 16;  // k-steps of S = Q K^T
+    constexpr int NT = D / 8;   // n-tiles of O += P V
+    constexpr float kThresh = 8.0f;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // the swizzled boxes need 1024-byte alignment
+    DecodeSmem<D, GP, false> &sm =
+        *reinterpret_cast<DecodeSmem<D, GP, false> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int kvh = (int)blockIdx.y / gsplit;
+    const int qh0 = kvh * (a.H / Hkv) + ((int)blockIdx.y % gsplit) * GP;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cap = a.max_pages * kPS;
+    const int ctx = min(max(a.ctx_lens[b], 0), cap);
+    const int tok0 = split * kDecodeChunkTokens;
+    if (tok0 >= ctx) return;
+    const int tok1 = min(ctx, tok0 + kDecodeChunkTokens);
+    const int page0 = tok0 / kPS;
+    const int npages = (tok1 - tok0 + kPS - 1) / kPS;
+    const int nk = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
+
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < kWarps; ++w)
+            for (int s2 = 0; s2 < kSl; ++s2) mbar_init(&sm.full[w][s2], 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    WaitCtx wc{&sm.abort_flag, a.status};
+
+    int my_pid = -1;
+    if (lane < nk) my_pid = a.page_table[(size_t)b * a.max_pages + page0 + warp + kWarps * lane];
+    const bool my_ok = (my_pid >= 0 && my_pid < a.num_pages);
+    if (lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    auto issue = [&](int k) {
+        const int pid = __shfl_sync(0xffffffffu, my_pid, k);
+        const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
+        if (lane == 0) {
+            uint64_t *bar = &sm.full[warp][k % kSl];
+            if (ok) {
+                const int row = pid * Hkv + kvh;  // page block in the pool viewed as [num_pages * Hkv, 16, D]
+                mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
+#pragma unroll
+                for (int i = 0; i < D / 64; ++i) {
+                    tma_load_3d(sm.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
+                    tma_load_3d(sm.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
+                }
+            } else {
+                mbar_arrive(bar);
+            }
+        }
+    };
+    const int first = nk < kSl ? nk : kSl;
+    for (int k = 0; k < first; ++k) issue(k);
+
+    // Q as A fragments: rows r0 = lane / 4 and r0 + 8 (query heads qh0 + row; zero past GP)
+    const int r0 = lane >> 2, kq = (lane & 3) * 2;
+    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                                                             ((size_t)b * a.H + qh0) * D);
+    uint32_t qa[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int c0 = ks * 16 + kq;
+        qa[ks][0] = r0 < GP ? q32[(r0 * D + c0) / 2] : 0u;
+        qa[ks][1] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0) / 2] : 0u;
+        qa[ks][2] = r0 < GP ? q32[(r0 * D + c0 + 8) / 2] : 0u;
+        qa[ks][3] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0 + 8) / 2] : 0u;
+    }
+    const float c = a.scale * kLog2e;
+
+    float o[NT][4];
+#pragma unroll
+    for (int nd = 0; nd < NT; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float m_ref[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // rows r0, r0 + 8
+
+    // ldmatrix: lane l gives row (l & 7) of 8x8 matrix l >> 3
+    const int mi = lane >> 3, mr = lane & 7;
+    const int k_row = (mi >> 1) * 8 + mr, k_col = (mi & 1) * 8;  // + ks * 16 columns
+    const int v_row = (mi & 1) * 8 + mr, v_col = (mi >> 1) * 8;  // + nd * 8 columns
+
+    int issued = first;
+    bool failed = false;
+    for (int k = 0; k < nk; ++k) {
+        const int slot = k % kSl;
+        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)((k / kSl) & 1), wc, 120 + warp)) {
+            failed = true;
+            break;
+        }
+        const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
+        const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
+        const int ntok = min(kPS, tok1 - page_tok0);
+        if (ok) {
+            const uint32_t Ks = smem_u32(sm.kv[warp][slot][0]);
+            const uint32_t Vs = smem_u32(sm.kv[warp][slot][1]);
+            if (ntok < kPS) {
+                // slots past the context end: zero their V rows (every box) so P = 0 meets finite values
+                const int per_box = (kPS - ntok) * 8;  // 16-byte chunks of the dead rows of one box
+                for (int i = lane; i < per_box * (D / 64); i += 32) {
+                    const int box = i / per_box, j = i % per_box;
+                    *reinterpret_cast<uint4 *>(sm.kv[warp][slot][1] + box * (16 * 128) + ntok * 128 + j * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t bk[4];
+                ldsm_x4(Ks + swz_off(k_row, ks * 16 + k_col), bk);
+                mma_16816(sc[0], qa[ks], bk[0], bk[1]);
+                mma_16816(sc[1], qa[ks], bk[2], bk[3]);
+            }
+            // log2-domain scores; this lane holds tokens nt*8 + (lane&3)*2 + {0,1} of rows r0 / r0+8
+            float x[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = nt * 8 + kq + (i & 1);
+                    x[nt][i] = tok < ntok ? sc[nt][i] * c : -INFINITY;
+                }
+            float mx[2];
+            mx[0] = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+            mx[1] = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            }
+            float al[2] = {1.f, 1.f};
+            bool resc = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (mx[h] > m_ref[h] + kThresh) {
+                    al[h] = ex2_approx(m_ref[h] - mx[h]);
+                    m_ref[h] = mx[h];
+                    l_run[h] *= al[h];
+                    resc = true;
+                }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                for (int nd = 0; nd < NT; ++nd) {
+                    o[nd][0] *= al[0];
+                    o[nd][1] *= al[0];
+                    o[nd][2] *= al[1];
+                    o[nd][3] *= al[1];
+                }
+            }
+            float p[2][4], ps[2] = {0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    p[nt][i] = ex2_approx(x[nt][i] - m_ref[i >> 1]);
+                    ps[i >> 1] += p[nt][i];
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                ps[h] += __shfl_xor_sync(0xffffffffu, ps[h], 1);
+                ps[h] += __shfl_xor_sync(0xffffffffu, ps[h], 2);
+                l_run[h] += ps[h];
+            }
+            const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
+                                    pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+#pragma unroll
+            for (int nd = 0; nd < NT; nd += 2) {
+                uint32_t bv[4];
+                ldsm_x4_trans(Vs + swz_off(v_row, nd * 8 + v_col), bv);
+                mma_16816(o[nd], pa, bv[0], bv[1]);
+                mma_16816(o[nd + 1], pa, bv[2], bv[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + kSl < nk) {
+            issue(k + kSl);
+            ++issued;
+        }
+    }
+    if (failed) {
+        WaitCtx drain{nullptr, a.status};
+        for (int k = 0; k < issued; ++k) {
+            if (lane == 0 && k + kSl >= issued)
+                (void)mbar_wait(&sm.full[warp][k % kSl], (uint32_t)((k / kSl) & 1), drain, 198);
+        }
+        __syncwarp();
+    }
+
+    // this warp's state of each query head -> shared memory, then the merge of the kernel above
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int g = r0 + 8 * h;
+        if (g < GP) {
+            if ((lane & 3) == 0) {
+                sm.red_m[warp][g] = m_ref[h];
+                sm.red_l[warp][g] = l_run[h];
+            }
+#pragma unroll
+            for (int nd = 0; nd < NT; ++nd) {
+                sm.red_o[warp][g][nd * 8 + kq] = o[nd][2 * h];
+                sm.red_o[warp][g][nd * 8 + kq + 1] = o[nd][2 * h + 1];
+            }
+        }
+    }
+    __syncthreads();
+    if (sm.abort_flag) return;
+    for (int e = threadIdx.x; e < GP * D; e += blockDim.x) {
+        const int g = e / D, dd = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w][g]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wgt = ex2_approx(sm.red_m[w][g] - M);
+                L += sm.red_l[w][g] * wgt;
+                O += sm.red_o[w][g][dd] * wgt;
+            }
+        }
+        float *ws = reinterpret_cast<float *>(a.workspace) +
+                    (((size_t)b * a.H + qh0 + g) * max_splits + split) * (size_t)ws_stride<D>();
+        ws[dd] = O;
+        if (dd == 0) {
+            ws[D] = M;
+            ws[D + 1] = L;
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, int max_splits) {
     const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
@@ -407,9 +689,25 @@ cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t st
 }
 
 template <int D, int GP>
+cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
+    CUtensorMap tk, tv;  // page pool [num_pages * Hkv, 16, D], one 16 x 64 box per page block and 64 columns
+    if (!encode_qkv_map(&tk, a.k_pages, a.num_pages * a.Hkv, kPS, D, kPS) ||
+        !encode_qkv_map(&tv, a.v_pages, a.num_pages * a.Hkv, kPS, D, kPS))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(DecodeSmem<D, GP, false>) + 1024;
+    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_gqa_mma_kernel<D, GP>), (int)smem);
+    if (e != cudaSuccess) return e;
+    const int gsplit = (a.H / a.Hkv) / GP;
+    dim3 g1(max_splits, a.Hkv * gsplit, a.B);
+    decode_gqa_mma_kernel<D, GP><<<g1, kWarps * 32, smem, stream>>>(tk, tv, a, max_splits, a.Hkv, gsplit);
+    return cudaGetLastError();
+}
+
+template <int D, int GP>
 cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
-    return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, stream)
-                    : launch_decode_g<D, GP, false>(a, max_splits, stream);
+    if (a.kv_fp8) return launch_decode_g<D, GP, true>(a, max_splits, stream);
+    if constexpr (GP >= 2) return launch_decode_mma<D, GP>(a, max_splits, stream);
+    else return launch_decode_g<D, GP, false>(a, max_splits, stream);
 }
 
 template <int D>

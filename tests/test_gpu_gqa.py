@@ -86,3 +86,37 @@ def test_gqa_decode_vs_oracle(lib, oracle_mod, shape, hkv, ctx):
     o_ref, lse_ref = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
                                                  inp["ctx_lens"], shape.scale)
     check(o, lse, o_ref, lse_ref, shape.name)
+
+
+def test_gqa_decode_full_size_vs_oracle(lib, oracle_mod):
+    # the grouped-query decode workload (B=32, 32 query heads over 8 cache heads, ctx U[512,8192])
+    shape = workloads.PAGED_DECODE_GQA
+    inp = workloads.decode_inputs(shape, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
+    d = {k: v.cuda() for k, v in inp.items()}
+    o, lse = lib.paged_attn_decode_gqa(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"],
+                                       shape.scale)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                                 inp["ctx_lens"], shape.scale)
+    check(o, lse, o_ref, lse_ref, shape.name)
+
+
+@pytest.mark.parametrize("hkv", [8, 2])
+def test_gqa_decode_ignores_nan_past_the_context(lib, oracle_mod, hkv):
+    # cache slots past each sequence's end hold NaN (memory nobody wrote): they must not reach O
+    shape = workloads.DecodeShape("GQA NaN tail", 3, 16, 128, (1, 700), seed=79)
+    ctx = [700, 33, 129]
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=hkv)
+    for b, n in enumerate(ctx):
+        if n % 16:
+            last = int(inp["page_table"][b, n // 16])
+            inp["k_pages"][last, :, n % 16:] = float("nan")
+            inp["v_pages"][last, :, n % 16:] = float("nan")
+    d = {k: v.cuda() for k, v in inp.items()}
+    o, lse = lib.paged_attn_decode_gqa(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"],
+                                       shape.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                                 inp["ctx_lens"], shape.scale)
+    check(o, lse, o_ref, lse_ref, shape.name)
