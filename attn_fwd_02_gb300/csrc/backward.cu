@@ -162,7 +162,7 @@ struct alignas(1024) DkvSmem {
     __nv_bfloat16 v[kT * D];
     __nv_bfloat16 q[kStages][kT * D];     // streamed query tiles
     __nv_bfloat16 dout[kStages][kT * D];  // and their upstream gradients
-    float lse2[kStages][kT];              // log2-domain LSE of each streamed query (0 past Nq)
+    float nlse2[kStages][kT];             // minus the log2-domain LSE of each streamed query (0 past Nq)
     float dterm[kStages][kT];             // row term D of each streamed query (0 past Nq)
     uint64_t kv_full;
     uint64_t u_full[kStages], u_empty[kStages];
@@ -203,6 +203,24 @@ __device__ void dkdv_producer(DkvSmem<D> &sm, const BwdParams &p, const CUtensor
             tma_load_3d(sm.v + i * (kT * 64), tmV, &sm.kv_full, i * 64, k0, bh_kv);
         }
     }
+    // the row statistics of unit u's 128 queries, four per lane (plain loads, zeros past Nq); they
+    // are loaded one unit ahead so their latency hides behind the ring wait
+    auto load_stats = [&](int u, float (&l4)[4], float (&d4)[4]) {
+        const int bh_q = b * p.Hq + hkv * p.group + u / nqt;
+        const int q0 = (qi_start + u % nqt) * kT;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int row = q0 + lane * 4 + t;
+            l4[t] = 0.f;
+            d4[t] = 0.f;
+            if (row < p.Nq) {
+                l4[t] = p.lse[(size_t)bh_q * p.Nq + row];
+                d4[t] = p.dterm[(size_t)bh_q * p.Nq + row];
+            }
+        }
+    };
+    float l4n[4], d4n[4];
+    load_stats(0, l4n, d4n);
     int fills = 0;
     for (int u = 0; u < n; ++u) {
         const int slot = u % kStages, use = u / kStages;
@@ -210,20 +228,10 @@ __device__ void dkdv_producer(DkvSmem<D> &sm, const BwdParams &p, const CUtensor
         const int g = u / nqt, qi = qi_start + u % nqt;
         const int bh_q = b * p.Hq + hkv * p.group + g;
         const int q0 = qi * kT;
-        // the tile's row statistics, four queries per lane (plain loads, before the arrive)
-        float l4[4], d4[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int row = q0 + lane * 4 + t;
-            l4[t] = 0.f;
-            d4[t] = 0.f;
-            if (row < p.Nq) {
-                l4[t] = p.lse[(size_t)bh_q * p.Nq + row] * kLog2e;
-                d4[t] = p.dterm[(size_t)bh_q * p.Nq + row];
-            }
-        }
-        *reinterpret_cast<float4 *>(&sm.lse2[slot][lane * 4]) = make_float4(l4[0], l4[1], l4[2], l4[3]);
-        *reinterpret_cast<float4 *>(&sm.dterm[slot][lane * 4]) = make_float4(d4[0], d4[1], d4[2], d4[3]);
+        *reinterpret_cast<float4 *>(&sm.nlse2[slot][lane * 4]) =
+            make_float4(l4n[0] * -kLog2e, l4n[1] * -kLog2e, l4n[2] * -kLog2e, l4n[3] * -kLog2e);
+        *reinterpret_cast<float4 *>(&sm.dterm[slot][lane * 4]) = make_float4(d4n[0], d4n[1], d4n[2], d4n[3]);
+        if (u + 1 < n) load_stats(u + 1, l4n, d4n);
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.u_full[slot], 2 * kBoxes * kBoxBytes);
 #pragma unroll
@@ -302,6 +310,18 @@ __device__ void dkdv_compute(DkvSmem<D> &sm, const BwdParams &p, uint32_t tmem, 
         if (!key_ok) hi = 0;
         const bool need_mask = lo > 0 || hi < 64;
 
+        // The columns' statistics are read before the score waits so that their latency hides
+        // behind them.  The producer wrote them before arriving on the unit's full barrier; waiting
+        // on that barrier (without arriving) orders these reads after its writes.  The slot cannot
+        // be refilled before this step ends (the refill waits for dK(j), which needs this step's dS).
+        if (!__all_sync(kFull, mbar_wait(&sm.u_full[slot], (uint32_t)((j / kStages) & 1), wc, 73))) {
+            ok = false;
+            break;
+        }
+        float4 L4[16];
+        const float4 *l2 = reinterpret_cast<const float4 *>(sm.nlse2[slot] + w * 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) L4[i] = l2[i];
         if (!__all_sync(kFull, mbar_wait(&sm.s_full, (uint32_t)(j & 1), wc, 70))) {
             ok = false;
             break;
@@ -310,17 +330,16 @@ __device__ void dkdv_compute(DkvSmem<D> &sm, const BwdParams &p, uint32_t tmem, 
         uint32_t x[2][32];
         load64(tS, x);
         // P^T = 2^(s * scale * log2e - lse2): bf16 pairs over the scores, fp32 kept in x
-        const float *l2 = sm.lse2[slot] + w * 64;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                const float4 L = *reinterpret_cast<const float4 *>(l2 + h * 32 + i);
+                const float4 L = L4[(h * 32 + i) / 4];
                 const uint64_t e01 = f32x2_fma(f32x2_pack(__uint_as_float(x[h][i]), __uint_as_float(x[h][i + 1])), c2,
-                                               f32x2_pack(-L.x, -L.y));
+                                               f32x2_pack(L.x, L.y));
                 const uint64_t e23 = f32x2_fma(f32x2_pack(__uint_as_float(x[h][i + 2]), __uint_as_float(x[h][i + 3])),
-                                               c2, f32x2_pack(-L.z, -L.w));
+                                               c2, f32x2_pack(L.z, L.w));
                 float e[4];
                 f32x2_unpack(e01, e[0], e[1]);
                 f32x2_unpack(e23, e[2], e[3]);
@@ -342,6 +361,10 @@ __device__ void dkdv_compute(DkvSmem<D> &sm, const BwdParams &p, uint32_t tmem, 
         tc_fence_before_sync();
         mbar_arrive(&sm.p_full);
 
+        float4 D4[16];
+        const float4 *dd = reinterpret_cast<const float4 *>(sm.dterm[slot] + w * 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) D4[i] = dd[i];
         if (!__all_sync(kFull, mbar_wait(&sm.dp_full, (uint32_t)(j & 1), wc, 71))) {
             ok = false;
             break;
@@ -350,13 +373,12 @@ __device__ void dkdv_compute(DkvSmem<D> &sm, const BwdParams &p, uint32_t tmem, 
         uint32_t y[2][32];
         load64(tdP, y);
         // dS^T = P^T * (dP^T - D): bf16 pairs over dP^T
-        const float *dd = sm.dterm[slot] + w * 64;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                const float4 Dv = *reinterpret_cast<const float4 *>(dd + h * 32 + i);
+                const float4 Dv = D4[(h * 32 + i) / 4];
                 const float s0 = __uint_as_float(x[h][i]) * (__uint_as_float(y[h][i]) - Dv.x);
                 const float s1 = __uint_as_float(x[h][i + 1]) * (__uint_as_float(y[h][i + 1]) - Dv.y);
                 const float s2 = __uint_as_float(x[h][i + 2]) * (__uint_as_float(y[h][i + 2]) - Dv.z);
