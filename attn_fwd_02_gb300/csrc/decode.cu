@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     constexpr int kElem = FP8 ? 1 : 2;
     constexpr uint32_t kRowBytes = D * kElem;
     constexpr uint32_t kBlockBytes = kPS * kRowBytes;
-    static_assert(FP8 || GP == 1, "bf16 grouped-query decode runs in decode_gqa_mma_kernel");
+    static_assert(GP == 1, "grouped-query decode runs in decode_gqa_mma_kernel");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem<D, GP, FP8> &sm = *reinterpret_cast<DecodeSmem<D, GP, FP8> *>(smem_raw);
 
@@ -409,21 +409,45 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
     return (uint32_t)((col >> 6) * (16 * 128) + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-template <int D, int GP>
+// An e4m3 cache takes the same path: each warp widens its fp8 page block into a bf16 staging tile
+// in the same swizzled layout (exact: every e4m3 value is a bf16 value), the key scale folds into
+// the score scale and the value scale into the partial O.
+template <int D, int GP, bool FP8>
+struct GqaMmaSmem {
+    DecodeSmem<D, GP, FP8> s;
+    alignas(128) __nv_bfloat16 stage[FP8 ? kWarps : 1][2][FP8 ? kPS * D : 8];  // bf16 K, V of one page
+};
+
+// 16 e4m3 codes (one 16-byte chunk of a page row) -> 16 bf16 values, two 16-byte chunks.
+__device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 &lo, uint4 &hi) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = e4m3x2_to_float2(w[i]), b = e4m3x2_to_float2(w[i] >> 16);
+        o[2 * i] = pack_bf16x2(a.x, a.y);
+        o[2 * i + 1] = pack_bf16x2(b.x, b.y);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <int D, int GP, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                      const __grid_constant__ CUtensorMap tmV,
                                                                      const DecodeArgs a, int max_splits, int Hkv,
                                                                      int gsplit) {
     static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
-    constexpr int kSl = kSlotsFor<false, GP>;
-    constexpr uint32_t kBlockBytes = kPS * D * 2;
+    constexpr int kSl = kSlotsFor<FP8, GP>;
+    constexpr uint32_t kBlockBytes = kPS * D * (FP8 ? 1 : 2);
     constexpr int KS = D / 16;  // k-steps of S = Q K^T
     constexpr int NT = D / 8;   // n-tiles of O += P V
     constexpr float kThresh = 8.0f;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // the swizzled boxes need 1024-byte alignment
-    DecodeSmem<D, GP, false> &sm =
-        *reinterpret_cast<DecodeSmem<D, GP, false> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    GqaMmaSmem<D, GP, FP8> &smx =
+        *reinterpret_cast<GqaMmaSmem<D, GP, FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    DecodeSmem<D, GP, FP8> &sm = smx.s;
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int kvh = (int)blockIdx.y / gsplit;
@@ -450,10 +474,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     int my_pid = -1;
     if (lane < nk) my_pid = a.page_table[(size_t)b * a.max_pages + page0 + warp + kWarps * lane];
     const bool my_ok = (my_pid >= 0 && my_pid < a.num_pages);
-    if (lane == 0) {
+    if (!FP8 && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(a.k_pages);
+    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(a.v_pages);
     auto issue = [&](int k) {
         const int pid = __shfl_sync(0xffffffffu, my_pid, k);
         const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
@@ -462,10 +488,15 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             if (ok) {
                 const int row = pid * Hkv + kvh;  // page block in the pool viewed as [num_pages * Hkv, 16, D]
                 mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
+                if constexpr (FP8) {
+                    bulk_load(sm.kv[warp][k % kSl][0], kbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
+                    bulk_load(sm.kv[warp][k % kSl][1], vbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
+                } else {
 #pragma unroll
-                for (int i = 0; i < D / 64; ++i) {
-                    tma_load_3d(sm.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
-                    tma_load_3d(sm.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
+                    for (int i = 0; i < D / 64; ++i) {
+                        tma_load_3d(sm.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
+                        tma_load_3d(sm.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
+                    }
                 }
             } else {
                 mbar_arrive(bar);
@@ -488,7 +519,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         qa[ks][2] = r0 < GP ? q32[(r0 * D + c0 + 8) / 2] : 0u;
         qa[ks][3] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0 + 8) / 2] : 0u;
     }
-    const float c = a.scale * kLog2e;
+    const float c = a.scale * kLog2e * (FP8 ? a.k_scale : 1.f);
 
     float o[NT][4];
 #pragma unroll
@@ -512,9 +543,33 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
         const int ntok = min(kPS, tok1 - page_tok0);
         if (ok) {
-            const uint32_t Ks = smem_u32(sm.kv[warp][slot][0]);
-            const uint32_t Vs = smem_u32(sm.kv[warp][slot][1]);
-            if (ntok < kPS) {
+            uint32_t Ks = smem_u32(sm.kv[warp][slot][0]);
+            uint32_t Vs = smem_u32(sm.kv[warp][slot][1]);
+            if constexpr (FP8) {
+                // widen the e4m3 block into this warp's bf16 staging tiles (swizzled as the TMA boxes);
+                // V rows past the context end are written as zeros
+                uint8_t *stK = reinterpret_cast<uint8_t *>(smx.stage[warp][0]);
+                uint8_t *stV = reinterpret_cast<uint8_t *>(smx.stage[warp][1]);
+                constexpr int kChunks = kPS * D / 16;  // 16-byte chunks of fp8 per block
+#pragma unroll
+                for (int i = lane; i < kChunks; i += 32) {
+                    const int r = i / (D / 16), c0 = (i % (D / 16)) * 16;
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.kv[warp][slot][0])[i], lo, hi);
+                    *reinterpret_cast<uint4 *>(stK + swz_off(r, c0)) = lo;
+                    *reinterpret_cast<uint4 *>(stK + swz_off(r, c0 + 8)) = hi;
+                    if (r < ntok) {
+                        e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.kv[warp][slot][1])[i], lo, hi);
+                    } else {
+                        lo = hi = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    *reinterpret_cast<uint4 *>(stV + swz_off(r, c0)) = lo;
+                    *reinterpret_cast<uint4 *>(stV + swz_off(r, c0 + 8)) = hi;
+                }
+                __syncwarp();
+                Ks = smem_u32(stK);
+                Vs = smem_u32(stV);
+            } else if (ntok < kPS) {
                 // slots past the context end: zero their V rows (every box) so P = 0 meets finite values
                 const int per_box = (kPS - ntok) * 8;  // 16-byte chunks of the dead rows of one box
                 for (int i = lane; i < per_box * (D / 64); i += 32) {
@@ -642,7 +697,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         }
         float *ws = reinterpret_cast<float *>(a.workspace) +
                     (((size_t)b * a.H + qh0 + g) * max_splits + split) * (size_t)ws_stride<D>();
-        ws[dd] = O;
+        ws[dd] = FP8 ? O * a.v_scale : O;
         if (dd == 0) {
             ws[D] = M;
             ws[D + 1] = L;
@@ -688,26 +743,33 @@ cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t st
     return cudaGetLastError();
 }
 
-template <int D, int GP>
+template <int D, int GP, bool FP8>
 cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
-    CUtensorMap tk, tv;  // page pool [num_pages * Hkv, 16, D], one 16 x 64 box per page block and 64 columns
-    if (!encode_qkv_map(&tk, a.k_pages, a.num_pages * a.Hkv, kPS, D, kPS) ||
-        !encode_qkv_map(&tv, a.v_pages, a.num_pages * a.Hkv, kPS, D, kPS))
+    // bf16 pages: page pool [num_pages * Hkv, 16, D], one 16 x 64 box per page block and 64 columns.
+    // e4m3 pages are fetched as plain bulk copies and the maps are not used.
+    CUtensorMap tk{}, tv{};
+    if (!FP8 && (!encode_qkv_map(&tk, a.k_pages, a.num_pages * a.Hkv, kPS, D, kPS) ||
+                 !encode_qkv_map(&tv, a.v_pages, a.num_pages * a.Hkv, kPS, D, kPS)))
         return cudaErrorInvalidValue;
-    const size_t smem = sizeof(DecodeSmem<D, GP, false>) + 1024;
-    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_gqa_mma_kernel<D, GP>), (int)smem);
+    const size_t smem = sizeof(GqaMmaSmem<D, GP, FP8>) + 1024;
+    cudaError_t e =
+        ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_gqa_mma_kernel<D, GP, FP8>), (int)smem);
     if (e != cudaSuccess) return e;
     const int gsplit = (a.H / a.Hkv) / GP;
     dim3 g1(max_splits, a.Hkv * gsplit, a.B);
-    decode_gqa_mma_kernel<D, GP><<<g1, kWarps * 32, smem, stream>>>(tk, tv, a, max_splits, a.Hkv, gsplit);
+    decode_gqa_mma_kernel<D, GP, FP8><<<g1, kWarps * 32, smem, stream>>>(tk, tv, a, max_splits, a.Hkv, gsplit);
     return cudaGetLastError();
 }
 
 template <int D, int GP>
 cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
-    if (a.kv_fp8) return launch_decode_g<D, GP, true>(a, max_splits, stream);
-    if constexpr (GP >= 2) return launch_decode_mma<D, GP>(a, max_splits, stream);
-    else return launch_decode_g<D, GP, false>(a, max_splits, stream);
+    if constexpr (GP >= 2) {
+        return a.kv_fp8 ? launch_decode_mma<D, GP, true>(a, max_splits, stream)
+                        : launch_decode_mma<D, GP, false>(a, max_splits, stream);
+    } else {
+        return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, stream)
+                        : launch_decode_g<D, GP, false>(a, max_splits, stream);
+    }
 }
 
 template <int D>

@@ -500,11 +500,13 @@ def gpu_arm(args):
         pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
         dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
         parts = [pre, dec]
-    elif args.workload in ("decode", "decode_small", "decode_gqa", "decode_fp8"):
+    elif args.workload in ("decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8"):
         if args.workload == "decode_gqa":
             dec = DecodeCase(workloads.PAGED_DECODE_GQA, torch, A, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
         elif args.workload == "decode_fp8":
             dec = DecodeFp8Case(workloads.PAGED_DECODE, torch, A)
+        elif args.workload == "decode_gqa_fp8":
+            dec = DecodeFp8Case(workloads.PAGED_DECODE_GQA, torch, A, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
         else:
             shape = workloads.PAGED_DECODE if args.workload == "decode" else workloads.PAGED_DECODE_SMALL
             dec = DecodeCase(shape, torch, A)
@@ -740,7 +742,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8",
+    ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8",
                                            "prefill_paged", "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")

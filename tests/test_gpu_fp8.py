@@ -112,3 +112,32 @@ def test_fp8_decode_unequal_scales(lib, oracle_mod):
 def test_fp8_decode_full_size(lib, oracle_mod):
     # the paged-decode workload (B=32, H=32, d=128, ctx U[512,8192]) with its cache in e4m3
     run_fp8_decode(lib, oracle_mod, workloads.PAGED_DECODE)
+
+
+def test_fp8_gqa_decode_full_size(lib, oracle_mod):
+    # the grouped-query decode workload (32 query heads over 8 cache heads) with its cache in e4m3
+    run_fp8_decode(lib, oracle_mod, workloads.PAGED_DECODE_GQA, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
+
+
+def test_fp8_gqa_decode_ignores_nan_codes_past_the_context(lib, oracle_mod):
+    # e4m3 NaN codes (0x7F) in cache slots past each sequence's end must not reach O
+    shape = workloads.DecodeShape("fp8 NaN tail", 3, 16, 128, (1, 700), seed=730)
+    ctx = [700, 33, 129]
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=4)
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], KV_SCALE)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], KV_SCALE)
+    for b, n in enumerate(ctx):
+        if n % 16:
+            last = int(inp["page_table"][b, n // 16])
+            kc[last, :, n % 16:] = 0x7F
+            vc[last, :, n % 16:] = 0x7F
+    o, lse = lib.paged_attn_decode_fp8(inp["q"].cuda(), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                                       KV_SCALE, KV_SCALE, inp["page_table"].cuda(), inp["ctx_lens"].cuda(),
+                                       shape.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle_mod.paged_decode_fp8_gqa(inp["q"], kc, vc, KV_SCALE, KV_SCALE, inp["page_table"],
+                                                     inp["ctx_lens"], shape.scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(og).all()
+    assert np.abs(og - o_ref).max() <= O_MAX
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
