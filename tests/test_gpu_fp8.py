@@ -141,3 +141,24 @@ def test_fp8_gqa_decode_ignores_nan_codes_past_the_context(lib, oracle_mod):
     assert np.isfinite(og).all()
     assert np.abs(og - o_ref).max() <= O_MAX
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
+
+
+def test_fp8_gqa_decode_query_beyond_fp16_range(lib, oracle_mod):
+    # the grouped-query e4m3 path multiplies q in fp16; a query of magnitude ~1e5 (past fp16's
+    # 65504) with a correspondingly smaller softmax scale must give the same attention
+    shape = workloads.DecodeShape("fp8 big q", 2, 8, 128, (1, 800), seed=740)
+    inp = workloads.decode_inputs(shape, ctx_lens=[800, 77], kv_heads=2)
+    big = 3.0e4
+    q = (inp["q"].float() * big).to(torch.bfloat16)
+    scale = shape.scale / big
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], KV_SCALE)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], KV_SCALE)
+    o, lse = lib.paged_attn_decode_fp8(q.cuda(), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(), KV_SCALE,
+                                       KV_SCALE, inp["page_table"].cuda(), inp["ctx_lens"].cuda(), scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle_mod.paged_decode_fp8_gqa(q, kc, vc, KV_SCALE, KV_SCALE, inp["page_table"],
+                                                     inp["ctx_lens"], scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(og).all()
+    assert np.abs(og - o_ref).max() <= O_MAX and np.abs(og - o_ref).mean() <= O_MEAN
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
