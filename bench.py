@@ -206,11 +206,9 @@ class PrefillCase:
         self.flops_nominal = metrics.prefill_flops(s.B, s.H, s.Nq, s.Nkv, s.d, s.causal)
         self.bytes = metrics.prefill_bytes(s.B, s.H, s.Nq, s.Nkv, s.d, kv_lens=self.kv_lens)
         self.launches = 1
-        # e2e buffers
-        self.o_host = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
-        self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values() if v is not None)
         self.d2h_bytes = self.o.numel() * 2 + self.lse.numel() * 4
+        self.out_names = ("o", "lse")
 
     def run(self):
         s, d = self.shape, self.dev
@@ -219,14 +217,6 @@ class PrefillCase:
         else:
             self.A.attn_fwd_kvlen(d["q"], d["k"], d["v"], s.causal, s.scale, kv_lens=d["kv_lens"], out=self.o,
                                   lse=self.lse)
-
-    def run_e2e(self):
-        for k, v in self.host.items():
-            if v is not None:
-                self.dev[k].copy_(v, non_blocking=True)
-        self.run()
-        self.o_host.copy_(self.o, non_blocking=True)
-        self.lse_host.copy_(self.lse, non_blocking=True)
 
 
 class DecodeCase:
@@ -245,23 +235,15 @@ class DecodeCase:
         self.ctx = [int(x) for x in inp["ctx_lens"]]
         self.bytes = metrics.decode_bytes(shape.H, shape.d, self.ctx, shape.page_size, kv_heads=kv_heads)
         self.launches = 2
-        self.o_host = torch.empty(self.o.shape, dtype=self.o.dtype, pin_memory=True)
-        self.lse_host = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.host.values())
         self.d2h_bytes = self.o.numel() * 2 + self.lse.numel() * 4
+        self.out_names = ("o", "lse")
 
     def run(self):
         d = self.dev
         fn = self.A.paged_attn_decode if self.kv_heads is None else self.A.paged_attn_decode_gqa
         fn(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["ctx_lens"], self.shape.scale, out=self.o,
            lse=self.lse, workspace=self.ws)
-
-    def run_e2e(self):
-        for k, v in self.host.items():
-            self.dev[k].copy_(v, non_blocking=True)
-        self.run()
-        self.o_host.copy_(self.o, non_blocking=True)
-        self.lse_host.copy_(self.lse, non_blocking=True)
 
 
 class DecodeFp8Case(DecodeCase):
@@ -340,23 +322,14 @@ class BackwardCase:
         qkv = 2.0 * s.B * s.H * s.Nq * s.d
         self.bytes = 8 * qkv + 8.0 * s.B * s.H * s.Nq
         self.launches = 3
-        self.dq_host, self.dk_host, self.dv_host = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                                                    for t in (self.dq, self.dk, self.dv))
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.dq, self.dk, self.dv))
+        self.out_names = ("dq", "dk", "dv")
 
     def run(self):
         d, s = self.dev, self.shape
         self.A.attn_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], s.causal, s.scale, dq=self.dq,
                         dk=self.dk, dv=self.dv, workspace=self.ws)
-
-    def run_e2e(self):
-        for n, t in self.host.items():
-            self.dev[n].copy_(t, non_blocking=True)
-        self.run()
-        self.dq_host.copy_(self.dq, non_blocking=True)
-        self.dk_host.copy_(self.dk, non_blocking=True)
-        self.dv_host.copy_(self.dv, non_blocking=True)
 
 
 def backward_arm(args, torch, A, rank, world, peaks, peak_kind):
@@ -385,7 +358,7 @@ def backward_arm(args, torch, A, rank, world, peaks, peak_kind):
                         "executed_tflops": round(case.flops_executed / (ms * 1e-3) / 1e12, 2),
                         "peak_source": f"{peak_kind} bf16_tflops"},
            "e2e": {"value": round(job_rate(case.flops, world, e2e_ms, 1e12), 2), "unit": "TFLOP/s",
-                   "h2d_bytes_per_step": int(case.h2d_bytes), "d2h_bytes_per_step": int(case.d2h_bytes),
+                   "schedule": E2E_SCHEDULE, "h2d_bytes_per_step": int(case.h2d_bytes), "d2h_bytes_per_step": int(case.d2h_bytes),
                    "ms_per_step": round(e2e_ms, 3)},
            "config": {"workload": "backward of " + s.name, "B": s.B, "H": s.H, "Nq": s.Nq, "Nkv": s.Nkv, "d": s.d,
                       "causal": s.causal, "flops_per_call": case.flops, "flops_executed_per_call": case.flops_executed,
@@ -456,17 +429,68 @@ def time_parts(torch, parts, steps, warmup, world, sampler=None, graphs=False):
     return region_ms, part_ms
 
 
+E2E_SCHEDULE = ("every step copies its inputs from pinned host memory and its outputs back; steps pipelined "
+                "(double-buffered device inputs/outputs, copies on two streams overlapping neighbouring steps)")
+
+
 def time_e2e(torch, part, steps, warmup, world):
-    stream = torch.cuda.current_stream()
-    for _ in range(max(1, warmup)):
-        part.run_e2e()
-    barrier_sync(world)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        part.run_e2e()
-    t1.record(stream)
-    barrier_sync(world)
+    """End to end through the public API with host buffers: every step copies its inputs from
+    pinned host memory to the device, runs the call, and copies its outputs back to pinned host
+    memory; all of it inside the timed region.  Steps are pipelined the way a serving loop runs
+    them: step s+1's inputs travel on a copy stream into a second set of device buffers while
+    step s computes, and step s's outputs travel back on a third stream from a second set of
+    output buffers, so copies in both directions overlap the compute of neighbouring steps."""
+    cmp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    names = [n for n, t in part.host.items() if t is not None]
+    ins = [dict(part.dev), {n: (torch.empty_like(t) if t is not None else None) for n, t in part.dev.items()}]
+    outs = [{n: getattr(part, n) for n in part.out_names}, {n: torch.empty_like(getattr(part, n)) for n in part.out_names}]
+    host_out = {n: torch.empty(getattr(part, n).shape, dtype=getattr(part, n).dtype, pin_memory=True)
+                for n in part.out_names}
+    ev = lambda: torch.cuda.Event()
+    in_ready, cmp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    saved_dev, saved_out = part.dev, {n: getattr(part, n) for n in part.out_names}
+
+    def step(s):
+        i = s % 2
+        with torch.cuda.stream(h2d):
+            if s >= 2:
+                h2d.wait_event(cmp_done[i])  # step s-2 has finished reading this input set
+            for n in names:
+                ins[i][n].copy_(part.host[n], non_blocking=True)
+            in_ready[i].record(h2d)
+        cmp.wait_event(in_ready[i])
+        if s >= 2:
+            cmp.wait_event(out_done[i])  # step s-2's outputs have left this output set
+        part.dev = ins[i]
+        for n in part.out_names:
+            setattr(part, n, outs[i][n])
+        part.run()
+        cmp_done[i].record(cmp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(cmp_done[i])
+            for n in part.out_names:
+                host_out[n].copy_(outs[i][n], non_blocking=True)
+            out_done[i].record(d2h)
+
+    try:
+        for s in range(max(2, warmup)):
+            step(s)
+        torch.cuda.synchronize()
+        barrier_sync(world)
+        t0, t1, start = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), ev()
+        t0.record(cmp)
+        start.record(cmp)
+        h2d.wait_event(start)
+        for s in range(steps):
+            step(s)
+        cmp.wait_event(out_done[(steps - 1) % 2])
+        t1.record(cmp)
+        barrier_sync(world)
+    finally:
+        part.dev = saved_dev
+        for n, t in saved_out.items():
+            setattr(part, n, t)
     return max_over_ranks(t0.elapsed_time(t1), world) / steps
 
 
@@ -548,7 +572,7 @@ def gpu_arm(args):
         out["roofline"] = roofline_prefill(pre, ms, peaks, peak_kind)
         e2e_ms = time_e2e(torch, pre, e2e_steps, 1, world)
         out["e2e"] = {"value": round(job_rate(pre.flops, world, e2e_ms, 1e12), 2), "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": int(pre.h2d_bytes), "d2h_bytes_per_step": int(pre.d2h_bytes),
+                      "schedule": E2E_SCHEDULE, "h2d_bytes_per_step": int(pre.h2d_bytes), "d2h_bytes_per_step": int(pre.d2h_bytes),
                       "ms_per_step": round(e2e_ms, 3), "part": "prefill"}
         cfg["workload"] = pre.shape.name
         s = pre.shape
@@ -566,7 +590,7 @@ def gpu_arm(args):
                    "bytes_per_call": dec.bytes,
                    "roofline": roofline_decode(dec, ms, ms, peaks, peak_kind),
                    "e2e": {"value": round(job_rate(dec.bytes, world, e2e_ms, 1e9), 1), "unit": "GB/s",
-                           "h2d_bytes_per_step": int(dec.h2d_bytes), "d2h_bytes_per_step": int(dec.d2h_bytes),
+                           "schedule": E2E_SCHEDULE, "h2d_bytes_per_step": int(dec.h2d_bytes), "d2h_bytes_per_step": int(dec.d2h_bytes),
                            "ms_per_step": round(e2e_ms, 3)}}
         s = dec.shape
         cfg["decode"] = {"workload": s.name, "B": s.B, "H": s.H, "d": s.d, "page_size": s.page_size,
