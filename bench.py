@@ -36,9 +36,13 @@ from attn_fwd_02_gb300 import metrics, workloads  # noqa: E402
 METRIC = "attention TFLOP/s (prefill) and HBM GB/s (paged decode), % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+# Traffic entries of profiles/ncu_traffic.txt: key -> source files whose hash the entry was taken on.
+# Each key stands for one kernel on the workload its bench line times.
 KERNEL_SOURCES = {
     "prefill_kernel": ["attn_fwd_02_gb300/csrc/prefill.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
     "decode_split_kernel": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
+    "decode_split_kernel_e4m3": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
+    "decode_gqa_mma_kernel": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
 }
 
 PREFILL_BY_NAME = {
@@ -497,19 +501,33 @@ def time_e2e(torch, part, steps, warmup, world):
 def roofline_prefill(case, ms, peaks, peak_kind):
     achieved = case.flops / (ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     traffic = ncu_traffic("prefill_kernel") if case.shape is workloads.LONG_CAUSAL else None
+    # attainable = min(peak, arithmetic intensity x HBM bandwidth) over the algorithmic bytes
+    ai = case.flops / case.bytes
+    attainable = min(peak, ai * hbm / 1e3)
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "prefill_kernel",
+            "arithmetic_intensity": round(ai, 1), "attainable": round(attainable, 1),
+            "frac_attainable": round(achieved / attainable, 4),
             "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed in sub-second steps)"}
 
 
 def roofline_decode(case, ms_split, ms_total, peaks, peak_kind):
     achieved = case.bytes / (ms_split * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    traffic = ncu_traffic("decode_split_kernel")
+    fp8 = isinstance(case, DecodeFp8Case)
+    if case.kv_heads is not None and case.kv_heads < case.shape.H:
+        kernel = "decode_gqa_mma_kernel"
+        key = kernel if (not fp8 and case.shape is workloads.PAGED_DECODE_GQA) else None
+    else:
+        kernel = "decode_split_kernel"
+        key = ("decode_split_kernel_e4m3" if fp8 else "decode_split_kernel") \
+            if case.shape is workloads.PAGED_DECODE else None
+    traffic = ncu_traffic(key) if key else None
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "decode_split_kernel",
-            "peak_source": f"{peak_kind} hbm_gbs"}
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": kernel + (" (e4m3 cache)" if fp8 else ""), "peak_source": f"{peak_kind} hbm_gbs"}
 
 
 def gpu_arm(args):
