@@ -77,11 +77,8 @@ template <int D>
 __device__ __forceinline__ void mma_scores(uint32_t d_tmem, const __nv_bfloat16 *a, const __nv_bfloat16 *b) {
     constexpr uint32_t id = idesc_bf16_f32(kT, kT, false, false);
     const uint64_t da = sdesc_sw128(smem_u32(a), 16, 1024), db = sdesc_sw128(smem_u32(b), 16, 1024);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
-        tc_mma_ss(d_tmem, sdesc_advance(da, off), sdesc_advance(db, off), id, kk > 0 ? 1u : 0u);
-    }
+    static_assert(kBoxBytes == 16384, "k-step layout of the grouped issue");
+    tc_mma_ss_ksteps<D / 16>(d_tmem, da, db, id, 0u);
 }
 
 // 128 x d accumulation: D[tmem] (+)= A[tmem] B, A = 128 x 128 bf16 written by the two warpgroups
@@ -91,10 +88,8 @@ template <int D>
 __device__ __forceinline__ void mma_accum(uint32_t d_tmem, uint32_t a_tmem, const __nv_bfloat16 *b, bool first) {
     constexpr uint32_t id = idesc_bf16_f32(kT, D, false, true);
     const uint64_t db = sdesc_sw128(smem_u32(b), kBoxBytes, 1024);
-#pragma unroll
-    for (int kk = 0; kk < kT / 16; ++kk)
-        tc_mma_ts(d_tmem, a_tmem + (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8),
-                  sdesc_advance(db, (uint32_t)(kk * 16 * 128)), id, (!first || kk > 0) ? 1u : 0u);
+    static_assert(kT / 16 == 8, "one group of eight k-steps");
+    tc_mma_ts_k8_halves(d_tmem, a_tmem, db, id, first ? 0u : 1u);
 }
 
 // 64 TMEM columns of this thread's lane -> registers.

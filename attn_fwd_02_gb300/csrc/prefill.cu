@@ -107,6 +107,8 @@ constexpr int kStages = 2;
 
 template <int D>
 struct alignas(1024) PrefillSmem {
+    // q, k, v: tiles of kBM x kPad elements back to back (the MMA issuer steps between them by
+    // a constant)
     __nv_bfloat16 q[Cfg<D>::QT][kBM * kPad<D>];  // kPad/64 boxes each
     __nv_bfloat16 k[kStages][kBN * kPad<D>];     // kPad/64 boxes each
     __nv_bfloat16 v[kStages][kBN * kPad<D>];     // kPad/64 boxes each
@@ -242,36 +244,31 @@ template <int D>
 __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-    static_assert(kStages == 2 && kQTilesMax == 2, "descriptor selects below");
-    // Descriptors of the operand buffers, built once; each MMA advances one by a constant.
-    const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-    const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[Cfg<D>::QT - 1]), 16, 1024);
-    const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024), dk1 = sdesc_sw128(smem_u32(sm.k[1]), 16, 1024);
-    const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
-    const uint64_t dv1 = sdesc_sw128(smem_u32(sm.v[1]), kBoxBytes, 1024);
+    static_assert(kStages == 2, "slot selects below");
+    // Descriptors of the operand buffers, built once (the tiles of Q, of K and of V are equally
+    // spaced, one tile = kTile descriptor units); each MMA advances one by a constant.
+    constexpr uint64_t kTile = (uint64_t)(kBM * kPad<D> * 2) >> 4;
+    const uint64_t dq = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
 
-    // S_t(j) = Q_t K_j^T  (A = Q_t, B = K_j: both K-major, 128-byte swizzle)
+    // S_t(j) = Q_t K_j^T  (A = Q_t, B = K_j: both K-major, 128-byte swizzle), d/16 k-steps
+    // issued in groups from single asm statements
     auto issue_S = [&](int t, int j) {
-        const uint64_t a = t ? dq1 : dq0;
-        const uint64_t b = (j & 1) ? dk1 : dk0;  // K(j) sits in slot j % 2
+        const uint64_t a = dq + (t ? kTile : 0);
+        const uint64_t b = dk + ((j & 1) ? kTile : 0);  // K(j) sits in slot j % 2
         const uint32_t tS = tmem + (uint32_t)(t * kBN);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * kBoxBytes + (kk & 3) * 32);
-            tc_mma_ss(tS, sdesc_advance(a, off), sdesc_advance(b, off), idS, kk > 0 ? 1u : 0u);
-        }
+        static_assert(kBoxBytes == 16384, "k-step layout of the grouped issue");
+        tc_mma_ss_ksteps<D / 16>(tS, a, b, idS, 0u);
         tc_commit(&sm.s_full[t]);
     };
     // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
+    static_assert(kBN / 16 == 8, "PV is one group of eight k-steps");
     auto issue_PV = [&](int t, int j) {
-        const uint64_t b = (j & 1) ? dv0 : dv1;  // V(j) sits in slot (j + 1) % 2
+        const uint64_t b = dv + ((j & 1) ? 0 : kTile);  // V(j) sits in slot (j + 1) % 2
         const uint32_t tP = tmem + p_col<D>(t);
         const uint32_t tO = tmem + o_col<D>(t);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-            tc_mma_ts(tO, tP + (uint32_t)(kk * 8), sdesc_advance(b, (uint32_t)(kk * 16 * 128)), idPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        tc_mma_ts_k8(tO, tP, b, idPV, j > 0 ? 1u : 0u);
     };
 
     // The data waits below (Q, ring units) need no tcgen05 fence: TMA writes and the MMA's

@@ -214,6 +214,100 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// Products issued in groups from one asm statement.  A thread that issues its MMAs one asm
+// statement at a time, with each operand buffer chosen at run time (a ring slot), keeps the
+// tensor core at about 107 cycles per 128x128x16 product; a group in one statement issues at
+// the full rate (64 cycles).  The operand descriptors advance by constants inside the
+// statement (two temporaries), which keeps the issuing thread's registers few.  In every
+// group the first product accumulates into D only if acc != 0, the others always.
+//
+// K-major operands with a 128-byte swizzle stored as 64-column boxes of box16 x 16 bytes:
+// k-steps 0-3 lie 32 bytes apart in the first box, 4-7 likewise in the second.
+#define ATTN_SS_STEP(ao, bo)                         \
+    "add.s64 ra, %1, " #ao ";\n\t"                   \
+    "add.s64 rb, %2, " #bo ";\n\t"                   \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, q;\n\t"
+__device__ __forceinline__ void tc_mma_ss_k4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 ra, rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        ATTN_SS_STEP(2, 2) ATTN_SS_STEP(4, 4) ATTN_SS_STEP(6, 6) "}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ss_k2(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 ra, rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        ATTN_SS_STEP(2, 2) "}" ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Eight k-steps over two 16 KB boxes (k-steps 4-7 start 16384 bytes = 1024 descriptor units on).
+__device__ __forceinline__ void tc_mma_ss_k8_box16k(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                    uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 ra, rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        ATTN_SS_STEP(2, 2) ATTN_SS_STEP(4, 4) ATTN_SS_STEP(6, 6)
+        ATTN_SS_STEP(1024, 1024) ATTN_SS_STEP(1026, 1026) ATTN_SS_STEP(1028, 1028) ATTN_SS_STEP(1030, 1030) "}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+#undef ATTN_SS_STEP
+// K = d/16 k-steps of a product over K-major 128-byte-swizzled tiles held as 64-column boxes
+// of 16 KB (128 rows): groups of four per box, then the remainder.
+template <int K>
+__device__ __forceinline__ void tc_mma_ss_ksteps(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc) {
+    static_assert(K >= 1 && K <= 8, "k-steps of a 128-column tile");
+    if constexpr (K == 8) {
+        tc_mma_ss_k8_box16k(d_tmem, a, b, idesc, acc);
+    } else if constexpr (K >= 4) {
+        tc_mma_ss_k4(d_tmem, a, b, idesc, acc);
+        constexpr uint64_t box = 16384 >> 4;  // the next box, in descriptor units
+        if constexpr (K - 4 >= 2) tc_mma_ss_k2(d_tmem, a + box, b + box, idesc, 1u);
+        if constexpr ((K - 4) % 2 == 1) tc_mma_ss(d_tmem, a + box + 2 * ((K - 4) / 2), b + box + 2 * ((K - 4) / 2), idesc, 1u);
+    } else {
+        if constexpr (K >= 2) tc_mma_ss_k2(d_tmem, a, b, idesc, acc);
+        if constexpr (K % 2 == 1) tc_mma_ss(d_tmem, a + 2 * (K / 2), b + 2 * (K / 2), idesc, K >= 2 ? 1u : acc);
+    }
+}
+
+// Eight k-steps of 16 of a product with A from TMEM (bf16 pairs: 8 columns per k-step, the
+// columns of step kk at a_tmem + acol(kk)) and B MN-major in shared memory (2048 bytes, 128
+// descriptor units, per k-step).  acol(kk) = 8 kk when cols_gap is 0, else 8 (kk % 4) +
+// 64 (kk / 4) (two 64-column halves, as the backward's P^T / dS^T tiles are laid out).
+#define ATTN_TS_STEP(ac, bo)                         \
+    "add.u32 ta, %1, " #ac ";\n\t"                   \
+    "add.s64 rb, %2, " #bo ";\n\t"                   \
+    "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %3, q;\n\t"
+__device__ __forceinline__ void tc_mma_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 ta;\n\t.reg .b64 rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        ATTN_TS_STEP(8, 128) ATTN_TS_STEP(16, 256) ATTN_TS_STEP(24, 384) ATTN_TS_STEP(32, 512)
+        ATTN_TS_STEP(40, 640) ATTN_TS_STEP(48, 768) ATTN_TS_STEP(56, 896) "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_k8_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                    uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 ta;\n\t.reg .b64 rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        ATTN_TS_STEP(8, 128) ATTN_TS_STEP(16, 256) ATTN_TS_STEP(24, 384) ATTN_TS_STEP(64, 512)
+        ATTN_TS_STEP(72, 640) ATTN_TS_STEP(80, 768) ATTN_TS_STEP(88, 896) "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+#undef ATTN_TS_STEP
+
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
 //   bits  0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout (2 = 128B swizzle).
