@@ -35,6 +35,14 @@ namespace attn {
 namespace {
 
 constexpr int kWarps = 4;
+
+// Programmatic dependent launch: the chunk merge is launched while the split kernel drains.
+// Each split CTA signals once its partial is written (launch_dependents); the merge's blocks
+// wait for the split grid's completion, with its memory visible, before reading (wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Ring slots per warp: 3 page blocks for a bf16 cache and one query head per CTA (4 KB each at
 // d = 128: 96 KB per CTA, 2 CTAs per SM); 2 when the arithmetic per byte is higher -- an e4m3
 // cache (half the bytes per token; 2 KB blocks, 32 KB per CTA, 7 CTAs per SM) or several query
@@ -368,6 +376,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             ws[D + 1] = L;
         }
     }
+    griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------ grouped-query decode on mma
@@ -703,6 +712,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             ws[D + 1] = L;
         }
     }
+    griddep_launch_dependents();
 }
 
 // Merge of one (sequence, query head)'s chunk partials.  The splits' maxima, weights and
@@ -732,6 +742,7 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, int max_splits) {
     __shared__ float red[D / 32];
     __shared__ float wgt[kCombineWeights];
+    griddep_wait();  // the split kernel's partials are complete and visible
     const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
     const int cap = a.max_pages * kPS;
     const int ctx = min(max(a.ctx_lens[b], 0), cap);
@@ -818,8 +829,18 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     else if (group % 2 == 0) e = launch_decode_gk<D, 2>(a, max_splits, stream);
     else e = launch_decode_gk<D, 1>(a, max_splits, stream);
     if (e != cudaSuccess) return e;
-    dim3 g2(a.H, a.B);
-    decode_combine_kernel<D><<<g2, D, 0, stream>>>(a, max_splits);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.H, a.B);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a, max_splits);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
