@@ -51,31 +51,37 @@ template <int D> constexpr int kPad = D <= 64 ? 64 : 128;
 // Shape of the CTA per padded head dimension.
 //   128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 12 warps with a
 //        per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
-//   64:  one query tile per CTA, 6 warps, two CTAs per SM: at d = 64 a tile needs 256 TMEM
+//   64:  one query tile per CTA, two CTAs per SM: at d = 64 a tile needs 256 TMEM
 //        columns (S 128 | O 64 | P 64) and 80 KB of shared memory, and two co-resident CTAs
 //        overlap each other's serial chains (Q load, first S, softmax, PV, epilogue), which
 //        dominate the short units of small problems.
+//        Two MMA-issuing threads (kMmaIssuers = 2): warp 5 issues the S products and warp 6 the PV
+//        products.  With P in its own columns the two touch disjoint TMEM, and S(j+1) no longer
+//        waits behind PV(j-1), which waits for the previous softmax.  8 warps, so that the second
+//        warpgroup (producer, two issuers, one idle warp) can hand registers to the softmax.
+// Register split (setmaxnreg) per warpgroup, within the block's launch pool (threads x
+// registers at launch):
+//   128: launched at 168 (384 x 168 = 64512): 128 x (64 + 216 + 216) = 63488.
+//   64:  launched at 128 (two CTAs of 256 per SM): 128 x (64 + 192) = 32768 = 256 x 128.
 template <int P> struct CfgPad;
 template <int D> struct Cfg : CfgPad<kPad<D>> {};
 template <> struct CfgPad<128> {
-    static constexpr int QT = 2, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1;
+    static constexpr int QT = 2, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1, kMmaIssuers = 1;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr bool kSplitRegs = true;
+    static constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 64;
 };
 template <> struct CfgPad<64> {
-    static constexpr int QT = 1, kThreads = 192, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 2;
+    static constexpr int QT = 1, kThreads = 256, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 2, kMmaIssuers = 2;
     static constexpr uint32_t kTmemCols = 256;
-    static constexpr bool kSplitRegs = false;
+    static constexpr bool kSplitRegs = true;
+    static constexpr uint32_t kRegsSoftmax = 192, kRegsOther = 64;
 };
+static_assert(128 * (Cfg<128>::kRegsOther + 2 * Cfg<128>::kRegsSoftmax) <= 384 * 168, "d=128 register split");
+static_assert(128 * (Cfg<64>::kRegsOther + Cfg<64>::kRegsSoftmax) <= 256 * 128, "d=64 register split");
 static_assert(Cfg<64>::QT * (128 + 64 + 64) <= (int)Cfg<64>::kTmemCols, "d=64 TMEM layout");
 static_assert(Cfg<128>::QT * (128 + 128) <= (int)Cfg<128>::kTmemCols, "d=128 TMEM layout");
 constexpr int kQTilesMax = 2;
-// Register split (d = 128): launched at 168 per thread (384 x 168 = 64512 in the block's
-// pool); the producer/MMA warpgroup drops to 64 and each softmax warpgroup rises to 216:
-// 128 x (64 + 216 + 216) = 63488 <= 64512, and per SM sub-partition (one warp of each
-// warpgroup) 32 x 496 <= 16384 registers.
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 64;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -237,6 +243,56 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
         for (int f = (fills > kStages ? fills - kStages : 0); f < fills; ++f)
             (void)mbar_wait(&sm.u_full[f % kStages], (uint32_t)((f / kStages) & 1), drain, 91);
     }
+}
+
+// ------------------------------------------------------------------ MMA issuers, separate P
+// role 0 issues S(0) and every S(j+1) (as soon as the softmax has read S(j)); role 1 issues every
+// PV(j) (once P(j) is written).  S and PV touch disjoint TMEM columns (S | O | P), so neither
+// waits for the other.  Both walk every ring unit and commit its release (the empty barriers
+// count both): unit u = {K(u), V(u-1)} is read by S(u) and by PV(u-1).
+template <int D>
+__device__ void run_mma_sep(PrefillSmem<D> &sm, uint32_t tmem, int n_all, int role, WaitCtx wc) {
+    static_assert(SeparateP<D>::value && Cfg<D>::QT == 1, "one query tile, P in its own columns");
+    constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
+    constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
+    constexpr uint64_t kTile = (uint64_t)(kBM * kPad<D> * 2) >> 4;
+    const uint64_t dq = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+    const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
+    bool ok = true;
+    if (role == 0) {
+        ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.u_full[0], 0, wc, 10);
+        if (ok) {
+            tc_fence_after_sync();
+            tc_mma_ss_ksteps<D / 16>(tmem, dq, dk, idS, 0u);  // S(0) = Q K(0)^T (K(0) in slot 0)
+            tc_commit(&sm.s_full[0]);
+        }
+    }
+    tc_commit(&sm.u_empty[0]);
+    for (int j = 0; j < n_all && ok; ++j) {
+        const int u = j + 1;  // unit with V(j) and K(j+1)
+        if (!(ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13))) break;
+        if (role == 0) {
+            if (j + 1 < n_all) {
+                if (!(ok = mbar_wait(&sm.s_free[0], (uint32_t)(j & 1), wc, 17))) break;
+                tc_fence_after_sync();
+                tc_mma_ss_ksteps<D / 16>(tmem, dq, dk + ((u & 1) ? kTile : 0), idS, 0u);  // K(j+1): slot u % 2
+                tc_commit(&sm.s_full[0]);
+            }
+        } else {
+            if (!(ok = mbar_wait(&sm.p_full[0], (uint32_t)(j & 1), wc, 12))) break;
+            tc_fence_after_sync();
+            tc_mma_ts_k8(tmem + o_col<D>(0), tmem + p_col<D>(0), dv + ((u & 1) ? kTile : 0), idPV,
+                         j > 0 ? 1u : 0u);  // V(j): slot u % 2
+            tc_commit(&sm.pv_done[0]);
+            if (j == n_all - 1) tc_commit(&sm.o_done[0]);
+        }
+        tc_commit(&sm.u_empty[u % kStages]);
+    }
+    // wait (bounded) until every MMA issued above has finished with TMEM and smem
+    tc_commit(&sm.drain);
+    WaitCtx drain{nullptr, wc.status};
+    (void)mbar_wait(&sm.drain, 0, drain, 19);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -583,7 +639,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
         mbar_init(&sm.q_full, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.u_full[s], 1);
-            mbar_init(&sm.u_empty[s], 1);
+            mbar_init(&sm.u_empty[s], Cfg<D>::kMmaIssuers);
         }
         for (int t = 0; t < Cfg<D>::QT; ++t) {
             mbar_init(&sm.s_full[t], 1);
@@ -592,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
             mbar_init(&sm.s_free[t], kBM);
             mbar_init(&sm.pv_done[t], 1);
         }
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain, Cfg<D>::kMmaIssuers);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -607,14 +663,20 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     WaitCtx wc{&sm.abort_flag, p.status};
 
     if (warp >= 4 * Cfg<D>::QT) {
-        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<kRegsOther>();
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<Cfg<D>::kRegsOther>();
         if (warp == Cfg<D>::kProducerWarp) {
             if (lane == 0 && n_all > 0) run_producer<D>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
         } else if (warp == Cfg<D>::kMmaWarp) {
-            if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
+            if constexpr (Cfg<D>::kMmaIssuers == 2) {
+                if (lane == 0 && n_all > 0) run_mma_sep<D>(sm, tmem, n_all, 0, wc);
+            } else {
+                if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
+            }
+        } else if constexpr (Cfg<D>::kMmaIssuers == 2) {
+            if (warp == Cfg<D>::kMmaWarp + 1 && lane == 0 && n_all > 0) run_mma_sep<D>(sm, tmem, n_all, 1, wc);
         }
     } else {
-        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<kRegsSoftmax>();
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<Cfg<D>::kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
         run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
     }
