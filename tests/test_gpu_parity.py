@@ -95,6 +95,29 @@ def test_prefill_small_vs_oracle(lib, oracle_mod, shape):
     compare(o, lse, o_ref, lse_ref, shape.name, o_max=o_max)
 
 
+GROWING_KEYS = [
+    workloads.PrefillShape("growing keys d128 causal", 1, 2, 520, 520, 128, True, seed=25),
+    workloads.PrefillShape("growing keys d128 non-causal", 2, 1, 130, 600, 128, False, seed=26),
+    workloads.PrefillShape("growing keys d64 causal", 1, 2, 520, 520, 64, True, seed=27),
+]
+
+
+@pytest.mark.parametrize("shape", GROWING_KEYS, ids=lambda s: s.name)
+def test_prefill_running_max_jumps(lib, oracle_mod, shape):
+    """Key j scaled by 1 + j/16: a row's largest score grows by about 30 (log2 units) from one
+    128-key tile to the next, far past the lazy-rescale threshold of 8, so the running maximum,
+    the normaliser and O move on most tiles (82-98 % of the fully visible (row, tile) pairs of
+    these inputs, counted in fp64 from the scores)."""
+    inp = workloads.prefill_inputs(shape)
+    grow = 1.0 + torch.arange(shape.Nkv, dtype=torch.float32) / 16.0
+    inp["k"] = (inp["k"].float() * grow[:, None]).to(torch.bfloat16)
+    inp, kl, o, lse = run_prefill(lib, shape, inputs=inp)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inp["q"], inp["k"], inp["v"], shape.causal, shape.scale, kv_lens=kl)
+    # the softmax is nearly one-hot here: the bound of the peaked-softmax cases applies
+    o_max = max(O_MAX, 2.0 ** -8 * float(inp["v"].float().abs().max()))
+    compare(o, lse, o_ref, lse_ref, shape.name, o_max=o_max)
+
+
 def test_prefill_zero_length_and_full_padding(lib, oracle_mod):
     shape = workloads.PrefillShape("kv_len 0 / 129 / 256", 3, 2, 256, 256, 64, True, seed=30)
     inp, kl, o, lse = run_prefill(lib, shape, kv_lens=[0, 129, 256])
