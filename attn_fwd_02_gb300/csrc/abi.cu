@@ -396,7 +396,7 @@ ATTN_API const char *attn_status_string(int status) {
         case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or oversized dimension, bad scale)";
         case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 32, 64, 80, 96 or 128 for prefill, 64 or 128 for decode and backward; page size 16; device sm_103)";
         case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment)";
-        case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size()";
+        case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size() (decode) or attn_bwd_workspace_size() (backward)";
         case ATTN_ERR_CUDA: return "CUDA runtime error or launch failure";
         case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out; results of the affected calls are invalid";
         case ATTN_ERR_SCRATCH_LIMIT: return "sizes need more decode scratch than the 12 MiB static array of paged_attn_decode_noalloc (use paged_attn_decode with a workspace)";
