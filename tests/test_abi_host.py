@@ -184,3 +184,42 @@ def test_product_package_never_imports_the_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+def test_grouped_query_argument_checks(lib):
+    gqa = lambda Hq=4, Hkv=2, **kw: lib.attn_fwd_gqa(
+        kw.get("q", ALIGNED), ALIGNED, ALIGNED, ALIGNED, None, 1, Hq, Hkv, 128, 128, kw.get("d", 64), 1, 0.125, None,
+        None)
+    assert gqa(Hkv=3) == 1  # query heads not a multiple of the key/value heads
+    assert gqa(Hkv=0) == 1
+    assert gqa(Hq=2, Hkv=4) == 1
+    assert gqa(d=48) == 2
+    assert gqa(q=ALIGNED + 8) == 3
+    dec = lambda H=4, Hkv=2, **kw: lib.paged_attn_decode_gqa(
+        ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 16, ALIGNED, None, 2, H, Hkv, kw.get("d", 128), 4, 8, 0.1,
+        kw.get("ws", ALIGNED), 1 << 20, None)
+    assert dec(Hkv=3) == 1
+    assert dec(Hkv=-1) == 1
+    assert dec(d=96) == 2
+    assert dec(ws=None) == 4
+
+
+def test_paged_prefill_and_append_argument_checks(lib):
+    pre = lambda **kw: lib.paged_attn_prefill(
+        ALIGNED, ALIGNED, ALIGNED, kw.get("pt", ALIGNED), kw.get("cl", ALIGNED), kw.get("ps", 16),
+        kw.get("o", ALIGNED), None, 1, kw.get("H", 4), kw.get("Hkv", 2), kw.get("Nq", 64), kw.get("d", 128),
+        kw.get("maxp", 8), kw.get("npages", 16), 1, kw.get("scale", 0.1), None)
+    assert pre(pt=None) == 1 and pre(cl=None) == 1 and pre(o=None) == 1
+    assert pre(Nq=0) == 1 and pre(maxp=0) == 1 and pre(npages=0) == 1
+    assert pre(Hkv=3) == 1
+    assert pre(scale=float("nan")) == 1
+    assert pre(maxp=1 << 27) == 1  # capacity past 2^30 tokens
+    assert pre(ps=32) == 2 and pre(d=48) == 2
+    assert pre(pt=ALIGNED + 2) == 3 and pre(cl=ALIGNED + 1) == 3 and pre(o=ALIGNED + 8) == 3
+    app = lambda **kw: lib.paged_kv_append(
+        kw.get("kn", ALIGNED), ALIGNED, kw.get("kp", ALIGNED), ALIGNED, kw.get("pt", ALIGNED), kw.get("sp", ALIGNED),
+        kw.get("ps", 16), 1, 2, kw.get("n", 4), kw.get("d", 96), 4, 8, None)
+    assert app(kn=None) == 1 and app(pt=None) == 1 and app(sp=None) == 1
+    assert app(n=0) == 1
+    assert app(d=48) == 2 and app(ps=8) == 2
+    assert app(kn=ALIGNED + 8) == 3 and app(kp=ALIGNED + 4) == 3 and app(sp=ALIGNED + 2) == 3
