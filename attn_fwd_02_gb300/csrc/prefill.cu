@@ -298,6 +298,7 @@ __device__ void run_mma_sep(PrefillSmem<D> &sm, uint32_t tmem, int n_all, int ro
 // ------------------------------------------------------------------ MMA issuer
 template <int D>
 __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
+    static_assert(!SeparateP<D>::value, "P over S; the separate-P shape uses run_mma_sep");
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
     static_assert(kStages == 2, "slot selects below");
@@ -340,28 +341,8 @@ __device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTile
             const int u = j + 1;  // unit with V(j) and K(j+1)
             ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13);
             if (!ok) break;
-            if constexpr (SeparateP<D>::value) {
-                // both S_t(j+1) first (a buffer is free once its softmax has read S_t(j)), then
-                // both PV_t(j): the softmax warpgroups find their next scores ready
-                for (int t = 0; t < Cfg<D>::QT && ok; ++t) {
-                    if (j + 1 < n[t]) {
-                        if (!(ok = mbar_wait(&sm.s_free[t], (uint32_t)(j & 1), wc, 17 + t))) break;
-                        tc_fence_after_sync();
-                        issue_S(t, j + 1);
-                    }
-                }
-                for (int t = 0; t < Cfg<D>::QT && ok; ++t) {
-                    if (j < n[t]) {
-                        if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
-                        tc_fence_after_sync();
-                        issue_PV(t, j);
-                        tc_commit(&sm.pv_done[t]);
-                        if (j == n[t] - 1) tc_commit(&sm.o_done[t]);
-                    }
-                }
-            }
             // P over S: PV_t(j) must be issued before S_t(j+1) overwrites its buffer
-            for (int t = 0; t < Cfg<D>::QT && !SeparateP<D>::value; ++t) {
+            for (int t = 0; t < Cfg<D>::QT; ++t) {
                 if (j < n[t]) {
                     if (!(ok = mbar_wait(&sm.p_full[t], (uint32_t)(j & 1), wc, 12 + 8 * t))) break;
                     tc_fence_after_sync();
