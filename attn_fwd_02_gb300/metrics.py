@@ -59,6 +59,19 @@ def decode_bytes(H: int, d: int, ctx_lens, page_size: int, elem: int = 2, lse: b
     return kv + qo + pt + (4.0 * B * H if lse else 0.0)
 
 
+def paged_prefill_bytes(H: int, Nq: int, d: int, ctx_lens, page_size: int, kv_heads: int | None = None,
+                        elem: int = 2, lse: bool = True) -> float:
+    """Chunked prefill over the paged cache: K and V of every cached token once (kv_heads cache
+    heads, default H), the Nq queries and their outputs once, LSE fp32, page-table entries used."""
+    ctx = [int(x) for x in ctx_lens]
+    B = len(ctx)
+    Hkv = H if kv_heads is None else kv_heads
+    kv = 2.0 * Hkv * d * elem * float(sum(ctx))
+    qo = 2.0 * B * H * Nq * d * elem
+    pt = 4.0 * float(sum(-(-c // page_size) for c in ctx))
+    return kv + qo + pt + (4.0 * B * H * Nq if lse else 0.0)
+
+
 def paged_prefill_flops(H: int, Nq: int, d: int, ctx_lens, causal: bool = True) -> float:
     """FLOPs of a chunked prefill whose Nq queries are the last Nq of ctx_b cached tokens:
     4*d per (query, visible key); with the bottom-right causal mask query i sees

@@ -286,6 +286,7 @@ class PagedPrefillCase:
         self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device="cuda")
         self.ctx = [int(x) for x in inp["ctx_lens"]]
         self.flops = metrics.paged_prefill_flops(shape.H, nq, shape.d, self.ctx, causal=True)
+        self.bytes = metrics.paged_prefill_bytes(shape.H, nq, shape.d, self.ctx, shape.page_size, kv_heads=kv_heads)
         self.launches = 1
 
     def run(self):

@@ -441,3 +441,11 @@ def test_paged_prefill_flop_count_closed_form():
     assert paged_prefill_flops(2, 1, 16, [7, 9]) == 4 * 16 * 2 * (7 + 9)
     # non-causal: every query sees every cached key
     assert paged_prefill_flops(1, 4, 2, [6], causal=False) == 4 * 2 * 4 * 6
+
+
+def test_paged_prefill_byte_count():
+    from attn_fwd_02_gb300.metrics import decode_bytes, paged_prefill_bytes
+    # with one query per sequence it moves exactly what a decode step moves
+    assert paged_prefill_bytes(4, 1, 64, [17, 300], 16, kv_heads=2) == decode_bytes(4, 64, [17, 300], 16, kv_heads=2)
+    # by hand: 2 cache heads x 33 tokens of K and V (bf16), 4 heads x 5 queries of Q and O, LSE, 3 table entries
+    assert paged_prefill_bytes(4, 5, 8, [33], 16, kv_heads=2) == 2 * 2 * 8 * 2 * 33 + 2 * 4 * 5 * 8 * 2 + 4 * 4 * 5 + 4 * 3
