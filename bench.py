@@ -768,14 +768,42 @@ def reference_arm(args):
         sample = f"per step, seeded random query rows of {shape.name} for about {budget:.0f} s of fp64 C"
         cfgname = shape.name
         ms = statistics.mean(ms_l)
+    cfg = {"workload": cfgname, "l2": "n/a (CPU)"}
+    if shape is not None:
+        cfg["prefill"] = {"B": shape.B, "H": shape.H, "Nq": shape.Nq, "Nkv": shape.Nkv, "d": shape.d,
+                          "causal": shape.causal, "scale": shape.scale, "value_scale": shape.value_scale,
+                          "kv_len_range": shape.kv_len_range}
+    decode = None
+    if args.workload == "default":
+        # the default step is the prefill plus the paged decode: the decode leg, one whole oracle
+        # decode per step (about 0.1 s), is reported beside the prefill as the GPU arm reports it
+        dshape = workloads.PAGED_DECODE
+        dinp = workloads.decode_inputs(dshape)
+        ctx = [int(x) for x in dinp["ctx_lens"]]
+        dbytes = metrics.decode_bytes(dshape.H, dshape.d, ctx, dshape.page_size)
+        times = []
+        for s in range(args.warmup + args.steps):
+            t = time.perf_counter()
+            oracle.paged_decode(dinp["q"], dinp["k_pages"], dinp["v_pages"], dinp["page_table"], dinp["ctx_lens"],
+                                dshape.scale)
+            if s >= args.warmup:
+                times.append(time.perf_counter() - t)
+        decode = {"value": round(dbytes / statistics.mean(times) / 1e9, 3), "unit": "GB/s",
+                  "ms_per_call": round(statistics.mean(times) * 1e3, 1), "bytes_per_call": dbytes,
+                  "sample": f"the whole {dshape.name} per step"}
+        cfg["workload"] = f"{shape.name} + {dshape.name}"
+        cfg["decode"] = {"workload": dshape.name, "B": dshape.B, "H": dshape.H, "d": dshape.d,
+                         "page_size": dshape.page_size, "ctx_range": list(dshape.ctx_range), "ctx_total": sum(ctx)}
     out = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": unit, "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.randn -> bf16)",
-           "config": {"workload": cfgname, "l2": "n/a (CPU)"},
+           "config": cfg,
            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": round(val, 6),
                             "unit": unit},
            "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
            "gpu_launches": 0}
+    if decode is not None:
+        out["decode"] = decode
     print(json.dumps(out), flush=True)
 
 
