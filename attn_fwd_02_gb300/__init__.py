@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_workspace_size,
     attn_check_device_status,
+    attn_last_device_status,
     attn_selftest_bounded_wait,
     attn_fwd,
     attn_fwd_gqa,
@@ -24,5 +25,7 @@ from .binding import (  # noqa: F401
     paged_attn_prefill,
     paged_kv_append,
     paged_kv_append_fp8,
+    paged_attn_decode_gqa_workspace_size,
     paged_attn_decode_workspace_size,
+    paged_attn_decode_workspace_size_ctx,
 )

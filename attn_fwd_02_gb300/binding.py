@@ -31,6 +31,8 @@ SIGNATURES = {
     "attn_fwd_kvlen": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P]),
     "attn_fwd_gqa": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]),
     "paged_attn_decode_workspace_size": (Z, [I, I, I, I, I]),
+    "paged_attn_decode_workspace_size_ctx": (Z, [I, I, I, I]),
+    "paged_attn_decode_gqa_workspace_size": (Z, [I, I, I, I, I, I]),
     "paged_attn_decode": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P, Z, P]),
     "paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, F, P]),
     "paged_attn_decode_gqa": (I, [P, P, P, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
@@ -42,6 +44,7 @@ SIGNATURES = {
     "paged_kv_append_fp8": (I, [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, P]),
     "attn_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, Z, P]),
     "attn_check_device_status": (I, [P]),
+    "attn_last_device_status": (I, []),
     "attn_selftest_bounded_wait": (I, [P]),
     "attn_status_string": (ctypes.c_char_p, [I]),
     "attn_version": (ctypes.c_char_p, []),
@@ -113,6 +116,31 @@ def _require(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _out_like(out, like, name):
+    """``out`` given by the caller must match ``like`` (dtype, shape, device) and be contiguous;
+    None allocates one with torch."""
+    import torch
+    if out is None:
+        return torch.empty_like(like)
+    _require(out, name, like.dtype, like.dim())
+    if tuple(out.shape) != tuple(like.shape) or out.device != like.device:
+        raise ValueError(f"{name} must be {tuple(like.shape)} on {like.device}, got {tuple(out.shape)} "
+                         f"on {out.device}")
+    return out
+
+
+def _lse_out(lse, shape, device, want: bool):
+    """fp32 log-sum-exp output of the given shape on ``device``: checked if given, allocated
+    if None and wanted."""
+    import torch
+    if lse is None:
+        return torch.empty(shape, dtype=torch.float32, device=device) if want else None
+    _require(lse, "lse", torch.float32, len(shape))
+    if tuple(lse.shape) != tuple(shape) or lse.device != device:
+        raise ValueError(f"lse must be {tuple(shape)} on {device}, got {tuple(lse.shape)} on {lse.device}")
+    return lse
+
+
 def attn_fwd_kvlen(q, k, v, causal: bool, scale: float | None = None, kv_lens=None,
                    out=None, lse=None, return_lse: bool = True, stream=None):
     """Prefill attention. q [B,H,Nq,d], k/v [B,H,Nkv,d] bf16 CUDA tensors;
@@ -128,10 +156,8 @@ def attn_fwd_kvlen(q, k, v, causal: bool, scale: float | None = None, kv_lens=No
         _require(kv_lens, "kv_lens", torch.int32, 1)
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H, Nq), q.device, return_lse)
     lib = load_library()
     st = lib.attn_fwd_kvlen(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, H, Nq, Nkv, d,
                             int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
@@ -154,10 +180,8 @@ def attn_fwd_gqa(q, k, v, causal: bool, scale: float | None = None, kv_lens=None
         _require(kv_lens, "kv_lens", torch.int32, 1)
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, Hq, Nq), q.device, return_lse)
     st = load_library().attn_fwd_gqa(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, Hq, Hkv, Nq, Nkv,
                                      d, int(bool(causal)), float(scale), _dptr(kv_lens), _stream_ptr(stream))
     _check("attn_fwd_gqa", st)
@@ -172,6 +196,10 @@ def kv_quantize_fp8(x, scale: float, out=None, stream=None):
         raise TypeError("x must be a contiguous bf16 CUDA tensor")
     if out is None:
         out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    else:
+        _require(out, "out", torch.uint8, x.dim())
+        if tuple(out.shape) != tuple(x.shape) or out.device != x.device:
+            raise ValueError("out must be a uint8 tensor of x's shape on x's device")
     st = load_library().kv_quantize_fp8(_dptr(x), _dptr(out), x.numel(), float(scale), _stream_ptr(stream))
     _check("kv_quantize_fp8", st)
     return out
@@ -218,13 +246,11 @@ def paged_attn_decode_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float, p
         scale = d ** -0.5
     max_pages = page_table.shape[1]
     lib = load_library()
-    need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, ps))
+    need = int(lib.paged_attn_decode_gqa_workspace_size(B, H, Hkv, d, max_pages, ps))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H), q.device, return_lse)
     st = lib.paged_attn_decode_fp8(_dptr(q), _dptr(k_pages), _dptr(v_pages), float(k_scale), float(v_scale),
                                    _dptr(page_table), _dptr(ctx_lens), ps, _dptr(out), _dptr(lse), B, H, Hkv, d,
                                    max_pages, P, float(scale), _dptr(workspace),
@@ -257,9 +283,9 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float | None = None, kv
         _require(kv_lens, "kv_lens", torch.int32, 1)
     if scale is None:
         scale = d ** -0.5
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = _out_like(dq, q, "dq")
+    dk = _out_like(dk, k, "dk")
+    dv = _out_like(dv, v, "dv")
     lib = load_library()
     need = int(lib.attn_bwd_workspace_size(B, Hq, Nq))
     if workspace is None:
@@ -283,10 +309,8 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=No
         raise ValueError("k and v must be [B, H, Nkv, d] matching q")
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H, Nq), q.device, return_lse)
     lib = load_library()
     st = lib.attn_fwd(_dptr(q), _dptr(k), _dptr(v), _dptr(out), _dptr(lse), B, H, Nq, Nkv, d,
                       int(bool(causal)), float(scale), _stream_ptr(stream))
@@ -297,6 +321,15 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None, out=None, lse=No
 def paged_attn_decode_workspace_size(B: int, H: int, d: int, max_pages_per_seq: int,
                                      page_size: int = 16) -> int:
     return int(load_library().paged_attn_decode_workspace_size(B, H, d, max_pages_per_seq, page_size))
+
+
+def paged_attn_decode_workspace_size_ctx(B: int, H: int, d: int, max_ctx_len: int) -> int:
+    return int(load_library().paged_attn_decode_workspace_size_ctx(B, H, d, max_ctx_len))
+
+
+def paged_attn_decode_gqa_workspace_size(B: int, H: int, Hkv: int, d: int, max_pages_per_seq: int,
+                                         page_size: int = 16) -> int:
+    return int(load_library().paged_attn_decode_gqa_workspace_size(B, H, Hkv, d, max_pages_per_seq, page_size))
 
 
 def paged_attn_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float | None = None,
@@ -320,10 +353,8 @@ def paged_attn_decode(q, k_pages, v_pages, page_table, ctx_lens, scale: float | 
     max_pages = page_table.shape[1]
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H), q.device, return_lse)
     lib = load_library()
     need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, page_size))
     if workspace is None:
@@ -355,12 +386,10 @@ def paged_attn_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: floa
     max_pages = page_table.shape[1]
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H), q.device, return_lse)
     lib = load_library()
-    need = int(lib.paged_attn_decode_workspace_size(B, H, d, max_pages, page_size))
+    need = int(lib.paged_attn_decode_gqa_workspace_size(B, H, Hkv, d, max_pages, page_size))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     st = lib.paged_attn_decode_gqa(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table), _dptr(ctx_lens),
@@ -375,8 +404,9 @@ def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: 
                               out=None, lse=None, return_lse: bool = True, stream=None):
     """paged_attn_decode without a workspace, for callers that cannot allocate device
     memory: the library keeps the chunk partials in its own fixed 12 MiB device array.
-    Pass ``out`` (and ``lse``) to avoid any allocation here as well.  Calls that may
-    overlap on the GPU share that array and must be ordered by the caller.
+    Pass ``out`` (bf16, q's shape) and ``lse`` (fp32 [B, H]), both contiguous on q's device,
+    to avoid any allocation here as well.  Calls that may overlap on the GPU share that
+    array and must be ordered by the caller.
     Returns (o, lse)."""
     import torch
     _require(q, "q", torch.bfloat16, 3)
@@ -392,10 +422,8 @@ def paged_attn_decode_noalloc(q, k_pages, v_pages, page_table, ctx_lens, scale: 
         raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H), q.device, return_lse)
     st = load_library().paged_attn_decode_noalloc(
         _dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table), _dptr(ctx_lens), page_size, _dptr(out),
         _dptr(lse), B, H, d, page_table.shape[1], num_pages, float(scale), _stream_ptr(stream))
@@ -422,10 +450,8 @@ def paged_attn_prefill(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, 
         raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
     if scale is None:
         scale = d ** -0.5
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H, Nq), q.device, return_lse)
     st = load_library().paged_attn_prefill(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(page_table),
                                            _dptr(ctx_lens), page_size, _dptr(out), _dptr(lse), B, H, Hkv, Nq, d,
                                            page_table.shape[1], num_pages, int(bool(causal)), float(scale),
@@ -462,3 +488,8 @@ def attn_selftest_bounded_wait(stream=None) -> None:
 def attn_check_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the library's device status word."""
     return int(load_library().attn_check_device_status(_stream_ptr(stream)))
+
+
+def attn_last_device_status() -> int:
+    """The current device's host-visible timeout flag, without synchronising or clearing."""
+    return int(load_library().attn_last_device_status())

@@ -2,6 +2,7 @@
 // checks, the device status word, and dispatch to the kernel launchers.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -12,29 +13,71 @@
 
 namespace {
 
-__device__ int g_status[2];  // [0]: bit flags (1 = a bounded wait ran out), [1]: first failing site
+// Device status word (see sm103_ptx.cuh): [0] flags, [1] first failing site, [2..3] the address
+// of this device's host-visible flag.
+__device__ __align__(8) int g_status[4];
 
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices];
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 std::mutex g_mu;
 
-// Per-device set-up: status-word address and architecture check.
-int device_setup(int **status_out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
+// Host-visible timeout flags, one per device (16 ints apart), in one page of the library's own
+// static storage that is page-locked and mapped for the GPUs once per process.  A kernel whose
+// bounded wait runs out stores 1 into its device's flag (and fences), so the host can see the
+// timeout with a plain load, without synchronising any stream.
+alignas(4096) volatile int g_host_flags[kMaxDevices * 16];
+int g_host_flags_registered = 0;  // 0 not yet, 1 registered, -1 failed
+
+int *host_flag_of(int dev) { return const_cast<int *>(&g_host_flags[dev * 16]); }
+
+// Per-device set-up, done once per device by the first call on it (with the device current):
+// architecture check, the status word's device address, registration of the flag page, and a
+// copy of the flag's device-side address into the status word.  The copy is synchronous, so the
+// first call on each device should come before any stream capture.
+int device_setup_locked(int dev) {
     if (g_arch_ok[dev] == 0) {
         cudaDeviceProp prop;
         if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return ATTN_ERR_CUDA;
         g_arch_ok[dev] = (prop.major == 10 && prop.minor == 3) ? 1 : -1;
     }
     if (g_arch_ok[dev] != 1) return ATTN_ERR_UNSUPPORTED;
-    if (!g_status_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess || !p) return ATTN_ERR_CUDA;
-        g_status_ptr[dev] = static_cast<int *>(p);
+    if (g_status_ptr[dev]) return ATTN_OK;
+    if (g_host_flags_registered == 0) {
+        const cudaError_t e = cudaHostRegister(const_cast<int *>(g_host_flags), sizeof(g_host_flags),
+                                               cudaHostRegisterMapped | cudaHostRegisterPortable);
+        g_host_flags_registered = (e == cudaSuccess) ? 1 : -1;
     }
+    if (g_host_flags_registered != 1) return ATTN_ERR_CUDA;
+    void *flag_dev = nullptr;
+    if (cudaHostGetDevicePointer(&flag_dev, host_flag_of(dev), 0) != cudaSuccess || !flag_dev) return ATTN_ERR_CUDA;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+    int init[4] = {0, 0, 0, 0};
+    static_assert(sizeof(void *) == 2 * sizeof(int), "64-bit device addresses");
+    memcpy(&init[2], &flag_dev, sizeof flag_dev);
+    if (cudaMemcpy(p, init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    *host_flag_of(dev) = 0;
+    g_status_ptr[dev] = static_cast<int *>(p);
+    return ATTN_OK;
+}
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+// Set-up for a call that launches work: also refuses (ATTN_ERR_DEVICE_TIMEOUT, nothing
+// launched) while a timeout recorded by an earlier call on this device is not yet cleared.
+int device_setup(int **status_out) {
+    int dev = -1;
+    if (current_device(&dev) != ATTN_OK) return ATTN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int st = device_setup_locked(dev);
+        if (st != ATTN_OK) return st;
+    }
+    if (*host_flag_of(dev) != 0) return ATTN_ERR_DEVICE_TIMEOUT;
     *status_out = g_status_ptr[dev];
     return ATTN_OK;
 }
@@ -235,28 +278,50 @@ ATTN_API int paged_kv_append(const void *k_new, const void *v_new, void *k_pages
 }
 
 ATTN_API size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size) {
-    return attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    return attn::decode_workspace_bytes(B, H, H, d, max_pages_per_seq, page_size);
+}
+
+ATTN_API size_t paged_attn_decode_workspace_size_ctx(int B, int H, int d, int max_ctx_len) {
+    if (max_ctx_len <= 0) return 0;
+    return attn::decode_workspace_bytes(B, H, H, d, (int)(((int64_t)max_ctx_len + 15) / 16), 16);
+}
+
+ATTN_API size_t paged_attn_decode_gqa_workspace_size(int B, int H, int Hkv, int d, int max_pages_per_seq,
+                                                     int page_size) {
+    return attn::decode_workspace_bytes(B, H, Hkv, d, max_pages_per_seq, page_size);
 }
 
 namespace {
 bool finite_positive(float x) { return x > 0.f && x < 3.0e38f; }
+// Head dims of the decode kernels.
+bool decode_head_dim(int d) { return d == 64 || d == 128; }
 
-int decode_checks(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
-                  const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
-                  int max_pages_per_seq, int num_pages, float scale, void *workspace, size_t workspace_bytes) {
+// Checks shared by every decode entry point: everything but the caller's workspace.
+int decode_arg_checks(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                      const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
+                      int max_pages_per_seq, int num_pages, float scale) {
     if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
         return ATTN_ERR_INVALID_ARG;
     if (Hkv <= 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if ((uint64_t)num_pages * (uint64_t)Hkv > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;  // TMA rows
     if (!finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!decode_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
     if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;  // grid y/z limits
     if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
     if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
-    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    return ATTN_OK;
+}
+
+int decode_checks(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                  const int32_t *ctx_lens, int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
+                  int max_pages_per_seq, int num_pages, float scale, void *workspace, size_t workspace_bytes) {
+    const int st = decode_arg_checks(q, k_pages, v_pages, page_table, ctx_lens, page_size, o, lse, B, H, Hkv, d,
+                                     max_pages_per_seq, num_pages, scale);
+    if (st != ATTN_OK) return st;
+    const size_t need = attn::decode_workspace_bytes(B, H, Hkv, d, max_pages_per_seq, page_size);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
     return ATTN_OK;
 }
@@ -348,20 +413,13 @@ ATTN_API int paged_attn_decode_noalloc(const void *q, const void *k_pages, const
                                        const int32_t *page_table, const int32_t *ctx_lens, int page_size, void *o,
                                        float *lse, int B, int H, int d, int max_pages_per_seq, int num_pages,
                                        float scale, attn_stream_t stream) {
-    if (!q || !k_pages || !v_pages || !page_table || !ctx_lens || !o) return ATTN_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (!(scale > 0.f) || !(scale < 3.0e38f)) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
-    if (B > 65535 || H > 65535) return ATTN_ERR_INVALID_ARG;
-    if ((uint64_t)max_pages_per_seq * (uint64_t)page_size > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
-    if (!aligned4(page_table) || !aligned4(ctx_lens) || (lse && !aligned4(lse))) return ATTN_ERR_MISALIGNED;
-    const size_t need = attn::decode_workspace_bytes(B, H, d, max_pages_per_seq, page_size);
+    int st = decode_arg_checks(q, k_pages, v_pages, page_table, ctx_lens, page_size, o, lse, B, H, H, d,
+                               max_pages_per_seq, num_pages, scale);
+    if (st != ATTN_OK) return st;
+    const size_t need = attn::decode_workspace_bytes(B, H, H, d, max_pages_per_seq, page_size);
     if (need == 0 || need > attn::decode_noalloc_scratch_bytes()) return ATTN_ERR_SCRATCH_LIMIT;
     int *status = nullptr;
-    int st = device_setup(&status);
+    st = device_setup(&status);
     if (st != ATTN_OK) return st;
     attn::DecodeArgs a{q,  k_pages, v_pages, page_table, ctx_lens, o, lse, nullptr, status, B, H, d, page_size,
                        max_pages_per_seq, num_pages, scale, H};
@@ -378,27 +436,46 @@ ATTN_API int attn_selftest_bounded_wait(attn_stream_t stream) {
 }
 
 ATTN_API int attn_check_device_status(attn_stream_t stream) {
+    int dev = -1;
+    if (current_device(&dev) != ATTN_OK) return ATTN_ERR_CUDA;
     int *status = nullptr;
-    int st = device_setup(&status);
-    if (st != ATTN_OK) return st;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int st = device_setup_locked(dev);
+        if (st != ATTN_OK) return st;
+        status = g_status_ptr[dev];
+    }
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     int h[2] = {0, 0};
     if (cudaMemcpy(h, status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (h[0] == 0) return ATTN_OK;
-    const int zero[2] = {0, 0};
+    const bool timed_out = h[0] != 0 || *host_flag_of(dev) != 0;
+    if (!timed_out) return ATTN_OK;
+    const int zero[2] = {0, 0};  // flags and site; the flag address in [2..3] stays
     if (cudaMemcpy(status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    *host_flag_of(dev) = 0;
     return ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+ATTN_API int attn_last_device_status(void) {
+    int dev = -1;
+    if (current_device(&dev) != ATTN_OK) return ATTN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int st = device_setup_locked(dev);
+        if (st != ATTN_OK) return st;
+    }
+    return *host_flag_of(dev) != 0 ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
 }
 
 ATTN_API const char *attn_status_string(int status) {
     switch (status) {
         case ATTN_OK: return "ok";
         case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive or oversized dimension, bad scale)";
-        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 32, 64, 80, 96 or 128 for prefill, 64 or 128 for decode and backward; page size 16; device sm_103)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim 32, 64, 80, 96 or 128; 64 or 128 for the backward; page size 16; device sm_103)";
         case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment)";
         case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than paged_attn_decode_workspace_size() (decode) or attn_bwd_workspace_size() (backward)";
         case ATTN_ERR_CUDA: return "CUDA runtime error or launch failure";
-        case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out; results of the affected calls are invalid";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out; results of the affected calls are invalid, and calls launch nothing until attn_check_device_status() clears it";
         case ATTN_ERR_SCRATCH_LIMIT: return "sizes need more decode scratch than the 12 MiB static array of paged_attn_decode_noalloc (use paged_attn_decode with a workspace)";
         default: return "unknown status";
     }

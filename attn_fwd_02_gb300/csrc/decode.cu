@@ -56,6 +56,11 @@ constexpr int kPS = 16;    // page size (tokens)
 // x 8 key/value heads (4 query heads each), contexts U[512, 8192]: 512 tokens 5.84-5.90 TB/s,
 // 1024 5.97, 2048 5.78-5.81 (too few CTAs for an even last wave).
 constexpr int kGqaChunkTokens = 2 * kDecodeChunkTokens;
+// Tokens per split for H query heads over Hkv cache heads: groups of two or more query heads run
+// the grouped-query kernel and its longer splits.
+__host__ __device__ constexpr int decode_chunk_tokens(int H, int Hkv) {
+    return (H / Hkv) % 2 == 0 ? kGqaChunkTokens : kDecodeChunkTokens;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -828,7 +833,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     // query heads per CTA: the largest of 8, 4, 2, 1 dividing the group size; groups of two or more
     // run the grouped-query kernel and its longer chunks
     const int group = a.H / a.Hkv;
-    const int chunk = group % 2 == 0 ? kGqaChunkTokens : kDecodeChunkTokens;
+    const int chunk = decode_chunk_tokens(a.H, a.Hkv);
     const int max_splits = (a.max_pages * kPS + chunk - 1) / chunk;
     cudaError_t e;
     if (group % 8 == 0) e = launch_decode_gk<D, 8>(a, max_splits, stream);
@@ -853,9 +858,12 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size) {
-    if (B <= 0 || H <= 0 || max_pages <= 0 || page_size != kPS || (d != 64 && d != 128)) return 0;
-    const size_t max_splits = ((size_t)max_pages * kPS + kDecodeChunkTokens - 1) / kDecodeChunkTokens;
+size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int max_pages, int page_size) {
+    if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || max_pages <= 0 || page_size != kPS ||
+        (d != 64 && d != 128))
+        return 0;
+    const size_t chunk = (size_t)decode_chunk_tokens(H, Hkv);
+    const size_t max_splits = ((size_t)max_pages * kPS + chunk - 1) / chunk;
     return (size_t)B * H * max_splits * (size_t)(d + 4) * sizeof(float);
 }
 
@@ -876,9 +884,12 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
 // buffers.  For them the chunk partials live in a fixed array in this library's
 // own device memory.  Every GPU that loads the library holds this array until
 // the process exits.  All calls share it: its contents are whatever the last
-// call left, and nothing in it needs clearing because each call writes every
-// slot it later reads.  Calls that overlap on the GPU (different streams, or
-// different host threads without ordering) race on it.
+// call left.  Nothing in it needs clearing: a call that completes normally
+// writes every slot it later reads.  A split CTA whose bounded wait runs out
+// returns without writing its partial, so the merge of that call may read an
+// earlier call's partial; the call's status (ATTN_ERR_DEVICE_TIMEOUT) already
+// marks its result invalid.  Calls that overlap on the GPU (different streams,
+// or different host threads without ordering) race on it.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 12u << 20;  // 12 MiB: e.g. B=32, H=32, d=128, 8192-token contexts

@@ -86,8 +86,9 @@ cudaError_t launch_kv_append_fp8(const void *k_new, const void *v_new, void *k_p
 // Launches the split kernel and the combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 
-// Workspace bytes the decode needs (0 if the sizes are unsupported).
-size_t decode_workspace_bytes(int B, int H, int d, int max_pages, int page_size);
+// Workspace bytes the decode needs for H query heads over Hkv cache heads (0 if the sizes are
+// unsupported).
+size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int max_pages, int page_size);
 
 // Same kernels with the chunk partials in the library's static scratch array
 // (no workspace from the caller); see decode.cu.

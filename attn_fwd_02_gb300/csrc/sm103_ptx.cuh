@@ -12,8 +12,12 @@
 namespace attn {
 
 // ---------------------------------------------------------------- status word
-// Bit 0 of status[0]: a bounded wait ran out.  status[1]: site code of the
-// first wait that ran out (for diagnosis).
+// The status word is four ints of device memory, 8-byte aligned:
+//   status[0]  bit 0: a bounded wait ran out;
+//   status[1]  site code of the first wait that ran out (for diagnosis);
+//   status[2..3]  address of a host-visible flag (mapped, page-locked host memory), written
+//              once per device when the library sets the device up; a wait that runs out
+//              also sets that flag, so the host learns of it without synchronising.
 enum : int { kStatusTimeout = 1 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -60,7 +64,7 @@ constexpr uint32_t kWaitLimitPolls = 1u << 28;
 
 struct WaitCtx {
     volatile int *abort_flag;  // shared memory, one per CTA; null for drain waits
-    int *status;               // device status word (global)
+    int *status;               // device status word (global, four ints; see above)
 };
 
 // A wait with a null abort flag (used to drain copies in flight while unwinding)
@@ -78,6 +82,12 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t pa
     }
     if (w.abort_flag) *w.abort_flag = 1;
     if (atomicOr(&w.status[0], kStatusTimeout) == 0) atomicExch(&w.status[1], site);
+    // the host-visible copy: a plain store (no atomics on host memory), then a system fence
+    volatile int *host_flag = *reinterpret_cast<int *const volatile *>(w.status + 2);
+    if (host_flag) {
+        *host_flag = kStatusTimeout;
+        __threadfence_system();
+    }
     return false;
 }
 

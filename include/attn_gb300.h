@@ -47,9 +47,19 @@
  *     the host.  The kernels clamp lengths to [0, capacity] and treat a page id
  *     outside [0, num_pages) as an empty page (its keys are skipped), so bad
  *     values give wrong numbers, never out-of-bounds accesses.
- *   - Every wait inside a kernel is bounded.  A wait that runs out sets a
- *     device status word (ATTN_ERR_DEVICE_TIMEOUT) and the kernel exits
- *     cleanly; attn_check_device_status() reports and clears it.
+ *   - Every wait inside a kernel is bounded.  A wait that runs out records
+ *     ATTN_ERR_DEVICE_TIMEOUT in a device status word and in a host-visible flag
+ *     of that device, and the kernel exits cleanly.  The flag is reported without
+ *     synchronising: once it is set, every later call that would launch work on
+ *     that device returns ATTN_ERR_DEVICE_TIMEOUT and launches nothing, and
+ *     attn_last_device_status() returns it, until attn_check_device_status()
+ *     clears it.  (A kernel still running when a call is made has not reported
+ *     yet; attn_check_device_status() synchronises first.)
+ *   - The first call on each device does a one-time set-up with that device
+ *     current: a check of the architecture, the lookup of the status word, the
+ *     page-locking of the library's static page of host flags (once per process)
+ *     and one small synchronous copy into the status word.  Make that first call
+ *     before any stream capture.
  *   - Supported: head dim d in {32, 64, 80, 96, 128} for the prefill entry
  *     points (forward, paged prefill, KV append), {64, 128} for decode and the
  *     backward; page_size 16.
@@ -116,10 +126,29 @@ int attn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *ls
  * Bytes of device workspace paged_attn_decode needs for these sizes (0 on
  * invalid sizes).  The caller allocates it (16-byte aligned) and may reuse it
  * across calls on the same stream; calls that overlap on the GPU need
- * separate workspaces.
+ * separate workspaces.  The size depends on the page table's capacity,
+ * max_pages_per_seq * page_size tokens, because the split grid covers every
+ * position the table can address.
  */
 size_t paged_attn_decode_workspace_size(int B, int H, int d, int max_pages_per_seq,
                                         int page_size);
+
+/*
+ * The same size stated by the longest context: max_ctx_len tokens in 16-token
+ * pages, i.e. paged_attn_decode_workspace_size(B, H, d, ceil(max_ctx_len / 16),
+ * 16).  Pass the capacity of the table the decode will get (max_pages_per_seq *
+ * 16), which is at least the longest context.
+ */
+size_t paged_attn_decode_workspace_size_ctx(int B, int H, int d, int max_ctx_len);
+
+/*
+ * Workspace of paged_attn_decode_gqa and paged_attn_decode_fp8 for H query heads
+ * over Hkv cache heads.  Groups of two or more query heads run longer splits
+ * (1024 tokens instead of 512) and need about half the multi-head size; the
+ * multi-head size is always enough.
+ */
+size_t paged_attn_decode_gqa_workspace_size(int B, int H, int Hkv, int d, int max_pages_per_seq,
+                                            int page_size);
 
 /*
  * Paged-KV decode: one query per sequence over its cached tokens.
@@ -145,8 +174,9 @@ int paged_attn_decode(const void *q, const void *k_pages, const void *v_pages,
  * (k_pages, v_pages [num_pages, Hkv, page_size, d]) shared by the H query heads
  * (q, o [B, H, d]; lse [B, H]); query head h reads cache head h / (H / Hkv), and
  * each cache page is read once for all the query heads that share it.  H % Hkv
- * must be 0.  The workspace is sized by paged_attn_decode_workspace_size(B, H,
- * ...) with H the number of query heads.  Other arguments as paged_attn_decode.
+ * must be 0.  The workspace is sized by paged_attn_decode_gqa_workspace_size(B,
+ * H, Hkv, ...) with H the number of query heads.  Other arguments as
+ * paged_attn_decode.
  */
 int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_pages,
                           const int32_t *page_table, const int32_t *ctx_lens, int page_size,
@@ -268,8 +298,12 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
  * The first call on each device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  All calls
  * share the one array: calls that may overlap on the GPU (other streams, other
- * host threads) race on it and must be ordered by the caller.  Each call writes
- * every part of the array it later reads, so leftover contents do no harm.
+ * host threads) race on it and must be ordered by the caller.  A call that
+ * completes normally writes every part of the array it later reads, so what an
+ * earlier call left there does not reach its result.  A call whose bounded wait
+ * runs out (ATTN_ERR_DEVICE_TIMEOUT) is different: the split that gave up does
+ * not write its partial, and the merge may then read an earlier call's partial
+ * from the array, so that call's O and LSE are invalid (as the status says).
  */
 int paged_attn_decode_noalloc(const void *q, const void *k_pages, const void *v_pages,
                               const int32_t *page_table, const int32_t *ctx_lens, int page_size,
@@ -277,11 +311,24 @@ int paged_attn_decode_noalloc(const void *q, const void *k_pages, const void *v_
                               int num_pages, float scale, attn_stream_t stream);
 
 /*
- * Synchronises `stream`, then returns and clears the device status word:
- * ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since
- * the last check, or ATTN_ERR_CUDA if the synchronisation itself failed.
+ * Synchronises `stream`, then returns and clears the current device's status
+ * (the device word and the host-visible flag): ATTN_OK,
+ * ATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since the last
+ * check, or ATTN_ERR_CUDA if the synchronisation itself failed.  After it the
+ * other entry points launch work again.
  */
 int attn_check_device_status(attn_stream_t stream);
+
+/*
+ * The current device's host-visible timeout flag, read without synchronising
+ * and without clearing it: ATTN_ERR_DEVICE_TIMEOUT if a kernel that has already
+ * reached its timeout path recorded one since the last attn_check_device_status(),
+ * else ATTN_OK.  The same condition makes the launching entry points return
+ * ATTN_ERR_DEVICE_TIMEOUT.  (The op sequence of the Kernel-Inference-Engine
+ * README reads the error state right after a launch, with no host round trip;
+ * this is that check for the asynchronous in-kernel timeouts.)
+ */
+int attn_last_device_status(void);
 
 /*
  * Self-test of the failure detection: launches one block whose only thread waits

@@ -61,6 +61,36 @@ def test_workspace_size(lib):
     assert ws(1, 1, 64, 1, 32) == 0
 
 
+def test_workspace_size_by_context_length(lib):
+    ws, ws_ctx = lib.paged_attn_decode_workspace_size, lib.paged_attn_decode_workspace_size_ctx
+    # the longest context in 16-token pages: 8192 tokens = 512 pages; 8193 needs a 513th page
+    assert ws_ctx(32, 32, 128, 8192) == ws(32, 32, 128, 512, 16)
+    assert ws_ctx(32, 32, 128, 8193) == ws(32, 32, 128, 513, 16)
+    assert ws_ctx(2, 3, 64, 1) == ws(2, 3, 64, 1, 16)
+    assert ws_ctx(1, 1, 64, 0) == 0
+    assert ws_ctx(1, 1, 64, -16) == 0
+
+
+def test_grouped_query_workspace_size(lib):
+    ws, ws_g = lib.paged_attn_decode_workspace_size, lib.paged_attn_decode_gqa_workspace_size
+    # groups of an even number of query heads use 1024-token splits: 8 of them over 8192 tokens
+    assert ws_g(32, 32, 8, 128, 512, 16) == 32 * 32 * 8 * (128 + 4) * 4
+    assert ws_g(32, 32, 8, 128, 512, 16) * 2 == ws(32, 32, 128, 512, 16)
+    assert ws_g(4, 6, 2, 64, 3, 16) == 4 * 6 * 1 * (64 + 4) * 4  # 48 tokens: one split
+    # odd groups and multi-head attention keep the 512-token splits
+    assert ws_g(2, 9, 3, 64, 100, 16) == ws(2, 9, 64, 100, 16)
+    assert ws_g(2, 8, 8, 128, 100, 16) == ws(2, 8, 128, 100, 16)
+    assert ws_g(2, 8, 3, 128, 100, 16) == 0  # 8 % 3 != 0
+    assert ws_g(2, 8, 0, 128, 100, 16) == 0
+
+
+def test_last_device_status_without_synchronising(lib):
+    # no device here: the set-up fails and says so; on a GPU machine a clean device reads ATTN_OK
+    import torch
+    st = lib.attn_last_device_status()
+    assert st == (0 if torch.cuda.is_available() else 5)
+
+
 ALIGNED = 1 << 20  # fake, 16-byte aligned addresses: the checks below fail before any use
 
 

@@ -36,6 +36,17 @@ def _both(binding, shape, ctx):
     assert torch.equal(torch.isneginf(lse), inf)
     if (~inf).any():
         assert (lse[~inf] - lse_ref[~inf]).abs().max().item() <= LSE_MAX
+    # and on its own against the fp64 oracle, within the same tolerances
+    from oracle import oracle
+    o64, lse64 = oracle.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                     shape.scale)
+    err64 = np.abs(o.float().cpu().numpy() - o64)
+    assert err64.max() <= O_MAX and err64.mean() <= O_MEAN
+    lse_c = lse.cpu().numpy()
+    fin = np.isfinite(lse64)
+    assert np.array_equal(np.isneginf(lse_c), np.isneginf(lse64))
+    if fin.any():
+        assert np.abs(lse_c[fin] - lse64[fin]).max() <= LSE_MAX
 
 
 @pytest.mark.gpu
