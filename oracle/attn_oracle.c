@@ -180,12 +180,19 @@ int oracle_attn_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return err;
 }
 
+/* Page ids outside [0, num_pages).  The pages describe the page table as an operating
+ * system's page table over the KV cache (inference-kernel-cookbook README, recipe 03) and are
+ * silent on an entry that maps no page.  With skip_bad_pages = 0 such an entry is an error
+ * (return 1).  With skip_bad_pages = 1 it is read as an unmapped page that holds no tokens: the
+ * positions it covers are left out of J (their keys get no weight and their values add
+ * nothing), the other positions keep their places, so causal masks are unchanged. */
+
 /* Paged decode, grouped-query form: q [B,Hq,d]; k_pages/v_pages [num_pages,Hkv,page_size,d];
  * query head h reads key/value head h / (Hq / Hkv).  o [B,Hq,d], lse [B,Hq]. */
 int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                                 const int32_t *page_table, const int32_t *ctx_lens, int page_size,
                                 int B, int Hq, int Hkv, int d, int max_pages, int num_pages, double scale,
-                                double *o, double *lse, int nthreads) {
+                                double *o, double *lse, int nthreads, int skip_bad_pages) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 || max_pages <= 0 ||
         num_pages <= 0)
         return 1;
@@ -221,7 +228,14 @@ int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, cons
                 int bad = 0;
                 for (int t = 0; t < n; ++t) {
                     int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
-                    if (pg < 0 || pg >= num_pages) { bad = 1; break; }
+                    valid[t] = 1;
+                    if (pg < 0 || pg >= num_pages) {
+                        if (!skip_bad_pages) { bad = 1; break; }
+                        valid[t] = 0;  /* an unmapped page: no token here */
+                        memset(kc + (size_t)t * d, 0, sizeof(uint16_t) * (size_t)d);
+                        memset(vc + (size_t)t * d, 0, sizeof(uint16_t) * (size_t)d);
+                        continue;
+                    }
                     size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
                     memcpy(kc + (size_t)t * d, k_pages + src, sizeof(uint16_t) * (size_t)d);
                     memcpy(vc + (size_t)t * d, v_pages + src, sizeof(uint16_t) * (size_t)d);
@@ -231,7 +245,6 @@ int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, cons
                     err = 1;
                     continue;
                 }
-                for (int t = 0; t < n; ++t) valid[t] = 1;
                 attend_row(q + (size_t)bh * d, kc, vc, valid, n, d, scale, srow,
                            o + (size_t)bh * d, lse + bh);
             }
@@ -254,7 +267,7 @@ int oracle_paged_decode_gqa_f64(const uint16_t *q, const uint16_t *k_pages, cons
 int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                                  const int32_t *page_table, const int32_t *ctx_lens, int page_size, int B,
                                  int Hq, int Hkv, int Nq, int d, int max_pages, int num_pages, int causal,
-                                 double scale, double *o, double *lse, int nthreads) {
+                                 double scale, double *o, double *lse, int nthreads, int skip_bad_pages) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || d <= 0 || page_size <= 0 ||
         max_pages <= 0 || num_pages <= 0)
         return 1;
@@ -272,7 +285,8 @@ int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, con
         uint16_t *vc = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)cap * d);
         double *srow = (double *)malloc(sizeof(double) * (size_t)cap);
         unsigned char *valid = (unsigned char *)malloc((size_t)cap);
-        if (!kc || !vc || !srow || !valid) {
+        unsigned char *mapped = (unsigned char *)malloc((size_t)cap);
+        if (!kc || !vc || !srow || !valid || !mapped) {
 #pragma omp atomic write
             err = 2;
         } else {
@@ -288,7 +302,14 @@ int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, con
                 int bad = 0;
                 for (int t = 0; t < n; ++t) {
                     int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
-                    if (pg < 0 || pg >= num_pages) { bad = 1; break; }
+                    mapped[t] = 1;
+                    if (pg < 0 || pg >= num_pages) {
+                        if (!skip_bad_pages) { bad = 1; break; }
+                        mapped[t] = 0;  /* an unmapped page: no token here */
+                        memset(kc + (size_t)t * d, 0, sizeof(uint16_t) * (size_t)d);
+                        memset(vc + (size_t)t * d, 0, sizeof(uint16_t) * (size_t)d);
+                        continue;
+                    }
                     size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
                     memcpy(kc + (size_t)t * d, k_pages + src, sizeof(uint16_t) * (size_t)d);
                     memcpy(vc + (size_t)t * d, v_pages + src, sizeof(uint16_t) * (size_t)d);
@@ -299,7 +320,8 @@ int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, con
                     continue;
                 }
                 for (int i = 0; i < Nq; ++i) {
-                    for (int j = 0; j < n; ++j) valid[j] = (unsigned char)key_valid(i, j, Nq, n, n, causal);
+                    for (int j = 0; j < n; ++j)
+                        valid[j] = (unsigned char)(mapped[j] && key_valid(i, j, Nq, n, n, causal));
                     size_t r = (size_t)bh * Nq + i;
                     attend_row(q + r * d, kc, vc, valid, n, d, scale, srow, o + r * d, lse + r);
                 }
@@ -309,6 +331,7 @@ int oracle_paged_prefill_gqa_f64(const uint16_t *q, const uint16_t *k_pages, con
         free(vc);
         free(srow);
         free(valid);
+        free(mapped);
     }
     return err;
 }
@@ -319,7 +342,7 @@ int oracle_paged_decode_f64(const uint16_t *q, const uint16_t *k_pages, const ui
                             int B, int H, int d, int max_pages, int num_pages, double scale,
                             double *o, double *lse, int nthreads) {
     return oracle_paged_decode_gqa_f64(q, k_pages, v_pages, page_table, ctx_lens, page_size, B, H, H, d,
-                                       max_pages, num_pages, scale, o, lse, nthreads);
+                                       max_pages, num_pages, scale, o, lse, nthreads, 0);
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -538,7 +561,7 @@ int oracle_paged_decode_fp8_gqa_f64(const uint16_t *q, const uint8_t *k_pages, c
                                     double k_scale, double v_scale, const int32_t *page_table,
                                     const int32_t *ctx_lens, int page_size, int B, int Hq, int Hkv, int d,
                                     int max_pages, int num_pages, double scale, double *o, double *lse,
-                                    int nthreads) {
+                                    int nthreads, int skip_bad_pages) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 || max_pages <= 0 ||
         num_pages <= 0)
         return 1;
@@ -568,25 +591,29 @@ int oracle_paged_decode_fp8_gqa_f64(const uint16_t *q, const uint8_t *k_pages, c
                     err = 1;
                     continue;
                 }
-                int bad = 0;
+                /* the decode query has no position-dependent mask, so the tokens of mapped pages
+                 * are gathered back to back (unmapped pages, when skipped, contribute none) */
+                int bad = 0, kept = 0;
                 for (int t = 0; t < n && !bad; ++t) {
                     const int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
                     if (pg < 0 || pg >= num_pages) {
+                        if (skip_bad_pages) continue;
                         bad = 1;
                         break;
                     }
                     const size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
                     for (int c = 0; c < d; ++c) {
-                        kc[(size_t)t * d + c] = oracle_e4m3_value(k_pages[src + c]) * k_scale;
-                        vc[(size_t)t * d + c] = oracle_e4m3_value(v_pages[src + c]) * v_scale;
+                        kc[(size_t)kept * d + c] = oracle_e4m3_value(k_pages[src + c]) * k_scale;
+                        vc[(size_t)kept * d + c] = oracle_e4m3_value(v_pages[src + c]) * v_scale;
                     }
+                    ++kept;
                 }
                 if (bad) {
 #pragma omp atomic write
                     err = 1;
                     continue;
                 }
-                attend_row_f64kv(q + (size_t)bh * d, kc, vc, n, d, scale, srow, o + (size_t)bh * d, lse + bh);
+                attend_row_f64kv(q + (size_t)bh * d, kc, vc, kept, d, scale, srow, o + (size_t)bh * d, lse + bh);
             }
         }
         free(kc);

@@ -75,9 +75,9 @@ def _load():
             lib.oracle_attn_gqa_rows_f64.argtypes = [P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
                                                      P, ctypes.c_int64, P, P, I]
             lib.oracle_paged_decode_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I,
-                                                        ctypes.c_double, P, P, I]
+                                                        ctypes.c_double, P, P, I, I]
             lib.oracle_paged_prefill_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I,
-                                                         ctypes.c_double, P, P, I]
+                                                         ctypes.c_double, P, P, I, I]
             lib.oracle_paged_prefill_gqa_f64.restype = ctypes.c_int
             lib.oracle_attn_bwd_gqa_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double,
                                                     P, P, P, P, P, P, I]
@@ -91,7 +91,7 @@ def _load():
             lib.oracle_e4m3_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_float, P]
             lib.oracle_e4m3_quantize.restype = ctypes.c_int
             lib.oracle_paged_decode_fp8_gqa_f64.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P, P, I, I,
-                                                            I, I, I, I, I, ctypes.c_double, P, P, I]
+                                                            I, I, I, I, I, ctypes.c_double, P, P, I, I]
             lib.oracle_paged_decode_fp8_gqa_f64.restype = ctypes.c_int
             lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
             lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
@@ -222,9 +222,11 @@ def attn_fwd_gqa(q, k, v, causal: bool, scale: float, kv_lens=None, nthreads: in
     return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
 
 
-def paged_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nthreads: int = 0):
+def paged_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nthreads: int = 0,
+                     skip_bad_pages: bool = False):
     """Grouped-query paged decode: q [B,Hq,d]; k_pages/v_pages [P,Hkv,page_size,d].
-    Returns (O [B,Hq,d], LSE [B,Hq]) in float64."""
+    A page id outside [0, P) is an error, or with ``skip_bad_pages`` an unmapped page whose
+    positions hold no token.  Returns (O [B,Hq,d], LSE [B,Hq]) in float64."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k_pages), bf16_bits(v_pages)
     B, Hq, d = qb.shape
     P, Hkv, ps, dk = kb.shape
@@ -236,15 +238,18 @@ def paged_decode_gqa(q, k_pages, v_pages, page_table, ctx_lens, scale: float, nt
     lse = np.empty((B, Hq), np.float64)
     err = _load().oracle_paged_decode_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(cl), ps, B, Hq,
                                               Hkv, d, pt.shape[1], P, float(scale), _ptr(o), _ptr(lse),
-                                              nthreads)
+                                              nthreads, int(bool(skip_bad_pages)))
     if err:
         raise RuntimeError(f"oracle_paged_decode_gqa_f64 failed ({err})")
     return o, lse
 
 
-def paged_prefill_gqa(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, scale: float, nthreads: int = 0):
+def paged_prefill_gqa(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, scale: float, nthreads: int = 0,
+                      skip_bad_pages: bool = False):
     """Chunked prefill over the paged cache: q [B,Hq,Nq,d] are the last Nq of the ctx_lens[b]
     cached tokens of sequence b (bottom-right causal); k_pages/v_pages [P,Hkv,page_size,d].
+    A page id outside [0, P) is an error, or with ``skip_bad_pages`` an unmapped page whose
+    positions hold no token (the other positions keep theirs).
     Returns (O [B,Hq,Nq,d], LSE [B,Hq,Nq]) in float64."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k_pages), bf16_bits(v_pages)
     B, Hq, Nq, d = qb.shape
@@ -257,7 +262,7 @@ def paged_prefill_gqa(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, s
     lse = np.empty((B, Hq, Nq), np.float64)
     err = _load().oracle_paged_prefill_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pt), _ptr(cl), ps, B, Hq, Hkv,
                                                Nq, d, pt.shape[1], P, int(bool(causal)), float(scale), _ptr(o),
-                                               _ptr(lse), nthreads)
+                                               _ptr(lse), nthreads, int(bool(skip_bad_pages)))
     if err:
         raise RuntimeError(f"oracle_paged_prefill_gqa_f64 failed ({err})")
     return o, lse
@@ -343,7 +348,7 @@ def _u8(x) -> np.ndarray:
 
 
 def paged_decode_fp8_gqa(q, k_codes, v_codes, k_scale: float, v_scale: float, page_table, ctx_lens, scale: float,
-                         nthreads: int = 0):
+                         nthreads: int = 0, skip_bad_pages: bool = False):
     """Paged decode over an e4m3 cache (codes uint8 [P,Hkv,page_size,d]; value = e4m3 * scale).
     Returns (O [B,Hq,d], LSE [B,Hq]) in float64."""
     qb = bf16_bits(q)
@@ -358,7 +363,7 @@ def paged_decode_fp8_gqa(q, k_codes, v_codes, k_scale: float, v_scale: float, pa
     lse = np.empty((B, Hq), np.float64)
     err = _load().oracle_paged_decode_fp8_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), float(k_scale), float(v_scale),
                                                   _ptr(pt), _ptr(cl), ps, B, Hq, Hkv, d, pt.shape[1], P, float(scale),
-                                                  _ptr(o), _ptr(lse), nthreads)
+                                                  _ptr(o), _ptr(lse), nthreads, int(bool(skip_bad_pages)))
     if err:
         raise RuntimeError(f"oracle_paged_decode_fp8_gqa_f64 failed ({err})")
     return o, lse

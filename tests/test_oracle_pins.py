@@ -274,6 +274,119 @@ def test_paged_rejects_bad_page_ids(oracle_mod):
         oracle_mod.paged_decode(inp["q"], inp["k_pages"], inp["v_pages"], pt, inp["ctx_lens"], 1.0)
 
 
+def _torch_masked_attention(q, kc, vc, mask, scale):
+    """fp64 attention of query rows q [n, d] over keys kc/vc [m, d] with a boolean mask [n, m],
+    written with torch primitives (softmax, logsumexp); rows with no key give 0 and -inf."""
+    s = (q.to(torch.float64) @ kc.to(torch.float64).T) * scale
+    s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    p = torch.softmax(s, dim=-1).nan_to_num(0.0)
+    return (p @ vc.to(torch.float64)).numpy(), lse.numpy()
+
+
+def _unmapped_case(shape_seed, ctx, bad):
+    """Decode-layout inputs whose page-table entries listed in ``bad`` ((b, logical page, id))
+    point outside the pool."""
+    shape = workloads.DecodeShape("t", len(ctx), 4, 32, (1, max(ctx)), seed=shape_seed)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=2)
+    for b, lp, pid in bad:
+        inp["page_table"][b, lp] = pid
+    return inp
+
+
+def _mapped_positions(inp, b, n, ps=16):
+    P = inp["k_pages"].shape[0]
+    ids = inp["page_table"][b].long()
+    return torch.tensor([0 <= int(ids[t // ps]) < P for t in range(n)], dtype=torch.bool)
+
+
+def _gather(pages, inp, b, n, kvh, ps=16):
+    """Contiguous [n, d] cache of key/value head kvh by torch indexing; unmapped pages -> 0."""
+    P = pages.shape[0]
+    ids = inp["page_table"][b].long()
+    rows = []
+    for t in range(n):
+        pid = int(ids[t // ps])
+        rows.append(pages[pid, kvh, t % ps] if 0 <= pid < P else torch.zeros_like(pages[0, 0, 0]))
+    return torch.stack(rows)
+
+
+def test_paged_decode_skips_unmapped_pages(oracle_mod):
+    # an id past the pool and a negative id inside the context, one at the very start; sequence 2
+    # has every page unmapped (no key at all: 0 and -inf)
+    ctx = [70, 33, 20]
+    inp = _unmapped_case(9, ctx, [(0, 1, 10_000), (0, 3, -1), (1, 0, -7), (2, 0, -1), (2, 1, 999_999)])
+    scale = 0.21
+    o, lse = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"],
+                                         inp["ctx_lens"], scale, skip_bad_pages=True)
+    with pytest.raises(RuntimeError):
+        oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                    scale)
+    for b, n in enumerate(ctx):
+        keep = _mapped_positions(inp, b, n)
+        for h in range(4):
+            kc = _gather(inp["k_pages"], inp, b, n, h // 2)
+            vc = _gather(inp["v_pages"], inp, b, n, h // 2)
+            ro, rl = _torch_masked_attention(inp["q"][b, h][None], kc, vc, keep[None], scale)
+            np.testing.assert_allclose(o[b, h], ro[0], rtol=0, atol=1e-12)
+            if np.isfinite(rl[0]):
+                np.testing.assert_allclose(lse[b, h], rl[0], rtol=0, atol=1e-12)
+            else:
+                assert lse[b, h] == -np.inf and not o[b, h].any()
+    assert lse[2].tolist() == [-np.inf] * 4
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill_skips_unmapped_pages(oracle_mod, causal):
+    ctx, Nq = [70, 40], 24
+    inp = _unmapped_case(10, ctx, [(0, 2, 55_555), (1, 0, -3)])
+    scale = 0.19
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(2, 4, Nq, 32, generator=g).to(torch.bfloat16)
+    o, lse = oracle_mod.paged_prefill_gqa(q, inp["k_pages"], inp["v_pages"], inp["page_table"], inp["ctx_lens"],
+                                          causal, scale, skip_bad_pages=True)
+    for b, n in enumerate(ctx):
+        keep = _mapped_positions(inp, b, n)
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(n)[None, :]
+        mask = keep[None, :].expand(Nq, n)
+        if causal:
+            mask = mask & (j <= i + n - Nq)  # bottom-right: query i sits at position n - Nq + i
+        for h in range(4):
+            kc = _gather(inp["k_pages"], inp, b, n, h // 2)
+            vc = _gather(inp["v_pages"], inp, b, n, h // 2)
+            ro, rl = _torch_masked_attention(q[b, h], kc, vc, mask, scale)
+            np.testing.assert_allclose(o[b, h], ro, rtol=0, atol=1e-12)
+            fin = np.isfinite(rl)
+            np.testing.assert_allclose(lse[b, h][fin], rl[fin], rtol=0, atol=1e-12)
+            assert np.all(lse[b, h][~fin] == -np.inf) and not o[b, h][~fin].any()
+    if causal:
+        # sequence 1's first page (positions 0-15) is unmapped; its query 0 sits at position 16
+        # and still sees the mapped key 16
+        assert np.isfinite(lse[1, :, 0]).all()
+
+
+def test_paged_decode_fp8_skips_unmapped_pages(oracle_mod):
+    ctx = [50, 17]
+    inp = _unmapped_case(12, ctx, [(0, 1, 1 << 20), (1, 1, -2)])
+    kc8 = oracle_mod.e4m3_quantize(inp["k_pages"], 0.5)
+    vc8 = oracle_mod.e4m3_quantize(inp["v_pages"], 0.25)
+    vals = torch.from_numpy(oracle_mod.e4m3_values())
+    scale = 0.3
+    o, lse = oracle_mod.paged_decode_fp8_gqa(inp["q"], kc8, vc8, 0.5, 0.25, inp["page_table"], inp["ctx_lens"], scale,
+                                             skip_bad_pages=True)
+    kd = vals[torch.from_numpy(kc8).long()] * 0.5
+    vd = vals[torch.from_numpy(vc8).long()] * 0.25
+    for b, n in enumerate(ctx):
+        keep = _mapped_positions(inp, b, n)
+        for h in range(4):
+            kc = _gather(kd, inp, b, n, h // 2)
+            vc = _gather(vd, inp, b, n, h // 2)
+            ro, rl = _torch_masked_attention(inp["q"][b, h][None], kc, vc, keep[None], scale)
+            np.testing.assert_allclose(o[b, h], ro[0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b, h], rl[0], rtol=0, atol=1e-12)
+
+
 # ----------------------------------------------------------------------------- accounting
 
 def test_flop_formula_reproduces_printed_numbers():
