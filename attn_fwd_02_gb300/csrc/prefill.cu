@@ -174,8 +174,8 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
     // paged mode: pool row (page * Hkv + head) of each page of a tile; pages past the
-    // sequence's last page, or with an id outside the pool, get an out-of-range row, which
-    // TMA reads as zeros
+    // sequence's last page, or with an id outside the pool (an unmapped page, whose keys the
+    // softmax masks), get an out-of-range row, which TMA reads as zeros
     constexpr int kTilePages = kBN / kPageTokens;
     const int kvh = bh_kv % p.Hkv;
     const int pages_used = p.paged ? (kv_end_of(p, b) + kPageTokens - 1) / kPageTokens : 0;
@@ -387,6 +387,18 @@ __device__ __forceinline__ void mask_chunks(uint32_t (&s)[2][32], int nvalid) {
             if (cc * 32 + i >= nvalid) s[cc][i] = __float_as_uint(-INFINITY);
 }
 
+// Paged mode: scores of keys whose page is unmapped (bit pg of `bad` set: keys 16 pg .. 16 pg + 15
+// of the tile) become -inf, as a padded key would.
+__device__ __forceinline__ void mask_pages(uint32_t (&s)[2][2][32], uint32_t bad) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if ((bad >> (h * 4 + cc * 2 + (i >> 4))) & 1u) s[h][cc][i] = __float_as_uint(-INFINITY);
+}
+
 // Max of 64 scores: eight independent three-input chains, then a tree.
 __device__ __forceinline__ float max64(const uint32_t (&s)[2][32]) {
     float m[8];
@@ -441,7 +453,25 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by l and O
     float l = 0.f;
     bool ok = true;
+    // Paged mode: a page id outside the pool is an unmapped page that holds no token (the producer
+    // loads zeros there; its keys are masked here).  Lanes 0-7 of each warp read the 8 table entries
+    // of a tile themselves, one tile ahead of its use, and a ballot turns them into a warp-uniform
+    // mask of unmapped pages.
+    const int lane = threadIdx.x & 31;
+    const int pages_used = p.paged ? (kv_end + kPageTokens - 1) / kPageTokens : 0;
+    const int32_t *table = p.paged ? p.page_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
+    auto table_entry = [&](int tile) {
+        const int lp = tile * (kBN / kPageTokens) + lane;
+        return (lane < kBN / kPageTokens && lp < pages_used) ? table[lp] : 0;
+    };
+    int next_id = p.paged ? table_entry(0) : 0;
     for (int j = 0; j < n_tiles; ++j) {
+        uint32_t unmapped = 0;
+        if (p.paged) {
+            const int id = next_id;
+            if (j + 1 < n_tiles) next_id = table_entry(j + 1);
+            unmapped = __ballot_sync(0xffffffffu, id < 0 || id >= p.num_pages);
+        }
         // every decision that guards a .sync.aligned tcgen05 instruction is warp-uniform
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], (uint32_t)(j & 1), wc, 20 + t))) {
             ok = false;
@@ -479,6 +509,7 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             mask_chunks(s[0], nvalid);
             mask_chunks(s[1], nvalid - 64);
         }
+        if (unmapped) mask_pages(s, unmapped);
         const float mx = fmaxf(max64(s[0]), max64(s[1]));
         const float m_cand = mx * c;  // -inf stays -inf (c > 0)
         const bool resc = m_cand > m_ref + kRescaleThreshold;

@@ -11,7 +11,11 @@ data anyway).
 Output: one JSON line.  `value` is the prefill rate in TFLOP/s (FLOPs =
 4*B*H*N^2*d / 2 for causal) summed over ranks; the `decode` object carries the
 paged-decode rate in GB/s of algorithmic HBM traffic.  Each carries a roofline
-against the measured peaks of this GPU type.
+against the measured peaks of this GPU type.  The default run adds `configs`:
+one sub-line for each of the three small prefill workloads (a single 128x64
+tile, a BERT-large-like encoder with key padding, a GPT-2-small-like causal
+decoder), timed on their own after the main region with L2 flushed between
+steps, each with its roofline and the oracle timed on the whole workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
@@ -633,11 +637,74 @@ def gpu_arm(args):
         out["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pre, dec, args.cpu_seconds)
+    if args.workload == "default" and not args.no_configs:
+        out["configs"] = small_prefill_lines(args, torch, A, rank, world, peaks, peak_kind)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+SMALL_PREFILL = (workloads.TILE_128x64, workloads.ENCODER_PAD, workloads.DECODER_CAUSAL)
+
+
+def oracle_whole_prefill(shape, min_seconds=0.3):
+    """The oracle on the whole prefill workload, repeated until at least min_seconds have passed.
+    Returns (seconds per call, calls)."""
+    from oracle import oracle
+    inp = workloads.prefill_inputs(shape)
+    calls, t_all = 0, 0.0
+    while t_all < min_seconds or calls == 0:
+        t = time.perf_counter()
+        oracle.attn_fwd(inp["q"], inp["k"], inp["v"], shape.causal, shape.scale, kv_lens=inp["kv_lens"])
+        t_all += time.perf_counter() - t
+        calls += 1
+    return t_all / calls, calls
+
+
+def small_prefill_lines(args, torch, A, rank, world, peaks, peak_kind):
+    """Sub-lines of the default run for the three small prefill workloads (the single 128x64 tile,
+    the BERT-large-like encoder with key padding, the GPT-2-small-like causal decoder): each timed
+    on its own after the main region, L2 flushed between steps, as CUDA-graph replays of the call
+    (the host's per-call issue time exceeds the device time of the smallest ones), with its
+    roofline and the oracle timed on the whole workload on the host cores."""
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    cases = [PrefillCase(shape, torch, A) for shape in SMALL_PREFILL]
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+        sampler.mark(True)
+    timed = []
+    for case in cases:
+        _, part_ms = time_parts(torch, [case], args.steps, args.warmup, world, None, graphs=True)
+        timed.append(part_ms[0])
+    if sampler:
+        sampler.mark(False)
+    clocks = sampler.stop() if sampler else None
+    if A.attn_check_device_status() != 0:
+        raise RuntimeError("device status set after the small-workload timing")
+    lines = []
+    for case, ms in zip(cases, timed):
+        s = case.shape
+        line = {"workload": s.name, "value": round(job_rate(case.flops, world, ms, 1e12), 3), "unit": "TFLOP/s",
+                "ms_per_call": round(ms, 5), "flops_per_call": case.flops, "flops_nominal": case.flops_nominal,
+                "bytes_per_call": case.bytes,
+                "l2": "L2 flushed between steps (512 MiB write, outside the per-call events)",
+                "launch": "CUDA graph replay per call (captured through the API)", "steps": args.steps,
+                "roofline": roofline_prefill(case, ms, peaks, peak_kind),
+                "prefill": {"B": s.B, "H": s.H, "Nq": s.Nq, "Nkv": s.Nkv, "d": s.d, "causal": s.causal,
+                            "scale": s.scale, "kv_len_range": s.kv_len_range}}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            from oracle import oracle
+            sec, calls = oracle_whole_prefill(s)
+            line["cpu_baseline"] = {"kind": "oracle", "cores": oracle.num_threads(),
+                                    "value": round(case.flops / sec / 1e12, 6), "unit": "TFLOP/s",
+                                    "sample": f"the whole workload, {calls} call(s) of fp64 C (OpenMP), "
+                                              f"{sec * 1e3:.1f} ms per call"}
+        lines.append(line)
+    return {"lines": lines, "clocks": clocks,
+            "gpu_launches": len(cases) * args.steps}
 
 
 def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
@@ -821,6 +888,8 @@ def main():
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default run: skip the sub-lines of the three small prefill workloads")
     ap.add_argument("--graphs", action="store_true", help="time CUDA graph replays of each call instead of direct calls")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps, always

@@ -45,8 +45,9 @@
  *     and the outputs are untouched.
  *   - Device-resident lengths (kv_lens, ctx_lens, page_table) are not read on
  *     the host.  The kernels clamp lengths to [0, capacity] and treat a page id
- *     outside [0, num_pages) as an empty page (its keys are skipped), so bad
- *     values give wrong numbers, never out-of-bounds accesses.
+ *     outside [0, num_pages) as an unmapped page that holds no token (its keys
+ *     are skipped, on every paged entry point alike), so bad values give wrong
+ *     numbers, never out-of-bounds accesses.
  *   - Every wait inside a kernel is bounded.  A wait that runs out records
  *     ATTN_ERR_DEVICE_TIMEOUT in a device status word and in a host-visible flag
  *     of that device, and the kernel exits cleanly.  The flag is reported without
@@ -196,8 +197,10 @@ int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_page
  *   q, o [B, H, Nq, d] bf16; lse [B, H, Nq] fp32 (may be NULL)
  *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16; page_table [B, max_pages_per_seq]
  *   H % Hkv == 0 (grouped-query heads as attn_fwd_gqa); page_size 16; d in {64, 128}.
- * Page ids outside [0, num_pages) read as zero keys/values (their scores still count
- * for positions < ctx_lens[b]).  Runs on the same tcgen05 pipeline as attn_fwd, with
+ * A page id outside [0, num_pages) is an unmapped page, as in decode: the positions
+ * it covers hold no token (their keys are masked out; the other positions keep their
+ * places, so the causal alignment is unchanged), and a query that sees no mapped key
+ * gets O = 0 and LSE = -inf.  Runs on the same tcgen05 pipeline as attn_fwd, with
  * each 128-key tile gathered page by page through TMA.
  */
 int paged_attn_prefill(const void *q, const void *k_pages, const void *v_pages,

@@ -103,3 +103,62 @@ def test_append_then_paged_prefill_matches_contiguous(lib):
         torch.cuda.synchronize()
         assert (oc[0].float() - o[b].float()).abs().max().item() <= 1e-2
         assert (lc[0] - lse[b]).abs().max().item() <= 1e-3
+
+
+def _check(o, lse, o_ref, lse_ref):
+    og = o.float().cpu().numpy().astype(np.float64)
+    err = np.abs(og - o_ref)
+    assert np.isfinite(og).all() and err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    lg = lse.cpu().numpy().astype(np.float64)
+    inf = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lg), inf)
+    if (~inf).any():
+        assert np.abs(lg[~inf] - lse_ref[~inf]).max() <= LSE_MAX
+    assert not og[inf].any()  # rows without a key are exactly zero
+
+
+def test_unmapped_pages_mean_the_same_on_every_paged_entry_point(lib, oracle_mod):
+    """A page id outside the pool is an unmapped page holding no token, on the chunked prefill
+    and on every decode entry point alike; compared with the oracle's reading of it."""
+    B, H, Hkv, d = 3, 8, 2, 128
+    ctx = [1000, 300, 40]
+    shape = workloads.DecodeShape("unmapped", B, H, d, (1, max(ctx)), seed=97)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
+    pt = inp["page_table"]
+    pt[0, 3] = 1 << 24          # past the pool, inside a 128-key tile
+    pt[0, 40] = -1              # negative, in a later tile
+    pt[0, 8:16] = -5            # one whole 128-key tile unmapped
+    pt[1, 0] = inp["k_pages"].shape[0]  # the first id past the end
+    pt[2, :3] = -1              # every page of sequence 2: no key at all
+    dv = {k: v.cuda() for k, v in inp.items()}
+    for Nq, causal in ((64, True), (200, False), (1, True)):
+        q = rand_bf16((B, H, Nq, d), 98 + Nq)
+        o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, H, Nq), float("nan"), device="cuda")
+        lib.paged_attn_prefill(q.cuda(), dv["k_pages"], dv["v_pages"], dv["page_table"], dv["ctx_lens"], causal,
+                               shape.scale, out=o, lse=lse)
+        torch.cuda.synchronize()
+        assert lib.attn_check_device_status() == 0
+        o_ref, lse_ref = oracle_mod.paged_prefill_gqa(q, inp["k_pages"], inp["v_pages"], pt, inp["ctx_lens"], causal,
+                                                      shape.scale, skip_bad_pages=True)
+        _check(o, lse, o_ref, lse_ref)
+    # decode over the same table: grouped-query, multi-head (the same heads repeated) and e4m3
+    o_ref, lse_ref = oracle_mod.paged_decode_gqa(inp["q"], inp["k_pages"], inp["v_pages"], pt, inp["ctx_lens"],
+                                                 shape.scale, skip_bad_pages=True)
+    o, lse = lib.paged_attn_decode_gqa(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["ctx_lens"],
+                                       shape.scale)
+    torch.cuda.synchronize()
+    _check(o, lse, o_ref, lse_ref)
+    kmh = dv["k_pages"].repeat_interleave(H // Hkv, dim=1).contiguous()
+    vmh = dv["v_pages"].repeat_interleave(H // Hkv, dim=1).contiguous()
+    o, lse = lib.paged_attn_decode(dv["q"], kmh, vmh, dv["page_table"], dv["ctx_lens"], shape.scale)
+    torch.cuda.synchronize()
+    _check(o, lse, o_ref, lse_ref)
+    kc = lib.kv_quantize_fp8(dv["k_pages"], 0.25)
+    vc = lib.kv_quantize_fp8(dv["v_pages"], 0.25)
+    o, lse = lib.paged_attn_decode_fp8(dv["q"], kc, vc, 0.25, 0.25, dv["page_table"], dv["ctx_lens"], shape.scale)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_decode_fp8_gqa(inp["q"], kc.cpu(), vc.cpu(), 0.25, 0.25, pt, inp["ctx_lens"],
+                                                     shape.scale, skip_bad_pages=True)
+    _check(o, lse, o_ref, lse_ref)

@@ -183,6 +183,16 @@ def test_prefill_long_context_sampled_rows(lib, oracle_mod):
     assert o.abs().max().item() <= inp["v"].abs().max().item() + 1e-2
 
 
+def test_prefill_long_context_all_rows(lib, oracle_mod):
+    # every row of the long-context workload (2 x 32 x 8192 rows of d = 128) against the fp64
+    # oracle, element by element: about 1.1e12 oracle FLOPs, half a minute on 16 host cores
+    shape = workloads.LONG_CAUSAL
+    inp, kl, o, lse = run_prefill(lib, shape)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inp["q"], inp["k"], inp["v"], True, shape.scale)
+    max_err, mean_err = compare(o, lse, o_ref, lse_ref, shape.name + " (all rows)")
+    assert np.isfinite(lse_ref).all()
+
+
 # ----------------------------------------------------------------------------- paged decode
 
 def run_decode(lib, shape, ctx_lens=None):
