@@ -293,8 +293,8 @@ ATTN_API size_t paged_attn_decode_gqa_workspace_size(int B, int H, int Hkv, int 
 
 namespace {
 bool finite_positive(float x) { return x > 0.f && x < 3.0e38f; }
-// Head dims of the decode kernels.
-bool decode_head_dim(int d) { return d == 64 || d == 128; }
+// Head dims of the decode kernels: the same five as the prefill.
+bool decode_head_dim(int d) { return prefill_head_dim(d); }
 
 // Checks shared by every decode entry point: everything but the caller's workspace.
 int decode_arg_checks(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
@@ -367,7 +367,7 @@ ATTN_API int paged_kv_append_fp8(const void *k_new, const void *v_new, void *k_p
     if (B <= 0 || Hkv <= 0 || Nnew <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0)
         return ATTN_ERR_INVALID_ARG;
     if (!finite_positive(k_scale) || !finite_positive(v_scale)) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!prefill_head_dim(d)) return ATTN_ERR_UNSUPPORTED;
     if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
     if ((uint64_t)max_pages_per_seq * 16 > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))

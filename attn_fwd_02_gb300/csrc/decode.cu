@@ -64,11 +64,19 @@ __host__ __device__ constexpr int decode_chunk_tokens(int H, int Hkv) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// 64-column boxes of a page block in the grouped-query kernel's swizzled layout (the columns past
+// D of the last box are read as zeros by TMA and never used by the products).
+template <int D> constexpr int kBoxes = (D + 63) / 64;
+// Bytes of one ring buffer (one page block of K or V): the bulk-copied block (kPS rows of D
+// elements), or kBoxes swizzled 16 x 64 boxes for the grouped-query kernel's bf16 TMA loads.
+template <int D, int GP, bool FP8>
+constexpr int kSlotBytes = (!FP8 && GP > 1) ? kBoxes<D> * kPS * 128 : kPS * D * (FP8 ? 1 : 2);
+
 template <int D, int GP, bool FP8>
 struct DecodeSmem {
-    // [warp][slot][0 = K, 1 = V][kPS * D] elements (bf16, or e4m3 bytes); 16-byte aligned blocks
-    // (1024-byte alignment for the swizzled TMA boxes of the grouped-query mma kernel)
-    alignas((!FP8 && GP > 1) ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kPS * D * (FP8 ? 1 : 2)];
+    // [warp][slot][0 = K, 1 = V][one page block]; 16-byte aligned blocks (1024-byte alignment for
+    // the swizzled TMA boxes of the grouped-query mma kernel)
+    alignas((!FP8 && GP > 1) ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kSlotBytes<D, GP, FP8>];
     uint64_t full[kWarps][kSlotsFor<FP8, GP>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
@@ -97,6 +105,25 @@ __device__ __forceinline__ float warp_sum_pairs(float x) {
     return x;
 }
 
+// How the 32 lanes of a warp share the D dims of a row in the multi-head kernel.
+//   D = 32, 64, 128: lane l holds DPL = D / 32 consecutive dims from l * DPL (one 2-, 4- or 8-byte
+//                    load of bf16);
+//   D = 80, 96:      lane l holds the pair 2l, 2l + 1 and, if 64 + l < D, dim 64 + l (DPL = 3: a
+//                    4-byte and a 2-byte load); the single slot of lanes 16-31 at D = 80 holds no
+//                    dim and stays zero.
+template <int D>
+struct LaneDims {
+    static constexpr bool kSplit = (D % 32 != 0) || (D / 32 == 3);
+    static constexpr int DPL = kSplit ? 3 : D / 32;
+    static_assert(kSplit ? (D > 64 && D <= 96) : (D == 32 || D == 64 || D == 128), "head dim");
+    __device__ static __forceinline__ int dim(int lane, int i) {
+        return kSplit ? (i < 2 ? 2 * lane + i : 64 + lane) : lane * DPL + i;
+    }
+    __device__ static __forceinline__ bool has(int lane, int i) { return dim(lane, i) < D; }
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t lo16) { return __uint_as_float(lo16 << 16); }
+
 // Load DPL consecutive bf16 from shared memory as fp32.
 template <int DPL>
 __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL]) {
@@ -106,10 +133,12 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL
         f[1] = __uint_as_float(u.x & 0xffff0000u);
         f[2] = __uint_as_float(u.y << 16);
         f[3] = __uint_as_float(u.y & 0xffff0000u);
-    } else {
+    } else if constexpr (DPL == 2) {
         uint32_t u = *reinterpret_cast<const uint32_t *>(p);
         f[0] = __uint_as_float(u << 16);
         f[1] = __uint_as_float(u & 0xffff0000u);
+    } else {
+        f[0] = bf16_bits_to_float(*reinterpret_cast<const uint16_t *>(p));
     }
 }
 
@@ -129,37 +158,43 @@ __device__ __forceinline__ void load_e4m3(const uint8_t *p, float (&f)[DPL]) {
         f[1] = a.y;
         f[2] = b.x;
         f[3] = b.y;
-    } else {
+    } else if constexpr (DPL == 2) {
         const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t *>(p));
         f[0] = a.x;
         f[1] = a.y;
-    }
-}
-
-// DPL consecutive cache elements of one row (bf16 or e4m3) as fp32.
-template <int DPL, bool FP8>
-__device__ __forceinline__ void load_kv(const uint8_t *row, int lane, float (&f)[DPL]) {
-    if constexpr (FP8) load_e4m3<DPL>(row + lane * DPL, f);
-    else load_bf16<DPL>(reinterpret_cast<const __nv_bfloat16 *>(row) + lane * DPL, f);
-}
-
-// Loads DPL consecutive bf16 of global memory (the query) as fp32 scaled by c.
-template <int DPL>
-__device__ __forceinline__ void load_q(const __nv_bfloat16 *qp, float c, float (&qf)[DPL]) {
-    float t[DPL];
-    if constexpr (DPL == 4) {
-        uint2 u = *reinterpret_cast<const uint2 *>(qp);
-        t[0] = __uint_as_float(u.x << 16);
-        t[1] = __uint_as_float(u.x & 0xffff0000u);
-        t[2] = __uint_as_float(u.y << 16);
-        t[3] = __uint_as_float(u.y & 0xffff0000u);
     } else {
-        uint32_t u = *reinterpret_cast<const uint32_t *>(qp);
-        t[0] = __uint_as_float(u << 16);
-        t[1] = __uint_as_float(u & 0xffff0000u);
+        f[0] = e4m3x2_to_float2(*p).x;
     }
+}
+
+// This lane's dims of one cache row (bf16 or e4m3) as fp32, laid out as LaneDims<D>.
+template <int D, bool FP8>
+__device__ __forceinline__ void load_kv(const uint8_t *row, int lane, float (&f)[LaneDims<D>::DPL]) {
+    using LD = LaneDims<D>;
+    if constexpr (LD::kSplit) {
+        float pr[2], one[1] = {0.f};
+        if constexpr (FP8) {
+            load_e4m3<2>(row + 2 * lane, pr);
+            if (lane < D - 64) load_e4m3<1>(row + 64 + lane, one);
+        } else {
+            load_bf16<2>(reinterpret_cast<const __nv_bfloat16 *>(row) + 2 * lane, pr);
+            if (lane < D - 64) load_bf16<1>(reinterpret_cast<const __nv_bfloat16 *>(row) + 64 + lane, one);
+        }
+        f[0] = pr[0];
+        f[1] = pr[1];
+        f[2] = one[0];
+    } else {
+        if constexpr (FP8) load_e4m3<LD::DPL>(row + lane * LD::DPL, f);
+        else load_bf16<LD::DPL>(reinterpret_cast<const __nv_bfloat16 *>(row) + lane * LD::DPL, f);
+    }
+}
+
+// This lane's dims of the query row (bf16 in global memory) as fp32 scaled by c.
+template <int D>
+__device__ __forceinline__ void load_q(const __nv_bfloat16 *qrow, int lane, float c, float (&qf)[LaneDims<D>::DPL]) {
+    load_kv<D, false>(reinterpret_cast<const uint8_t *>(qrow), lane, qf);
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) qf[i] = t[i] * c;
+    for (int i = 0; i < LaneDims<D>::DPL; ++i) qf[i] *= c;
 }
 
 // Sum of part[t] over the 32 lanes for the 16 tokens t, as a reduce-scatter: afterwards lane
@@ -211,7 +246,8 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
 template <int D, int GP, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits, int Hkv,
                                                                    int gsplit) {
-    constexpr int DPL = D / 32;  // head dims per lane
+    using LD = LaneDims<D>;
+    constexpr int DPL = LD::DPL;  // head dims per lane
     constexpr int kElem = FP8 ? 1 : 2;
     constexpr uint32_t kRowBytes = D * kElem;
     constexpr uint32_t kBlockBytes = kPS * kRowBytes;
@@ -272,8 +308,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     float qf[GP][DPL];
 #pragma unroll
     for (int g = 0; g < GP; ++g)
-        load_q<DPL>(reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * a.H + qh0 + g) * D + lane * DPL, c,
-                    qf[g]);
+        load_q<D>(reinterpret_cast<const __nv_bfloat16 *>(a.q) + ((size_t)b * a.H + qh0 + g) * D, lane, c, qf[g]);
 
     float m_run[GP], l_run[GP], o[GP][DPL];
 #pragma unroll
@@ -301,7 +336,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             // this lane's DPL dims of the 16 keys, read once and used for every query head
             float kf[16][DPL];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) load_kv<DPL, FP8>(Ks + t * kRowBytes, lane, kf[t]);
+            for (int t = 0; t < 16; ++t) load_kv<D, FP8>(Ks + t * kRowBytes, lane, kf[t]);
             float p[GP];  // lane L: probability of token L >> 1, per query head
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
@@ -325,7 +360,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             }
             for (int t = 0; t < ntok; ++t) {
                 float vf[DPL];
-                load_kv<DPL, FP8>(Vs + t * kRowBytes, lane, vf);
+                load_kv<D, FP8>(Vs + t * kRowBytes, lane, vf);
 #pragma unroll
                 for (int g = 0; g < GP; ++g) {
                     const float pt = __shfl_sync(0xffffffffu, p[g], 2 * t);
@@ -360,7 +395,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             sm.red_l[warp][g] = l_run[g];
         }
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) sm.red_o[warp][g][lane * DPL + i] = o[g][i];
+        for (int i = 0; i < DPL; ++i)
+            if (LD::has(lane, i)) sm.red_o[warp][g][LD::dim(lane, i)] = o[g][i];
     }
     __syncthreads();
     if (sm.abort_flag) return;
@@ -434,7 +470,8 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
 template <int D, int GP, bool FP8>
 struct GqaMmaSmem {
     DecodeSmem<D, GP, FP8> s;
-    alignas(128) __nv_bfloat16 stage[FP8 ? kWarps : 1][2][FP8 ? kPS * D : 8];  // bf16 K, V of one page
+    // bf16 K, V of one page in the swizzled box layout (kBoxes<D> boxes of 16 x 64)
+    alignas(128) __nv_bfloat16 stage[FP8 ? kWarps : 1][2][FP8 ? kBoxes<D> * kPS * 64 : 8];
 };
 
 // 16 e4m3 codes (one 16-byte chunk of a page row) -> 16 bf16 values, two 16-byte chunks.
@@ -457,10 +494,13 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                                                                      const DecodeArgs a, int max_splits, int Hkv,
                                                                      int gsplit) {
     static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
+    static_assert(D % 16 == 0, "k-steps of 16");
     constexpr int kSl = kSlotsFor<FP8, GP>;
-    constexpr uint32_t kBlockBytes = kPS * D * (FP8 ? 1 : 2);
+    constexpr uint32_t kBlockBytes = kPS * D * (FP8 ? 1 : 2);   // bytes of a page block in HBM
+    constexpr uint32_t kBoxBytesAll = kBoxes<D> * kPS * 128;     // a block's TMA boxes (zero-filled past D)
     constexpr int KS = D / 16;  // k-steps of S = Q K^T
-    constexpr int NT = D / 8;   // n-tiles of O += P V
+    constexpr int NT = D / 8;   // n-tiles of O += P V (even: n-tiles go in pairs)
+    static_assert(NT % 2 == 0, "pairs of n-tiles");
     constexpr float kThresh = 8.0f;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // the swizzled boxes need 1024-byte alignment
@@ -506,13 +546,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             uint64_t *bar = &sm.full[warp][k % kSl];
             if (ok) {
                 const int row = pid * Hkv + kvh;  // page block in the pool viewed as [num_pages * Hkv, 16, D]
-                mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
                 if constexpr (FP8) {
+                    mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
                     bulk_load(sm.kv[warp][k % kSl][0], kbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
                     bulk_load(sm.kv[warp][k % kSl][1], vbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
                 } else {
+                    mbar_arrive_expect_tx(bar, 2 * kBoxBytesAll);
 #pragma unroll
-                    for (int i = 0; i < D / 64; ++i) {
+                    for (int i = 0; i < kBoxes<D>; ++i) {
                         tma_load_3d(sm.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
                         tma_load_3d(sm.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
                     }
@@ -591,7 +632,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             } else if (ntok < kPS) {
                 // slots past the context end: zero their V rows (every box) so P = 0 meets finite values
                 const int per_box = (kPS - ntok) * 8;  // 16-byte chunks of the dead rows of one box
-                for (int i = lane; i < per_box * (D / 64); i += 32) {
+                for (int i = lane; i < per_box * kBoxes<D>; i += 32) {
                     const int box = i / per_box, j = i % per_box;
                     *reinterpret_cast<uint4 *>(sm.kv[warp][slot][1] + box * (16 * 128) + ntok * 128 + j * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
@@ -731,6 +772,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
 // kCombineWeights splits from shared memory).  A walk with two dependent global loads per
 // split took about 9.5 us per call at 16 splits.
 constexpr int kCombineWeights = 256;
+// One thread per O column, in whole warps (D = 80 has 16 threads without a column).
+template <int D> constexpr int kCombineThreads = (D + 31) / 32 * 32;
 template <int D>
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
 #pragma unroll
@@ -744,13 +787,15 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) 
     __syncthreads();
     float r = red[0];
 #pragma unroll
-    for (int w = 1; w < D / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    for (int w = 1; w < kCombineThreads<D> / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
     return r;
 }
 
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, int max_splits, int chunk) {
-    __shared__ float red[D / 32];
+__global__ void __launch_bounds__(kCombineThreads<D>) decode_combine_kernel(const DecodeArgs a, int max_splits,
+                                                                             int chunk) {
+    constexpr int kT = kCombineThreads<D>;
+    __shared__ float red[kT / 32];
     __shared__ float wgt[kCombineWeights];
     griddep_wait();  // the split kernel's partials are complete and visible
     const int h = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
@@ -760,17 +805,18 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeArgs a, i
     const size_t stride = (size_t)ws_stride<D>();
     const float *ws = reinterpret_cast<const float *>(a.workspace) + ((size_t)b * a.H + h) * max_splits * stride;
     float m = -INFINITY;
-    for (int s = dd; s < nsplit; s += D) m = fmaxf(m, ws[(size_t)s * stride + D]);
+    for (int s = dd; s < nsplit; s += kT) m = fmaxf(m, ws[(size_t)s * stride + D]);
     const float M = block_reduce<D>(m, true, red);
     float lsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = dd; s < nsplit; s += D) {
+        for (int s = dd; s < nsplit; s += kT) {
             const float w = ex2_approx(ws[(size_t)s * stride + D] - M);
             if (s < kCombineWeights) wgt[s] = w;
             lsum += ws[(size_t)s * stride + D + 1] * w;
         }
     }
     const float L = block_reduce<D>(lsum, false, red);  // its barriers also publish wgt[]
+    if (dd >= D) return;  // no O column (after the block's last barrier)
     float O = 0.f;
     if (M != -INFINITY) {
 #pragma unroll 8
@@ -843,7 +889,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.H, a.B);
-    cfg.blockDim = dim3(D);
+    cfg.blockDim = dim3(kCombineThreads<D>);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -860,7 +906,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
 
 size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int max_pages, int page_size) {
     if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || max_pages <= 0 || page_size != kPS ||
-        (d != 64 && d != 128))
+        (d != 32 && d != 64 && d != 80 && d != 96 && d != 128))
         return 0;
     const size_t chunk = (size_t)decode_chunk_tokens(H, Hkv);
     const size_t max_splits = ((size_t)max_pages * kPS + chunk - 1) / chunk;
@@ -868,8 +914,14 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int max_pages, int p
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.d == 128) return launch_decode_d<128>(a, stream);
-    return launch_decode_d<64>(a, stream);
+    switch (a.d) {
+        case 32: return launch_decode_d<32>(a, stream);
+        case 64: return launch_decode_d<64>(a, stream);
+        case 80: return launch_decode_d<80>(a, stream);
+        case 96: return launch_decode_d<96>(a, stream);
+        case 128: return launch_decode_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace attn

@@ -92,6 +92,11 @@ PAGED_PREFILL = DecodeShape("chunked prefill B8 Hq32 Hkv8 d128 Nq1024 ctx U[1024
 PAGED_PREFILL_KV_HEADS = 8
 PAGED_PREFILL_NQ = 1024
 
+# The paged decode at the other head dims the Kernel-Inference-Engine README instantiates (same
+# seed, so the same context lengths and page table as the d = 128 workload).
+PAGED_DECODE_BY_DIM = {d: DecodeShape(f"paged decode B32 H32 d{d} ctx U[512,8192] page16", 32, 32, d, (512, 8192), 16,
+                                      seed=1005) for d in (32, 64, 80, 96)}
+
 # A quarter-size paged decode (same lengths distribution) for multi-pass profiler captures.
 PAGED_DECODE_SMALL = DecodeShape("paged decode B8 H32 d128 ctx U[512,8192] page16",
                                  8, 32, 128, (512, 8192), 16, seed=1006)

@@ -547,8 +547,13 @@ def gpu_arm(args):
         pre = PrefillCase(workloads.LONG_CAUSAL, torch, A)
         dec = DecodeCase(workloads.PAGED_DECODE, torch, A)
         parts = [pre, dec]
-    elif args.workload in ("decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8"):
-        if args.workload == "decode_gqa":
+    elif args.workload in ("decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8") or \
+            args.workload.startswith("decode_d"):
+        if args.workload.startswith("decode_d"):  # decode_d32, decode_d80_fp8, ...
+            d = int(args.workload[len("decode_d"):].split("_")[0])
+            shape = workloads.PAGED_DECODE_BY_DIM[d]
+            dec = DecodeFp8Case(shape, torch, A) if args.workload.endswith("_fp8") else DecodeCase(shape, torch, A)
+        elif args.workload == "decode_gqa":
             dec = DecodeCase(workloads.PAGED_DECODE_GQA, torch, A, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
         elif args.workload == "decode_fp8":
             dec = DecodeFp8Case(workloads.PAGED_DECODE, torch, A)
@@ -884,6 +889,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8",
+                                           *[f"decode_d{d}{s}" for d in (32, 64, 80, 96) for s in ("", "_fp8")],
                                            "prefill_paged", "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")

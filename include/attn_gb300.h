@@ -61,9 +61,8 @@
  *     page-locking of the library's static page of host flags (once per process)
  *     and one small synchronous copy into the status word.  Make that first call
  *     before any stream capture.
- *   - Supported: head dim d in {32, 64, 80, 96, 128} for the prefill entry
- *     points (forward, paged prefill, KV append), {64, 128} for decode and the
- *     backward; page_size 16.
+ *   - Supported: head dim d in {32, 64, 80, 96, 128} for the prefill, decode
+ *     and KV-cache entry points, {64, 128} for the backward; page_size 16.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -196,7 +195,7 @@ int paged_attn_decode_gqa(const void *q, const void *k_pages, const void *v_page
  * (paged_kv_append).
  *   q, o [B, H, Nq, d] bf16; lse [B, H, Nq] fp32 (may be NULL)
  *   k_pages, v_pages [num_pages, Hkv, page_size, d] bf16; page_table [B, max_pages_per_seq]
- *   H % Hkv == 0 (grouped-query heads as attn_fwd_gqa); page_size 16; d in {64, 128}.
+ *   H % Hkv == 0 (grouped-query heads as attn_fwd_gqa); page_size 16; d in {32, 64, 80, 96, 128}.
  * A page id outside [0, num_pages) is an unmapped page, as in decode: the positions
  * it covers hold no token (their keys are masked out; the other positions keep their
  * places, so the causal alignment is unchanged), and a query that sees no mapped key
@@ -240,7 +239,7 @@ int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v
  * kv_quantize_fp8: n contiguous bf16 elements of src -> n codes in dst (n a
  *   multiple of 8; both 16-byte aligned).  Converts a whole bf16 page pool.
  * paged_kv_append_fp8: paged_kv_append into an e4m3 cache, converting each new
- *   element with the tensor's scale (d in {64, 128}).
+ *   element with the tensor's scale.
  */
 int paged_attn_decode_fp8(const void *q, const void *k_pages, const void *v_pages, float k_scale,
                           float v_scale, const int32_t *page_table, const int32_t *ctx_lens,

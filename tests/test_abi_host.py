@@ -57,7 +57,9 @@ def test_workspace_size(lib):
     assert ws(32, 32, 128, 512, 16) == 32 * 32 * 16 * (128 + 4) * 4
     assert ws(1, 1, 64, 1, 16) == 1 * 1 * 1 * (64 + 4) * 4
     assert ws(0, 1, 64, 1, 16) == 0
-    assert ws(1, 1, 96, 1, 16) == 0
+    assert ws(1, 1, 96, 1, 16) == 1 * 1 * 1 * (96 + 4) * 4
+    assert ws(3, 2, 80, 33, 16) == 3 * 2 * 2 * (80 + 4) * 4  # 528 tokens: two 512-token splits
+    assert ws(1, 1, 48, 1, 16) == 0  # not a supported head dim
     assert ws(1, 1, 64, 1, 32) == 0
 
 
@@ -153,7 +155,7 @@ def test_fp8_argument_checks(lib):
     assert dec(q=None) == 1
     assert dec(ks=0.0) == 1 and dec(vs=float("inf")) == 1 and dec(ks=float("nan")) == 1
     assert dec(Hkv=3) == 1
-    assert dec(d=80) == 2
+    assert dec(d=48) == 2 and dec(d=160) == 2
     assert dec(q=ALIGNED + 4) == 3
     assert dec(ws=None) == 4
     assert lib.kv_quantize_fp8(None, ALIGNED, 64, 1.0, None) == 1
@@ -163,7 +165,7 @@ def test_fp8_argument_checks(lib):
     app = lambda **kw: lib.paged_kv_append_fp8(ALIGNED, ALIGNED, ALIGNED, ALIGNED, kw.get("ks", 1.0), 1.0,
                                                kw.get("pt", ALIGNED), ALIGNED, 16, 1, 1, 4, kw.get("d", 64), 4, 8,
                                                None)
-    assert app(pt=None) == 1 and app(ks=0.0) == 1 and app(d=96) == 2
+    assert app(pt=None) == 1 and app(ks=0.0) == 1 and app(d=48) == 2 and app(d=256) == 2
 
 
 def call_dec(lib, q=ALIGNED, kp=ALIGNED, vp=ALIGNED, pt=ALIGNED, cl=ALIGNED, ps=16, o=ALIGNED, lse=None,
@@ -177,7 +179,8 @@ def test_decode_argument_checks(lib):
     assert call_dec(lib, B=0) == 1
     assert call_dec(lib, npages=0) == 1
     assert call_dec(lib, scale=0.0) == 1
-    assert call_dec(lib, d=80) == 2
+    assert call_dec(lib, d=48) == 2
+    assert call_dec(lib, d=256) == 2
     assert call_dec(lib, ps=32) == 2
     assert call_dec(lib, kp=ALIGNED + 4) == 3
     assert call_dec(lib, pt=ALIGNED + 2) == 3
@@ -230,7 +233,7 @@ def test_grouped_query_argument_checks(lib):
         kw.get("ws", ALIGNED), 1 << 20, None)
     assert dec(Hkv=3) == 1
     assert dec(Hkv=-1) == 1
-    assert dec(d=96) == 2
+    assert dec(d=112) == 2
     assert dec(ws=None) == 4
 
 
