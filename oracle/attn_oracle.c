@@ -530,6 +530,37 @@ int oracle_e4m3_quantize(const uint16_t *x, int64_t n, float inv_scale, uint8_t 
     return 0;
 }
 
+/* One query row against n_keys fp64 keys/values with a validity mask (valid[j] != 0 marks the
+ * keys in J): the three passes of attend_row, in the same order. */
+static void attend_row_f64kv_masked(const uint16_t *qrow, const double *kb, const double *vb,
+                                    const unsigned char *valid, int n_keys, int d, double scale, double *srow,
+                                    double *out, double *lse_out) {
+    double m = -INFINITY;
+    int any = 0;
+    for (int j = 0; j < n_keys; ++j) {
+        if (!valid[j]) continue;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_to_f64(qrow[c]) * kb[(size_t)j * d + c];
+        srow[j] = scale * dot;
+        if (!any || srow[j] > m) m = srow[j];
+        any = 1;
+    }
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    if (!any) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int j = 0; j < n_keys; ++j)
+        if (valid[j]) l += exp(srow[j] - m);
+    for (int j = 0; j < n_keys; ++j) {
+        if (!valid[j]) continue;
+        double p = exp(srow[j] - m) / l;
+        for (int c = 0; c < d; ++c) out[c] += p * vb[(size_t)j * d + c];
+    }
+    *lse_out = m + log(l);
+}
+
 /* One query row against n_keys fp64 keys/values (all valid): the three passes of attend_row. */
 static void attend_row_f64kv(const uint16_t *qrow, const double *kb, const double *vb, int n_keys, int d,
                              double scale, double *srow, double *out, double *lse_out) {
@@ -619,6 +650,85 @@ int oracle_paged_decode_fp8_gqa_f64(const uint16_t *q, const uint8_t *k_pages, c
         free(kc);
         free(vc);
         free(srow);
+    }
+    return err;
+}
+
+/* Chunked prefill over an e4m3 cache: oracle_paged_prefill_gqa_f64 with k_pages/v_pages holding
+ * e4m3 codes [num_pages, Hkv, page_size, d]; each cached value is e4m3(code) * k_scale (keys) or
+ * * v_scale (values), dequantised exactly in fp64, after which the plain definition is applied
+ * per query row exactly as in the bf16 form (same masks, same order of operations).  Page ids
+ * outside [0, num_pages) follow skip_bad_pages as in the bf16 form. */
+int oracle_paged_prefill_fp8_gqa_f64(const uint16_t *q, const uint8_t *k_pages, const uint8_t *v_pages,
+                                     double k_scale, double v_scale, const int32_t *page_table,
+                                     const int32_t *ctx_lens, int page_size, int B, int Hq, int Hkv, int Nq,
+                                     int d, int max_pages, int num_pages, int causal, double scale, double *o,
+                                     double *lse, int nthreads, int skip_bad_pages) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || d <= 0 || page_size <= 0 ||
+        max_pages <= 0 || num_pages <= 0)
+        return 1;
+    const int group = Hq / Hkv;
+    const int cap = max_pages * page_size;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double *kc = (double *)malloc(sizeof(double) * (size_t)cap * d);
+        double *vc = (double *)malloc(sizeof(double) * (size_t)cap * d);
+        double *srow = (double *)malloc(sizeof(double) * (size_t)cap);
+        unsigned char *valid = (unsigned char *)malloc((size_t)cap);
+        unsigned char *mapped = (unsigned char *)malloc((size_t)cap);
+        if (!kc || !vc || !srow || !valid || !mapped) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+                const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+                const int n = ctx_lens[b];
+                if (n < 0 || n > cap) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                int bad = 0;
+                for (int t = 0; t < n; ++t) {
+                    const int32_t pg = page_table[(size_t)b * max_pages + t / page_size];
+                    mapped[t] = 1;
+                    if (pg < 0 || pg >= num_pages) {
+                        if (!skip_bad_pages) { bad = 1; break; }
+                        mapped[t] = 0;  /* an unmapped page: no token here */
+                        for (int c = 0; c < d; ++c) kc[(size_t)t * d + c] = vc[(size_t)t * d + c] = 0.0;
+                        continue;
+                    }
+                    const size_t src = (((size_t)pg * Hkv + h / group) * page_size + (size_t)(t % page_size)) * d;
+                    for (int c = 0; c < d; ++c) {
+                        kc[(size_t)t * d + c] = oracle_e4m3_value(k_pages[src + c]) * k_scale;
+                        vc[(size_t)t * d + c] = oracle_e4m3_value(v_pages[src + c]) * v_scale;
+                    }
+                }
+                if (bad) {
+#pragma omp atomic write
+                    err = 1;
+                    continue;
+                }
+                for (int i = 0; i < Nq; ++i) {
+                    for (int j = 0; j < n; ++j)
+                        valid[j] = (unsigned char)(mapped[j] && key_valid(i, j, Nq, n, n, causal));
+                    const size_t r = (size_t)bh * Nq + i;
+                    attend_row_f64kv_masked(q + r * d, kc, vc, valid, n, d, scale, srow, o + r * d, lse + r);
+                }
+            }
+        }
+        free(kc);
+        free(vc);
+        free(srow);
+        free(valid);
+        free(mapped);
     }
     return err;
 }

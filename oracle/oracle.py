@@ -93,6 +93,9 @@ def _load():
             lib.oracle_paged_decode_fp8_gqa_f64.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P, P, I, I,
                                                             I, I, I, I, I, ctypes.c_double, P, P, I, I]
             lib.oracle_paged_decode_fp8_gqa_f64.restype = ctypes.c_int
+            lib.oracle_paged_prefill_fp8_gqa_f64.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P, P, I,
+                                                             I, I, I, I, I, I, I, I, ctypes.c_double, P, P, I, I]
+            lib.oracle_paged_prefill_fp8_gqa_f64.restype = ctypes.c_int
             lib.oracle_attn_gqa_rows_f64.restype = ctypes.c_int
             lib.oracle_paged_decode_gqa_f64.restype = ctypes.c_int
             for f in (lib.oracle_attn_rows_f64, lib.oracle_attn_fwd_f64,
@@ -366,4 +369,28 @@ def paged_decode_fp8_gqa(q, k_codes, v_codes, k_scale: float, v_scale: float, pa
                                                   _ptr(o), _ptr(lse), nthreads, int(bool(skip_bad_pages)))
     if err:
         raise RuntimeError(f"oracle_paged_decode_fp8_gqa_f64 failed ({err})")
+    return o, lse
+
+
+def paged_prefill_fp8_gqa(q, k_codes, v_codes, k_scale: float, v_scale: float, page_table, ctx_lens, causal: bool,
+                          scale: float, nthreads: int = 0, skip_bad_pages: bool = False):
+    """Chunked prefill over an e4m3 cache (codes uint8 [P,Hkv,page_size,d]; value = e4m3 * scale):
+    q [B,Hq,Nq,d] bf16 are the last Nq of the ctx_lens[b] cached tokens (bottom-right causal).
+    Returns (O [B,Hq,Nq,d], LSE [B,Hq,Nq]) in float64."""
+    qb = bf16_bits(q)
+    kb, vb = _u8(k_codes), _u8(v_codes)
+    B, Hq, Nq, d = qb.shape
+    P, Hkv, ps, dk = kb.shape
+    if dk != d or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    pt = _i32(page_table)
+    cl = _i32(ctx_lens)
+    o = np.empty((B, Hq, Nq, d), np.float64)
+    lse = np.empty((B, Hq, Nq), np.float64)
+    err = _load().oracle_paged_prefill_fp8_gqa_f64(_ptr(qb), _ptr(kb), _ptr(vb), float(k_scale), float(v_scale),
+                                                   _ptr(pt), _ptr(cl), ps, B, Hq, Hkv, Nq, d, pt.shape[1], P,
+                                                   int(bool(causal)), float(scale), _ptr(o), _ptr(lse), nthreads,
+                                                   int(bool(skip_bad_pages)))
+    if err:
+        raise RuntimeError(f"oracle_paged_prefill_fp8_gqa_f64 failed ({err})")
     return o, lse

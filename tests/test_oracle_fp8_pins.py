@@ -121,6 +121,72 @@ def test_fp8_scales_fold_into_score_scale_and_output(oracle_mod):
     np.testing.assert_allclose(l2, l1, atol=1e-12)
 
 
+def _fp8_prefill_case(seed=7, B=3, H=4, Hkv=2, d=32, ctx=(40, 150, 17), Nq=24):
+    shape = workloads.DecodeShape("fp8 prefill", B, H, d, (1, max(ctx)), seed=seed)
+    inp = workloads.decode_inputs(shape, ctx_lens=list(ctx), kv_heads=Hkv)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(B, H, Nq, d, generator=g).to(torch.bfloat16)
+    return shape, inp, q
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_fp8_paged_prefill_with_unit_scales_equals_bf16_paged_prefill(oracle_mod, causal):
+    # e4m3 values are bf16 values: the chunked prefill over codes at scale 1 is the bf16 chunked
+    # prefill of those values (same masks, same order of operations: equal to the last bit)
+    shape, inp, q = _fp8_prefill_case()
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], 0.5)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], 0.5)
+    table = oracle_mod.e4m3_values()
+    kb = torch.tensor(table[kc]).to(torch.bfloat16)
+    vb = torch.tensor(table[vc]).to(torch.bfloat16)
+    o8, l8 = oracle_mod.paged_prefill_fp8_gqa(q, kc, vc, 1.0, 1.0, inp["page_table"], inp["ctx_lens"], causal,
+                                              shape.scale)
+    ob, lb = oracle_mod.paged_prefill_gqa(q, kb, vb, inp["page_table"], inp["ctx_lens"], causal, shape.scale)
+    np.testing.assert_array_equal(o8, ob)
+    np.testing.assert_array_equal(l8, lb)
+
+
+def test_fp8_paged_prefill_scales_fold_into_score_scale_and_output(oracle_mod):
+    shape, inp, q = _fp8_prefill_case(seed=8)
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], 0.05)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], 0.05)
+    args = (inp["page_table"], inp["ctx_lens"], True)
+    o1, l1 = oracle_mod.paged_prefill_fp8_gqa(q, kc, vc, 1.0, 1.0, *args, shape.scale * 0.25)
+    o2, l2 = oracle_mod.paged_prefill_fp8_gqa(q, kc, vc, 0.25, 3.0, *args, shape.scale)
+    np.testing.assert_allclose(o2, 3.0 * o1, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, atol=1e-12)
+
+
+def test_fp8_paged_prefill_against_torch_fp64(oracle_mod):
+    # the definition over the dequantised cache, written with torch primitives and an explicit
+    # bottom-right causal mask (a library special case, independent of the oracle's gather)
+    shape, inp, q = _fp8_prefill_case(seed=9, d=64)
+    ks, vs = 0.04, 0.02
+    kc = oracle_mod.e4m3_quantize(inp["k_pages"], ks)
+    vc = oracle_mod.e4m3_quantize(inp["v_pages"], vs)
+    o, lse = oracle_mod.paged_prefill_fp8_gqa(q, kc, vc, ks, vs, inp["page_table"], inp["ctx_lens"], True,
+                                              shape.scale)
+    vals = torch.from_numpy(oracle_mod.e4m3_values())
+    kd = vals[torch.from_numpy(kc).long()] * ks
+    vd = vals[torch.from_numpy(vc).long()] * vs
+    Nq = q.shape[2]
+    for b, n in enumerate(inp["ctx_lens"].tolist()):
+        pages = inp["page_table"][b, :(n + 15) // 16].long()
+        for h in range(q.shape[1]):
+            kvh = h // 2
+            kk = kd[pages, kvh].reshape(-1, 64)[:n]
+            vv = vd[pages, kvh].reshape(-1, 64)[:n]
+            s_ = (q[b, h].to(torch.float64) @ kk.T) * shape.scale
+            mask = torch.arange(n)[None, :] <= torch.arange(Nq)[:, None] + n - Nq
+            s_ = s_.masked_fill(~mask, float("-inf"))
+            ref_l = torch.logsumexp(s_, -1)
+            ref_o = torch.softmax(s_, -1).nan_to_num(0.0) @ vv
+            fin = torch.isfinite(ref_l).numpy()
+            np.testing.assert_allclose(o[b, h], ref_o.numpy(), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b, h][fin], ref_l.numpy()[fin], rtol=0, atol=1e-12)
+            assert np.all(lse[b, h][~fin] == -np.inf)
+
+
 def test_planted_fp8_mistakes_are_caught(oracle_mod, tmp_path):
     """A plausible bug planted in a copy of the oracle C source must fail the pins above."""
     import ctypes
