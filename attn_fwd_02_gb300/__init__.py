@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     paged_attn_decode_gqa,
     paged_attn_decode_noalloc,
     paged_attn_prefill,
+    paged_attn_prefill_fp8,
     paged_kv_append,
     paged_kv_append_fp8,
     paged_attn_decode_gqa_workspace_size,

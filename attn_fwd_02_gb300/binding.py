@@ -41,6 +41,7 @@ SIGNATURES = {
     "attn_bwd_workspace_size": (Z, [I, I, I]),
     "paged_attn_decode_fp8": (I, [P, P, P, F, F, P, P, I, P, P, I, I, I, I, I, I, F, P, Z, P]),
     "kv_quantize_fp8": (I, [P, P, Z, F, P]),
+    "paged_attn_prefill_fp8": (I, [P, P, P, F, F, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P]),
     "paged_kv_append_fp8": (I, [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, P]),
     "attn_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, Z, P]),
     "attn_check_device_status": (I, [P]),
@@ -457,6 +458,35 @@ def paged_attn_prefill(q, k_pages, v_pages, page_table, ctx_lens, causal: bool, 
                                            page_table.shape[1], num_pages, int(bool(causal)), float(scale),
                                            _stream_ptr(stream))
     _check("paged_attn_prefill", st)
+    return out, lse
+
+
+def paged_attn_prefill_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float, page_table, ctx_lens,
+                           causal: bool, scale: float | None = None, out=None, lse=None, return_lse: bool = True,
+                           stream=None):
+    """paged_attn_prefill over an e4m3 cache: q [B,H,Nq,d] bf16; k_pages/v_pages uint8 codes
+    [P,Hkv,16,d] with per-tensor scales (value = e4m3(code) * scale).  Returns (o, lse)."""
+    import torch
+    _require(q, "q", torch.bfloat16, 4)
+    _require(k_pages, "k_pages", torch.uint8, 4)
+    _require(v_pages, "v_pages", torch.uint8, 4)
+    _require(page_table, "page_table", torch.int32, 2)
+    _require(ctx_lens, "ctx_lens", torch.int32, 1)
+    B, H, Nq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages must be [num_pages, Hkv, page_size, d] matching q")
+    if page_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages] and ctx_lens [B]")
+    if scale is None:
+        scale = d ** -0.5
+    out = _out_like(out, q, "out")
+    lse = _lse_out(lse, (B, H, Nq), q.device, return_lse)
+    st = load_library().paged_attn_prefill_fp8(_dptr(q), _dptr(k_pages), _dptr(v_pages), float(k_scale),
+                                               float(v_scale), _dptr(page_table), _dptr(ctx_lens), page_size,
+                                               _dptr(out), _dptr(lse), B, H, Hkv, Nq, d, page_table.shape[1],
+                                               num_pages, int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check("paged_attn_prefill_fp8", st)
     return out, lse
 
 

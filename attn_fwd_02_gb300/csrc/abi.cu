@@ -257,6 +257,37 @@ ATTN_API int paged_attn_prefill(const void *q, const void *k_pages, const void *
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+ATTN_API int paged_attn_prefill_fp8(const void *q, const void *k_pages, const void *v_pages, float k_scale,
+                                    float v_scale, const int32_t *page_table, const int32_t *ctx_lens, int page_size,
+                                    void *o, float *lse, int B, int H, int Hkv, int Nq, int d, int max_pages_per_seq,
+                                    int num_pages, int causal, float scale, attn_stream_t stream) {
+    if (!page_table || !ctx_lens || !k_pages || !v_pages) return ATTN_ERR_INVALID_ARG;
+    if (page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(k_scale < 3.0e38f) || !(v_scale > 0.f) || !(v_scale < 3.0e38f))
+        return ATTN_ERR_INVALID_ARG;
+    if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if ((uint64_t)max_pages_per_seq * 16 > (1ull << 30)) return ATTN_ERR_INVALID_ARG;
+    if (Hkv <= 0 || (uint64_t)num_pages * (uint64_t)Hkv > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;
+    const int cap = max_pages_per_seq * 16;
+    int st = prefill_checks(q, k_pages, v_pages, o, lse, B, H, Hkv, Nq, cap, d, causal, scale, nullptr);
+    if (st != ATTN_OK) return st;
+    if (!aligned4(page_table) || !aligned4(ctx_lens)) return ATTN_ERR_MISALIGNED;
+    int *status = nullptr;
+    st = device_setup(&status);
+    if (st != ATTN_OK) return st;
+    attn::PrefillArgs a{q, k_pages, v_pages, o, lse, nullptr, status, B, H, Nq, cap, d, causal, scale, Hkv};
+    a.paged = 1;
+    a.page_table = page_table;
+    a.ctx_lens = ctx_lens;
+    a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    a.kv_fp8 = 1;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t e = attn::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 ATTN_API int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v_pages,
                              const int32_t *page_table, const int32_t *start_pos, int page_size, int B, int Hkv,
                              int Nnew, int d, int max_pages_per_seq, int num_pages, attn_stream_t stream) {

@@ -23,6 +23,9 @@ struct PrefillArgs {
     int paged = 0;
     const int32_t *page_table = nullptr, *ctx_lens = nullptr;
     int max_pages = 0, num_pages = 0;
+    // paged mode over an e4m3 cache: k, v hold codes; value = e4m3(code) * k_scale / v_scale
+    int kv_fp8 = 0;
+    float k_scale = 1.f, v_scale = 1.f;
 };
 
 struct DecodeArgs {

@@ -9,9 +9,9 @@
 // memory, and K/V tiles wholly above the causal diagonal (or past the
 // key-padding length) are never visited.
 //
-// GB300 mapping (d = 128; d = 64 uses one query tile per CTA and two CTAs per SM, see Cfg).
-// One CTA = one (batch, head) and 256 query rows held as two 128-row tiles Q0, Q1 that share
-// every K/V tile.  12 warps (three warpgroups):
+// GB300 mapping (d = 128; d <= 64 uses one query tile per CTA, 64-key tiles and four CTAs per SM,
+// see Cfg).  One CTA = one (batch, head) and 256 query rows held as two 128-row tiles Q0, Q1 that
+// share every K/V tile.  12 warps (three warpgroups):
 //   warps 0-3  softmax warpgroup 0 (rows of Q0), warps 4-7  softmax warpgroup 1
 //              (rows of Q1).  Thread r of a warpgroup owns query row r = TMEM
 //              lane r: it loads its 128 scores from TMEM, masks, takes the row
@@ -33,6 +33,8 @@
 // Every tcgen05 op of the MMA thread completes in issue order, so the commit
 // that signals S_t(j) also tells warpgroup t that PV_t(j-1) has finished with
 // O_t and with the P_t columns.
+#include <cuda_fp8.h>
+
 #include <cmath>
 
 #include "launch.h"
@@ -42,51 +44,57 @@ namespace attn {
 namespace {
 
 constexpr int kBM = 128;  // query rows per tile
-constexpr int kBN = 128;  // keys per tile
 // Head dims 32, 64, 80, 96 and 128 (the set the Kernel-Inference-Engine README instantiates its
 // attention kernel for).  Tiles are laid out at a padded width kPad<D> (64 up to d = 64, else
 // 128) in 64-column boxes; TMA fills the columns past d with zeros, the S product runs over d/16
 // k-steps and the PV product has N = d, so the padding costs shared memory but no tensor work.
 template <int D> constexpr int kPad = D <= 64 ? 64 : 128;
 // Shape of the CTA per padded head dimension.
-//   128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 12 warps with a
-//        per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
-//   64:  one query tile per CTA, two CTAs per SM: at d = 64 a tile needs 256 TMEM
-//        columns (S 128 | O 64 | P 64) and 80 KB of shared memory, and two co-resident CTAs
-//        overlap each other's serial chains (Q load, first S, softmax, PV, epilogue), which
-//        dominate the short units of small problems.
-//        Two MMA-issuing threads (kMmaIssuers = 2): warp 5 issues the S products and warp 6 the PV
-//        products.  With P in its own columns the two touch disjoint TMEM, and S(j+1) no longer
-//        waits behind PV(j-1), which waits for the previous softmax.  8 warps, so that the second
-//        warpgroup (producer, two issuers, one idle warp) can hand registers to the softmax.
+//   128: two 128-row query tiles per CTA (ping-pong softmax warpgroups), 128-key tiles, 12 warps
+//        with a per-warpgroup register split, one CTA per SM (192 KB smem, all 512 TMEM columns).
+//   64:  one query tile per CTA and 64-key tiles, four CTAs per SM.  At d <= 64 the softmax (one
+//        exponential per 256 tensor FLOPs) bounds each step, and a CTA's chain per key tile (S,
+//        scores loaded, row max, exponentials, PV) is mostly latency; four CTAs give each SM
+//        sub-partition four softmax warps to interleave instead of two.  A CTA needs 128 TMEM
+//        columns (S 64 | O 64, P over S) and 48 KB of shared memory (Q 16 KB, a 2-slot ring of
+//        8 KB K and V tiles).  8 warps: softmax warpgroup, producer, MMA issuer, two idle warps
+//        whose registers go to the softmax warpgroup.
 // Register split (setmaxnreg) per warpgroup, within the block's launch pool (threads x
 // registers at launch):
 //   128: launched at 168 (384 x 168 = 64512): 128 x (64 + 216 + 216) = 63488.
-//   64:  launched at 128 (two CTAs of 256 per SM): 128 x (64 + 192) = 32768 = 256 x 128.
+//   64:  launched at 64 (four CTAs of 256 per SM): 128 x (32 + 96) = 16384 = 256 x 64.
 template <int P> struct CfgPad;
 template <int D> struct Cfg : CfgPad<kPad<D>> {};
 template <> struct CfgPad<128> {
-    static constexpr int QT = 2, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1, kMmaIssuers = 1;
+    static constexpr int QT = 2, BN = 128, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr bool kSplitRegs = true;
     static constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 64;
 };
 template <> struct CfgPad<64> {
-    static constexpr int QT = 1, kThreads = 256, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 2, kMmaIssuers = 2;
-    static constexpr uint32_t kTmemCols = 256;
+    static constexpr int QT = 1, BN = 64, kThreads = 256, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 4;
+    static constexpr uint32_t kTmemCols = 128;
     static constexpr bool kSplitRegs = true;
-    static constexpr uint32_t kRegsSoftmax = 192, kRegsOther = 64;
+    static constexpr uint32_t kRegsSoftmax = 96, kRegsOther = 32;
 };
 static_assert(128 * (Cfg<128>::kRegsOther + 2 * Cfg<128>::kRegsSoftmax) <= 384 * 168, "d=128 register split");
-static_assert(128 * (Cfg<64>::kRegsOther + Cfg<64>::kRegsSoftmax) <= 256 * 128, "d=64 register split");
-static_assert(Cfg<64>::QT * (128 + 64 + 64) <= (int)Cfg<64>::kTmemCols, "d=64 TMEM layout");
+static_assert(128 * (Cfg<64>::kRegsOther + Cfg<64>::kRegsSoftmax) <= 256 * 64, "d=64 register split");
+static_assert(Cfg<64>::QT * (Cfg<64>::BN + 64) <= (int)Cfg<64>::kTmemCols, "d=64 TMEM layout");
 static_assert(Cfg<128>::QT * (128 + 128) <= (int)Cfg<128>::kTmemCols, "d=128 TMEM layout");
+// keys per tile
+template <int D> constexpr int kBNd = Cfg<D>::BN;
 constexpr int kQTilesMax = 2;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box (16 KB)
+template <int D> constexpr uint32_t kKvBoxBytes = kBNd<D> * 64 * 2;  // one K or V box (kBNd rows)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kPageTokens = 16;            // tokens per page of the paged KV cache
+
+// Where K/V come from (a compile-time parameter of the kernel, so that each form carries only
+// its own code): contiguous [B, Hkv, Nkv, d] tensors; bf16 pages of a paged KV cache; or e4m3
+// pages, widened to bf16 in shared memory before the products.
+enum KvMode : int { kContig = 0, kPagedBf16 = 1, kPagedE4m3 = 2 };
 
 struct PrefillParams {
     __nv_bfloat16 *o;
@@ -99,9 +107,11 @@ struct PrefillParams {
     // [num_pages, Hkv, 16, d] found through page_table [B, max_pages]; sequence b holds
     // ctx_lens[b] tokens and the queries are its last Nq positions
     const int32_t *page_table, *ctx_lens;
-    int paged, max_pages, num_pages;
+    int max_pages, num_pages;
+    const uint8_t *k8, *v8;              // e4m3 pages [num_pages, Hkv, 16, d] (kPagedE4m3)
     int heads_per_chunk;                 // heads whose K/V share L2 at a time (see the CTA order)
-    float scale_log2;
+    float scale_log2;                    // scale * log2(e) (times the key scale of e4m3 pages)
+    float o_scale;                       // multiplies O in the epilogue (the value scale of e4m3 pages)
 };
 
 // K/V ring.  Step j of the MMA issuer (PV(j) then S(j+1)) needs V(j) and K(j+1) together,
@@ -111,20 +121,30 @@ struct PrefillParams {
 // one wait and one commit for the ring.
 constexpr int kStages = 2;
 
-template <int D>
+// e4m3 pages: one K tile and one V tile of codes, staged page block by page block (16 rows of d
+// bytes each) before the converter warps widen them into the bf16 ring.
+template <int D, int M> struct KvStage {};
+template <int D> struct alignas(128) KvStage<D, kPagedE4m3> {
+    uint8_t k[kBNd<D> * D];
+    uint8_t v[kBNd<D> * D];
+    uint64_t k_full, k_empty, v_full, v_empty;
+    uint64_t cv_bar;              // rendezvous of the 64 converter threads (bounded, unlike bar.sync)
+    uint32_t k_loaded, v_loaded;  // bit pg: page pg of the staged tile was loaded (else it is zeros)
+};
+
+template <int D, int M>
 struct alignas(1024) PrefillSmem {
     // q, k, v: tiles of kBM x kPad elements back to back (the MMA issuer steps between them by
     // a constant)
     __nv_bfloat16 q[Cfg<D>::QT][kBM * kPad<D>];  // kPad/64 boxes each
-    __nv_bfloat16 k[kStages][kBN * kPad<D>];     // kPad/64 boxes each
-    __nv_bfloat16 v[kStages][kBN * kPad<D>];     // kPad/64 boxes each
+    __nv_bfloat16 k[kStages][kBNd<D> * kPad<D>];  // kPad/64 boxes each
+    __nv_bfloat16 v[kStages][kBNd<D> * kPad<D>];  // kPad/64 boxes each
+    KvStage<D, M> st;
     uint64_t q_full;
     uint64_t u_full[kStages], u_empty[kStages];
     uint64_t s_full[kQTilesMax];
     uint64_t p_full[kQTilesMax];
     uint64_t o_done[kQTilesMax];
-    uint64_t s_free[kQTilesMax];   // separate-P pipeline: the softmax has read S_t
-    uint64_t pv_done[kQTilesMax];  // separate-P pipeline: PV_t finished with P_t and O_t
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -135,59 +155,112 @@ __device__ __forceinline__ int kv_end_of(const PrefillParams &p, int b) {
     return min(max(p.ctx_lens[b], 0), p.max_pages * kPageTokens);
 }
 
-// At d = 64 the TMEM has room for P next to S and O (S0|S1|O0|O1|P0|P1 = 128+128+64+64+64+64
-// columns), so P gets its own columns and S_t(j+1) can be issued as soon as the softmax has
-// read S_t(j), before PV_t(j): the next scores are ready when the softmax finishes a tile.
-// At d = 128 the 512 columns hold exactly S0|S1|O0|O1 and P is written over its scores.
-template <int D> struct SeparateP { static constexpr bool value = (kPad<D> == 64); };
-
-// TMEM columns: S_t at 128 t; O_t after all S buffers; P_t after all O accumulators when it
-// has its own columns, else over the first 64 columns of S_t.
+// TMEM columns: S_t at BN t; O_t after all S buffers; P_t (bf16 pairs) over the first BN/2
+// columns of S_t.
 template <int D> __device__ __forceinline__ uint32_t o_col(int t) {
-    return (uint32_t)(Cfg<D>::QT * kBN + t * kPad<D>);
+    return (uint32_t)(Cfg<D>::QT * kBNd<D> + t * kPad<D>);
 }
-template <int D> __device__ __forceinline__ uint32_t p_col(int t) {
-    return SeparateP<D>::value ? (uint32_t)(Cfg<D>::QT * (kBN + kPad<D>) + t * 64) : (uint32_t)(t * kBN);
-}
+template <int D> __device__ __forceinline__ uint32_t p_col(int t) { return (uint32_t)(t * kBNd<D>); }
 
 // Key tiles query tile t of this CTA must visit: keys < limit can be valid for some of its rows.
+template <int BN>
 __device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_end, int delta) {
     if (qs >= p.Nq) return 0;  // no rows in this tile (ragged end)
     int limit = kv_end;
     if (p.causal) limit = min(limit, min(qs + kBM, p.Nq) + delta);
-    return limit > 0 ? (limit + kBN - 1) / kBN : 0;
+    return limit > 0 ? (limit + BN - 1) / BN : 0;
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
-__device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
+template <int D, int M>
+__device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
                              const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int bh, int bh_kv, int q0,
                              int n_all, WaitCtx wc) {
     constexpr int kBoxes = kPad<D> / 64;
     prefetch_tensormap(tmQ);
-    prefetch_tensormap(tmK);
-    prefetch_tensormap(tmV);
+    if constexpr (M != kPagedE4m3) {
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
+    }
     mbar_arrive_expect_tx(&sm.q_full, Cfg<D>::QT * kBoxes * kBoxBytes);
 #pragma unroll
     for (int t = 0; t < Cfg<D>::QT; ++t)
 #pragma unroll
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
-    // paged mode: pool row (page * Hkv + head) of each page of a tile; pages past the
-    // sequence's last page, or with an id outside the pool (an unmapped page, whose keys the
-    // softmax masks), get an out-of-range row, which TMA reads as zeros
+    // paged modes: the page ids of each tile (-1 past the sequence's last page), fetched one
+    // ring unit ahead of their use, so the global loads stay in flight across the ring wait
+    constexpr int kBN = kBNd<D>;
     constexpr int kTilePages = kBN / kPageTokens;
     const int kvh = bh_kv % p.Hkv;
-    const int pages_used = p.paged ? (kv_end_of(p, b) + kPageTokens - 1) / kPageTokens : 0;
-    // raw page ids (-1 past the last page); they are only read when the tile is loaded, one
-    // unit later, so the global loads stay in flight across the ring wait
-    auto fetch_rows = [&](int tile, int (&ids)[kTilePages]) {
+    const int pages_used = (M != kContig) ? (kv_end_of(p, b) + kPageTokens - 1) / kPageTokens : 0;
+    auto fetch_ids = [&](int tile, int (&ids)[kTilePages]) {
 #pragma unroll
         for (int pg = 0; pg < kTilePages; ++pg) {
             const int lp = tile * kTilePages + pg;
             ids[pg] = lp < pages_used ? p.page_table[(size_t)b * p.max_pages + lp] : -1;
         }
     };
+    int ids_prev[kTilePages], ids_cur[kTilePages], ids_next[kTilePages];
+#pragma unroll
+    for (int pg = 0; pg < kTilePages; ++pg) ids_prev[pg] = ids_cur[pg] = ids_next[pg] = -1;
+    if constexpr (M != kContig) fetch_ids(0, ids_next);
+
+    if constexpr (M == kPagedE4m3) {
+        // e4m3 pages: one bulk copy per mapped page block (16 rows of d codes) into the staging
+        // tiles; pages past the sequence's end or unmapped are not loaded (the converters write
+        // zeros there, and the softmax masks those keys).  K(u) and V(u-1) are staged as the
+        // converters free the staging tiles; the ring slots are the converters' to fill.
+        constexpr uint32_t kPageBytes = kPageTokens * D;
+        auto stage = [&](uint8_t *dst, const uint8_t *pool, uint64_t *full, uint32_t *loaded,
+                         const int (&ids)[kTilePages]) {
+            uint32_t mask = 0, bytes = 0;
+#pragma unroll
+            for (int pg = 0; pg < kTilePages; ++pg)
+                if (ids[pg] >= 0 && ids[pg] < p.num_pages) {
+                    mask |= 1u << pg;
+                    bytes += kPageBytes;
+                }
+            *loaded = mask;
+            mbar_arrive_expect_tx(full, bytes);
+#pragma unroll
+            for (int pg = 0; pg < kTilePages; ++pg)
+                if ((mask >> pg) & 1u)
+                    bulk_load(dst + pg * kPageBytes, pool + ((size_t)ids[pg] * p.Hkv + kvh) * kPageBytes, kPageBytes,
+                              full);
+        };
+        int kf = 0, vf = 0;  // tiles staged so far
+        for (int u = 0; u <= n_all; ++u) {
+#pragma unroll
+            for (int pg = 0; pg < kTilePages; ++pg) {
+                ids_prev[pg] = ids_cur[pg];
+                ids_cur[pg] = ids_next[pg];
+            }
+            if (u + 1 < n_all) fetch_ids(u + 1, ids_next);
+            if (u < n_all) {  // K(u)
+                if (kf > 0 && !mbar_wait(&sm.st.k_empty, (uint32_t)((kf - 1) & 1), wc, 2)) break;
+                stage(sm.st.k, p.k8, &sm.st.k_full, &sm.st.k_loaded, ids_cur);
+                ++kf;
+            }
+            if (u > 0) {  // V(u-1)
+                if (vf > 0 && !mbar_wait(&sm.st.v_empty, (uint32_t)((vf - 1) & 1), wc, 3)) break;
+                stage(sm.st.v, p.v8, &sm.st.v_full, &sm.st.v_loaded, ids_prev);
+                ++vf;
+            }
+        }
+        if (*wc.abort_flag) {
+            // unwinding: let every copy still in flight land before the CTA exits
+            WaitCtx drain{nullptr, wc.status};
+            (void)mbar_wait(&sm.q_full, 0, drain, 90);
+            if (kf > 0) (void)mbar_wait(&sm.st.k_full, (uint32_t)((kf - 1) & 1), drain, 92);
+            if (vf > 0) (void)mbar_wait(&sm.st.v_full, (uint32_t)((vf - 1) & 1), drain, 93);
+        }
+        return;
+    }
+
+    // bf16 K/V by TMA into the ring slots.  Paged: pool row (page * Hkv + head) of each page of a
+    // tile; pages past the sequence's last page, or with an id outside the pool (an unmapped page,
+    // whose keys the softmax masks), get an out-of-range row, which TMA reads as zeros.
     auto load_tile = [&](__nv_bfloat16 *dst, const CUtensorMap *map, uint64_t *bar, const int (&ids)[kTilePages]) {
 #pragma unroll
         for (int pg = 0; pg < kTilePages; ++pg) {
@@ -198,18 +271,13 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
                 tma_load_3d(dst + i * (kBN * 64) + pg * (kPageTokens * 64), map, bar, i * 64, 0, row);
         }
     };
-    int rows_prev[kTilePages], rows_cur[kTilePages], rows_next[kTilePages];
-#pragma unroll
-    for (int pg = 0; pg < kTilePages; ++pg) rows_prev[pg] = rows_cur[pg] = rows_next[pg] = 0;
-    if (p.paged) fetch_rows(0, rows_next);
-
     int fills = 0;
     for (int u = 0; u <= n_all; ++u) {
         const int slot = u % kStages, use = u / kStages;
         if (use > 0 && !mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 1)) break;
         const bool has_k = u < n_all, has_v = u > 0;
-        mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kBoxBytes);
-        if (!p.paged) {
+        mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kKvBoxBytes<D>);
+        if constexpr (M == kContig) {
             if (has_k) {
 #pragma unroll
                 for (int i = 0; i < kBoxes; ++i)
@@ -221,18 +289,18 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
                     tma_load_3d(sm.v[slot] + i * (kBN * 64), tmV, &sm.u_full[slot], i * 64, (u - 1) * kBN, bh_kv);
             }
         } else {
-            // a 128-key tile is 8 pages of 16 keys: one 16-row box per page and 64-column
-            // block, stacked in the tile's 128-byte-swizzled rows.  K(u) uses the pages of
-            // tile u, V(u-1) those of tile u-1 (already looked up for K(u-1)); tile u+1's page
-            // ids are fetched here, one unit ahead of their use.
+            // a tile is kBN / 16 pages of 16 keys: one 16-row box per page and 64-column block,
+            // stacked in the tile's 128-byte-swizzled rows.  K(u) uses the pages of tile u,
+            // V(u-1) those of tile u-1 (already looked up for K(u-1)); tile u+1's page ids are
+            // fetched here, one unit ahead of their use.
 #pragma unroll
             for (int pg = 0; pg < kTilePages; ++pg) {
-                rows_prev[pg] = rows_cur[pg];
-                rows_cur[pg] = rows_next[pg];
+                ids_prev[pg] = ids_cur[pg];
+                ids_cur[pg] = ids_next[pg];
             }
-            if (u + 1 < n_all) fetch_rows(u + 1, rows_next);
-            if (has_k) load_tile(sm.k[slot], tmK, &sm.u_full[slot], rows_cur);
-            if (has_v) load_tile(sm.v[slot], tmV, &sm.u_full[slot], rows_prev);
+            if (u + 1 < n_all) fetch_ids(u + 1, ids_next);
+            if (has_k) load_tile(sm.k[slot], tmK, &sm.u_full[slot], ids_cur);
+            if (has_v) load_tile(sm.v[slot], tmV, &sm.u_full[slot], ids_prev);
         }
         ++fills;
     }
@@ -245,87 +313,124 @@ __device__ void run_producer(PrefillSmem<D> &sm, const PrefillParams &p, const C
     }
 }
 
-// ------------------------------------------------------------------ MMA issuers, separate P
-// role 0 issues S(0) and every S(j+1) (as soon as the softmax has read S(j)); role 1 issues every
-// PV(j) (once P(j) is written).  S and PV touch disjoint TMEM columns (S | O | P), so neither
-// waits for the other.  Both walk every ring unit and commit its release (the empty barriers
-// count both): unit u = {K(u), V(u-1)} is read by S(u) and by PV(u-1).
+// ------------------------------------------------------------------ e4m3 converters
+// Two warps widen each staged e4m3 tile into its bf16 ring slot, in the layout a TMA load with the
+// 128-byte swizzle gives (16-byte chunk c of row r of a 64-column box at chunk c ^ (r % 8)), so the
+// MMA issuer reads it exactly as a bf16 tile.  Each e4m3 value is a bf16 value (the widening is
+// exact); the tensor scales fold elsewhere (the key scale into the score scale, the value scale
+// into the epilogue).  Rows of pages that were not loaded become zeros.  A ring unit {K(u), V(u-1)}
+// is complete when both are written: the converters fence their shared-memory writes for the async
+// proxy, meet at a named barrier, and one of them arrives on the unit's full barrier.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack_bf16x2(f.x, f.y);
+}
+
 template <int D>
-__device__ void run_mma_sep(PrefillSmem<D> &sm, uint32_t tmem, int n_all, int role, WaitCtx wc) {
-    static_assert(SeparateP<D>::value && Cfg<D>::QT == 1, "one query tile, P in its own columns");
-    constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
-    constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-    constexpr uint64_t kTile = (uint64_t)(kBM * kPad<D> * 2) >> 4;
-    const uint64_t dq = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-    const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-    const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
+__device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, __nv_bfloat16 *dst, int ct) {
+    constexpr int kBN = kBNd<D>;
+    constexpr int kChunksPerRow = D / 16;  // 16-byte chunks of e4m3 per row
+    uint8_t *d8 = reinterpret_cast<uint8_t *>(dst);
+#pragma unroll 4
+    for (int idx = ct; idx < kBN * kChunksPerRow; idx += 64) {
+        const int r = idx / kChunksPerRow, c16 = idx % kChunksPerRow;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if ((loaded >> (r / kPageTokens)) & 1u) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + r * D + c16 * 16);
+            lo = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
+                            e4m3x2_to_bf16x2(v.y >> 16));
+            hi = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
+                            e4m3x2_to_bf16x2(v.w >> 16));
+        }
+        const int col = c16 * 16;               // first of the 16 columns
+        const int box = col >> 6, k0 = (col & 63) >> 3;  // 16-byte chunks k0, k0 + 1 of the row
+        uint8_t *row = d8 + box * (kBN * 128) + r * 128;
+        *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ (r & 7)) << 4)) = hi;
+    }
+}
+
+template <int D>
+__device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, WaitCtx wc) {
+    // every converter arrives, then waits for the phase to complete (bounded like every wait)
+    uint32_t cv_phase = 0;
+    auto sync_converters = [&]() -> bool {
+        mbar_arrive(&sm.st.cv_bar);
+        const bool done = __all_sync(0xffffffffu, mbar_wait(&sm.st.cv_bar, cv_phase & 1u, wc, 7));
+        ++cv_phase;
+        return done;
+    };
     bool ok = true;
-    if (role == 0) {
-        ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.u_full[0], 0, wc, 10);
-        if (ok) {
-            tc_fence_after_sync();
-            tc_mma_ss_ksteps<D / 16>(tmem, dq, dk, idS, 0u);  // S(0) = Q K(0)^T (K(0) in slot 0)
-            tc_commit(&sm.s_full[0]);
+    int kf = 0, vf = 0;
+    for (int u = 0; u <= n_all && ok; ++u) {
+        const int slot = u % kStages, use = u / kStages;
+        if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 4))) {
+            ok = false;
+            break;
         }
-    }
-    tc_commit(&sm.u_empty[0]);
-    for (int j = 0; j < n_all && ok; ++j) {
-        const int u = j + 1;  // unit with V(j) and K(j+1)
-        if (!(ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13))) break;
-        if (role == 0) {
-            if (j + 1 < n_all) {
-                if (!(ok = mbar_wait(&sm.s_free[0], (uint32_t)(j & 1), wc, 17))) break;
-                tc_fence_after_sync();
-                tc_mma_ss_ksteps<D / 16>(tmem, dq, dk + ((u & 1) ? kTile : 0), idS, 0u);  // K(j+1): slot u % 2
-                tc_commit(&sm.s_full[0]);
+        if (u < n_all) {  // K(u): stage -> slot u % 2
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.st.k_full, (uint32_t)(kf & 1), wc, 5))) {
+                ok = false;
+                break;
             }
-        } else {
-            if (!(ok = mbar_wait(&sm.p_full[0], (uint32_t)(j & 1), wc, 12))) break;
-            tc_fence_after_sync();
-            tc_mma_ts_k8(tmem + o_col<D>(0), tmem + p_col<D>(0), dv + ((u & 1) ? kTile : 0), idPV,
-                         j > 0 ? 1u : 0u);  // V(j): slot u % 2
-            tc_commit(&sm.pv_done[0]);
-            if (j == n_all - 1) tc_commit(&sm.o_done[0]);
+            widen_tile<D>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
+            if (!(ok = sync_converters())) break;
+            if (ct == 0) mbar_arrive(&sm.st.k_empty);
+            ++kf;
         }
-        tc_commit(&sm.u_empty[u % kStages]);
+        if (u > 0) {  // V(u-1): stage -> slot u % 2
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.st.v_full, (uint32_t)(vf & 1), wc, 6))) {
+                ok = false;
+                break;
+            }
+            widen_tile<D>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
+            ++vf;
+        }
+        fence_proxy_async_smem();  // this thread's tile writes, before the MMA's reads
+        if (!(ok = sync_converters())) break;
+        if (ct == 0) {
+            if (u > 0) mbar_arrive(&sm.st.v_empty);
+            mbar_arrive(&sm.u_full[slot]);
+        }
     }
-    // wait (bounded) until every MMA issued above has finished with TMEM and smem
-    tc_commit(&sm.drain);
-    WaitCtx drain{nullptr, wc.status};
-    (void)mbar_wait(&sm.drain, 0, drain, 19);
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D>
-__device__ void run_mma(PrefillSmem<D> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
-    static_assert(!SeparateP<D>::value, "P over S; the separate-P shape uses run_mma_sep");
+template <int D, int M>
+__device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
+    constexpr int kBN = kBNd<D>;
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
     static_assert(kStages == 2, "slot selects below");
-    // Descriptors of the operand buffers, built once (the tiles of Q, of K and of V are equally
-    // spaced, one tile = kTile descriptor units); each MMA advances one by a constant.
-    constexpr uint64_t kTile = (uint64_t)(kBM * kPad<D> * 2) >> 4;
+    // Descriptors of the operand buffers, built once (the Q tiles, the K tiles and the V tiles
+    // are each equally spaced: kQTile and kKvTile descriptor units); each MMA advances one by a
+    // constant.
+    constexpr uint64_t kQTile = (uint64_t)(kBM * kPad<D> * 2) >> 4;
+    constexpr uint64_t kKvTile = (uint64_t)(kBN * kPad<D> * 2) >> 4;
     const uint64_t dq = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
     const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-    const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), kBoxBytes, 1024);
+    const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), kKvBoxBytes<D>, 1024);
 
     // S_t(j) = Q_t K_j^T  (A = Q_t, B = K_j: both K-major, 128-byte swizzle), d/16 k-steps
-    // issued in groups from single asm statements
+    // issued in groups from single asm statements (the second 64-column box of a 128-row tile
+    // starts 16 KB on, which the grouped issue assumes)
+    static_assert(kPad<D> == 64 || kBN * 128 == 16384, "k-step layout of the grouped issue");
     auto issue_S = [&](int t, int j) {
-        const uint64_t a = dq + (t ? kTile : 0);
-        const uint64_t b = dk + ((j & 1) ? kTile : 0);  // K(j) sits in slot j % 2
+        const uint64_t a = dq + (t ? kQTile : 0);
+        const uint64_t b = dk + ((j & 1) ? kKvTile : 0);  // K(j) sits in slot j % 2
         const uint32_t tS = tmem + (uint32_t)(t * kBN);
-        static_assert(kBoxBytes == 16384, "k-step layout of the grouped issue");
         tc_mma_ss_ksteps<D / 16>(tS, a, b, idS, 0u);
         tc_commit(&sm.s_full[t]);
     };
     // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
-    static_assert(kBN / 16 == 8, "PV is one group of eight k-steps");
+    static_assert(kBN == 128 || kBN == 64, "PV is one group of eight or four k-steps");
     auto issue_PV = [&](int t, int j) {
-        const uint64_t b = dv + ((j & 1) ? 0 : kTile);  // V(j) sits in slot (j + 1) % 2
+        const uint64_t b = dv + ((j & 1) ? 0 : kKvTile);  // V(j) sits in slot (j + 1) % 2
         const uint32_t tP = tmem + p_col<D>(t);
         const uint32_t tO = tmem + o_col<D>(t);
-        tc_mma_ts_k8(tO, tP, b, idPV, j > 0 ? 1u : 0u);
+        if constexpr (kBN == 128) tc_mma_ts_k8(tO, tP, b, idPV, j > 0 ? 1u : 0u);
+        else tc_mma_ts_k4(tO, tP, b, idPV, j > 0 ? 1u : 0u);
     };
 
     // The data waits below (Q, ring units) need no tcgen05 fence: TMA writes and the MMA's
@@ -389,9 +494,10 @@ __device__ __forceinline__ void mask_chunks(uint32_t (&s)[2][32], int nvalid) {
 
 // Paged mode: scores of keys whose page is unmapped (bit pg of `bad` set: keys 16 pg .. 16 pg + 15
 // of the tile) become -inf, as a padded key would.
-__device__ __forceinline__ void mask_pages(uint32_t (&s)[2][2][32], uint32_t bad) {
+template <int H>
+__device__ __forceinline__ void mask_pages(uint32_t (&s)[H][2][32], uint32_t bad) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < H; ++h)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
@@ -436,15 +542,16 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t t
     }
 }
 
-template <int D>
-__device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t tmem, int t, int bh, int q0,
+template <int D, int M>
+__device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint32_t tmem, int t, int bh, int q0,
                             int n_tiles, int kv_end, int delta, WaitCtx wc) {
     const int r = threadIdx.x & 127;  // query row in the tile = TMEM lane
     const int wq = (threadIdx.x >> 5) & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    constexpr int kBN = kBNd<D>;
+    constexpr int kHalves = kBN / 64;  // the row's scores of a tile, in halves of 64
     const uint32_t tS = lane_base + (uint32_t)(t * kBN);
     const uint32_t tO = lane_base + o_col<D>(t);
-    const uint32_t tP = lane_base + p_col<D>(t);
     const int qs = q0 + t * kBM;  // first row of this tile
     const int row = qs + r;
     const float c = p.scale_log2;
@@ -454,20 +561,22 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     float l = 0.f;
     bool ok = true;
     // Paged mode: a page id outside the pool is an unmapped page that holds no token (the producer
-    // loads zeros there; its keys are masked here).  Lanes 0-7 of each warp read the 8 table entries
-    // of a tile themselves, one tile ahead of its use, and a ballot turns them into a warp-uniform
-    // mask of unmapped pages.
+    // loads zeros there; its keys are masked here).  The first lanes of each warp read the tile's
+    // table entries (one per 16 keys) themselves, one tile ahead of its use, and a ballot turns
+    // them into a warp-uniform mask of unmapped pages.
+    constexpr bool kPaged = (M != kContig);
     const int lane = threadIdx.x & 31;
-    const int pages_used = p.paged ? (kv_end + kPageTokens - 1) / kPageTokens : 0;
-    const int32_t *table = p.paged ? p.page_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
+    const int pages_used = kPaged ? (kv_end + kPageTokens - 1) / kPageTokens : 0;
+    const int32_t *table = kPaged ? p.page_table + (size_t)(bh / p.H) * p.max_pages : nullptr;
     auto table_entry = [&](int tile) {
         const int lp = tile * (kBN / kPageTokens) + lane;
         return (lane < kBN / kPageTokens && lp < pages_used) ? table[lp] : 0;
     };
-    int next_id = p.paged ? table_entry(0) : 0;
+    int next_id = 0;
+    if constexpr (kPaged) next_id = table_entry(0);
     for (int j = 0; j < n_tiles; ++j) {
         uint32_t unmapped = 0;
-        if (p.paged) {
+        if constexpr (kPaged) {
             const int id = next_id;
             if (j + 1 < n_tiles) next_id = table_entry(j + 1);
             unmapped = __ballot_sync(0xffffffffu, id < 0 || id >= p.num_pages);
@@ -489,28 +598,25 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             if (p.causal) lim = min(lim, row + delta + 1);
             nvalid = lim - key0;
         }
-        uint32_t s[2][2][32];  // the row's 128 scores as two halves of 64
+        uint32_t s[kHalves][2][32];  // the row's scores as halves of 64
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kHalves; ++h) {
             tmem_ld32(tS + h * 64, s[h][0]);
             tmem_ld32(tS + h * 64 + 32, s[h][1]);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kHalves; ++h) {
             tmem_wait_ld(s[h][0]);
             tmem_wait_ld(s[h][1]);
         }
-        if constexpr (SeparateP<D>::value) {
-            // the scores are in registers: the MMA issuer may compute S_t(j+1) into the buffer
-            tc_fence_before_sync();
-            mbar_arrive(&sm.s_free[t]);
-        }
         if (need_mask) {
-            mask_chunks(s[0], nvalid);
-            mask_chunks(s[1], nvalid - 64);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h) mask_chunks(s[h], nvalid - 64 * h);
         }
-        if (unmapped) mask_pages(s, unmapped);
-        const float mx = fmaxf(max64(s[0]), max64(s[1]));
+        if (kPaged && unmapped) mask_pages<kHalves>(s, unmapped);
+        float mx = max64(s[0]);
+#pragma unroll
+        for (int h = 1; h < kHalves; ++h) mx = fmaxf(mx, max64(s[h]));
         const float m_cand = mx * c;  // -inf stays -inf (c > 0)
         const bool resc = m_cand > m_ref + kRescaleThreshold;
         float alpha = 1.f;
@@ -523,24 +629,11 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
         const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
 
         // P = 2^(s*c - m_use) as bf16 pairs (even key in the low half, as the TMEM A operand
-        // expects): keys 0-63 -> columns 0-31, keys 64-127 -> columns 32-63, over scores
-        // already read into registers.
+        // expects): keys 64h .. 64h + 63 -> columns 32h .. 32h + 31, over the scores already
+        // read into registers.
         uint64_t rs2[4] = {0, 0, 0, 0};
-        if constexpr (SeparateP<D>::value) {
-            // P_t and O_t are free once PV_t(j-1) has completed
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done[t], (uint32_t)((j - 1) & 1), wc, 28 + t))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-            }
-            exp_store(s[0], tP, c2, negm2, rs2);
-            exp_store(s[1], tP + 32, c2, negm2, rs2);
-        } else {
-            exp_store(s[0], tS, c2, negm2, rs2);
-            exp_store(s[1], tS + 32, c2, negm2, rs2);
-        }
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h) exp_store(s[h], tS + 32 * h, c2, negm2, rs2);
         {
             const uint64_t t01 = f32x2_add(rs2[0], rs2[1]);
             const uint64_t t23 = f32x2_add(rs2[2], rs2[3]);
@@ -549,8 +642,8 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
             l += a0 + a1;
         }
 
-        // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled (P over S), or
-        // pv_done was waited for above (separate P)
+        // O_t is stable here: PV_t(j-1) completed before S_t(j) was signalled (the issuer's
+        // commits complete in order, and S_t(j) is issued after PV_t(j-1))
         if (j > 0 && __any_sync(0xffffffffu, resc)) rescale_o<D>(tO, alpha);
         tmem_wait_st();
         tc_fence_before_sync();
@@ -564,7 +657,7 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     }
     if (!ok) return;
     const bool have = (n_tiles > 0) && (l > 0.f);
-    const float inv_l = have ? 1.f / l : 0.f;
+    const float inv_l = have ? (M == kPagedE4m3 ? p.o_scale : 1.f) / l : 0.f;
     const bool store = row < p.Nq;
     __nv_bfloat16 *orow = p.o + ((size_t)bh * p.Nq + (store ? row : 0)) * D;
 #pragma unroll
@@ -606,13 +699,28 @@ __device__ void run_softmax(PrefillSmem<D> &sm, const PrefillParams &p, uint32_t
     if (store && p.lse) p.lse[(size_t)bh * p.Nq + row] = have ? kLn2 * (m_ref + __log2f(l)) : -INFINITY;
 }
 
-template <int D>
-__global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
+// CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
+// d <= 64 CTA 56 KB, so three of them share an SM, launched at 80 registers (128 x (104 + 56) =
+// 20480 = 256 x 80); the converter warps take registers from the producer's warpgroup.
+template <int D, int M> struct Occ {
+    static constexpr int kMinBlocks = Cfg<D>::kMinBlocks;
+    static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;
+};
+template <> struct Occ<32, kPagedE4m3> {
+    static constexpr int kMinBlocks = 3;
+    static constexpr uint32_t kRegsSoftmax = 104, kRegsOther = 56;
+};
+template <> struct Occ<64, kPagedE4m3> : Occ<32, kPagedE4m3> {};
+static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kRegsOther) <= 256 * 80,
+              "e4m3 d<=64 register split");
+
+template <int D, int M>
+__global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
-    PrefillSmem<D> &sm =
-        *reinterpret_cast<PrefillSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PrefillSmem<D, M> &sm =
+        *reinterpret_cast<PrefillSmem<D, M> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA order: heads are taken in chunks small enough that the chunk's K/V stays in L2
@@ -635,7 +743,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     const int q0 = unit * (kBM * Cfg<D>::QT);
     // keys of this sequence and the causal offset (query i sits at key position i + delta)
     int kv_end, delta;
-    if (p.paged) {
+    if constexpr (M != kContig) {
         kv_end = kv_end_of(p, b);
         delta = kv_end - p.Nq;
     } else {
@@ -644,23 +752,28 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     }
     int n[kQTilesMax] = {0, 0};
 #pragma unroll
-    for (int t = 0; t < Cfg<D>::QT; ++t) n[t] = tiles_for(p, q0 + t * kBM, kv_end, delta);
+    for (int t = 0; t < Cfg<D>::QT; ++t) n[t] = tiles_for<kBNd<D>>(p, q0 + t * kBM, kv_end, delta);
     const int n_all = max(n[0], n[1]);
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.u_full[s], 1);
-            mbar_init(&sm.u_empty[s], Cfg<D>::kMmaIssuers);
+            mbar_init(&sm.u_empty[s], 1);
         }
         for (int t = 0; t < Cfg<D>::QT; ++t) {
             mbar_init(&sm.s_full[t], 1);
             mbar_init(&sm.p_full[t], kBM);
             mbar_init(&sm.o_done[t], 1);
-            mbar_init(&sm.s_free[t], kBM);
-            mbar_init(&sm.pv_done[t], 1);
         }
-        mbar_init(&sm.drain, Cfg<D>::kMmaIssuers);
+        mbar_init(&sm.drain, 1);
+        if constexpr (M == kPagedE4m3) {
+            mbar_init(&sm.st.k_full, 1);
+            mbar_init(&sm.st.v_full, 1);
+            mbar_init(&sm.st.k_empty, 1);
+            mbar_init(&sm.st.v_empty, 1);
+            mbar_init(&sm.st.cv_bar, 64);
+        }
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -675,22 +788,19 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     WaitCtx wc{&sm.abort_flag, p.status};
 
     if (warp >= 4 * Cfg<D>::QT) {
-        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<Cfg<D>::kRegsOther>();
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<Occ<D, M>::kRegsOther>();
         if (warp == Cfg<D>::kProducerWarp) {
-            if (lane == 0 && n_all > 0) run_producer<D>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
+            if (lane == 0 && n_all > 0) run_producer<D, M>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
         } else if (warp == Cfg<D>::kMmaWarp) {
-            if constexpr (Cfg<D>::kMmaIssuers == 2) {
-                if (lane == 0 && n_all > 0) run_mma_sep<D>(sm, tmem, n_all, 0, wc);
-            } else {
-                if (lane == 0 && n_all > 0) run_mma<D>(sm, tmem, n, n_all, wc);
-            }
-        } else if constexpr (Cfg<D>::kMmaIssuers == 2) {
-            if (warp == Cfg<D>::kMmaWarp + 1 && lane == 0 && n_all > 0) run_mma_sep<D>(sm, tmem, n_all, 1, wc);
+            if (lane == 0 && n_all > 0) run_mma<D, M>(sm, tmem, n, n_all, wc);
+        } else if constexpr (M == kPagedE4m3) {
+            // the last two warps of the CTA convert e4m3 tiles into the ring
+            if (n_all > 0) run_convert<D>(sm, n_all, (int)threadIdx.x - (Cfg<D>::kThreads - 64), wc);
         }
     } else {
-        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<Cfg<D>::kRegsSoftmax>();
+        if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<Occ<D, M>::kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
-        run_softmax<D>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
+        run_softmax<D, M>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
     }
 
     tc_fence_before_sync();
@@ -701,17 +811,40 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, Cfg<D>::kMinBlocks)
     }
 }
 
-template <int D>
-cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
+// The register split of the kernel's warpgroups (setmaxnreg) draws on the block's launch
+// allocation; a split larger than it would wait forever.  Checked once per kernel against the
+// register count the compiler gave it, before the first launch.
+template <int D, int M>
+cudaError_t check_register_split() {
+    static int verdict = 0;  // 0 unknown, 1 fits, -1 does not
+    if (verdict == 0) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, M>);
+        if (e != cudaSuccess) return e;
+        const long pool = (long)fa.numRegs * Cfg<D>::kThreads;
+        const long need = 128L * (Cfg<D>::QT * (long)Occ<D, M>::kRegsSoftmax +
+                                  (Cfg<D>::kThreads / 128 - Cfg<D>::QT) * (long)Occ<D, M>::kRegsOther);
+        verdict = (!Cfg<D>::kSplitRegs || need <= pool) ? 1 : -1;
+    }
+    return verdict == 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+template <int D, int M>
+cudaError_t launch_prefill_dm(const PrefillArgs &a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
     bool ok_maps = encode_qkv_map(&tq, a.q, BH, a.Nq, D);
-    if (a.paged)  // pages [num_pages * Hkv] of 16 x D, one 16-row box per page
+    if constexpr (M == kPagedBf16)  // pages [num_pages * Hkv] of 16 x D, one 16-row box per page
         ok_maps = ok_maps && encode_qkv_map(&tk, a.k, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens) &&
                   encode_qkv_map(&tv, a.v, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens);
-    else
-        ok_maps = ok_maps && encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D) && encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D);
+    else if constexpr (M == kContig)  // boxes of kBNd<D> key rows
+        ok_maps = ok_maps && encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D, kBNd<D>) &&
+                  encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D, kBNd<D>);
+    else  // e4m3 pages travel by plain bulk copies: the K/V maps are not used
+        tk = tv = tq;
     if (!ok_maps) return cudaErrorInvalidValue;
+    cudaError_t e = check_register_split<D, M>();
+    if (e != cudaSuccess) return e;
     PrefillParams p;
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
@@ -724,26 +857,36 @@ cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
     p.causal = a.causal;
     p.Hkv = a.Hkv;
     p.group = a.H / a.Hkv;
-    p.paged = a.paged;
     p.page_table = a.page_table;
     p.ctx_lens = a.ctx_lens;
     p.max_pages = a.max_pages;
     p.num_pages = a.num_pages;
+    p.k8 = static_cast<const uint8_t *>(a.k);
+    p.v8 = static_cast<const uint8_t *>(a.v);
     p.n_units = (a.Nq + kBM * Cfg<D>::QT - 1) / (kBM * Cfg<D>::QT);
     {
         // about 48 MB of K/V per chunk: two chunks (the one finishing, the one starting) fit
         // in the 126 MB L2 together.  Query heads of one group share their K/V.
-        const double kv_bytes_per_head = 2.0 * a.Nkv * D * 2.0 / p.group;  // Nkv: capacity when paged
+        const double elem = (M == kPagedE4m3) ? 1.0 : 2.0;
+        const double kv_bytes_per_head = 2.0 * a.Nkv * D * elem / p.group;  // Nkv: capacity when paged
         int hpc = (int)(48.0e6 / kv_bytes_per_head);
         p.heads_per_chunk = hpc < 1 ? 1 : (hpc > BH ? BH : hpc);
     }
-    p.scale_log2 = a.scale * kLog2e;
-    const size_t smem = sizeof(PrefillSmem<D>) + 1024;
-    cudaError_t e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<D>), (int)smem);
+    p.scale_log2 = a.scale * kLog2e * (M == kPagedE4m3 ? a.k_scale : 1.f);
+    p.o_scale = (M == kPagedE4m3) ? a.v_scale : 1.f;
+    const size_t smem = sizeof(PrefillSmem<D, M>) + 1024;
+    e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<D, M>), (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)p.n_units * BH);
-    prefill_kernel<D><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, M><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillArgs &a, cudaStream_t stream) {
+    if (!a.paged) return launch_prefill_dm<D, kContig>(a, stream);
+    if (a.kv_fp8) return launch_prefill_dm<D, kPagedE4m3>(a, stream);
+    return launch_prefill_dm<D, kPagedBf16>(a, stream);
 }
 
 }  // namespace

@@ -254,6 +254,17 @@ __device__ __forceinline__ void tc_mma_ts_k8(uint32_t d_tmem, uint32_t a_tmem, u
         ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// Four k-steps (64 keys) of the same form: A columns 0, 8, 16, 24 from a_tmem.
+__device__ __forceinline__ void tc_mma_ts_k4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 ta;\n\t.reg .b64 rb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %4, %4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        ATTN_TS_STEP(8, 128) ATTN_TS_STEP(16, 256) ATTN_TS_STEP(24, 384) "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void tc_mma_ts_k8_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                     uint32_t acc) {
     asm volatile(

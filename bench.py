@@ -299,6 +299,24 @@ class PagedPrefillCase:
                                   self.shape.scale, out=self.o, lse=self.lse)
 
 
+class PagedPrefillFp8Case(PagedPrefillCase):
+    """The chunked prefill over an e4m3 copy of the same cache (kv_quantize_fp8, per-tensor
+    scale 6/448), with paged_attn_prefill_fp8."""
+    SCALE = 6.0 / 448
+
+    def __init__(self, shape, kv_heads, nq, torch, A):
+        super().__init__(shape, kv_heads, nq, torch, A)
+        d = self.dev
+        for n in ("k_pages", "v_pages"):
+            d[n] = A.kv_quantize_fp8(d[n], self.SCALE)
+        torch.cuda.synchronize()
+
+    def run(self):
+        d = self.dev
+        self.A.paged_attn_prefill_fp8(self.q, d["k_pages"], d["v_pages"], self.SCALE, self.SCALE, d["page_table"],
+                                      d["ctx_lens"], True, self.shape.scale, out=self.o, lse=self.lse)
+
+
 L2_BYTES = 129e6
 FLUSH_BYTES = 512 << 20
 
@@ -564,7 +582,7 @@ def gpu_arm(args):
             dec = DecodeCase(shape, torch, A)
         pre = None
         parts = [dec]
-    elif args.workload == "prefill_paged":
+    elif args.workload in ("prefill_paged", "prefill_paged_fp8"):
         return paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind)
     elif args.workload == "backward":
         return backward_arm(args, torch, A, rank, world, peaks, peak_kind)
@@ -714,8 +732,8 @@ def small_prefill_lines(args, torch, A, rank, world, peaks, peak_kind):
 
 def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
     """Chunked prefill over the paged cache, timed alone (not part of the default step)."""
-    case = PagedPrefillCase(workloads.PAGED_PREFILL, workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ,
-                            torch, A)
+    cls = PagedPrefillFp8Case if args.workload == "prefill_paged_fp8" else PagedPrefillCase
+    case = cls(workloads.PAGED_PREFILL, workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ, torch, A)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -735,7 +753,8 @@ def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                         "frac": round(achieved / peak, 4), "traffic": None, "kernel": "prefill_kernel (paged)",
                         "peak_source": f"{peak_kind} bf16_tflops"},
-           "config": {"workload": s.name, "B": s.B, "H": s.H, "Hkv": workloads.PAGED_PREFILL_KV_HEADS, "d": s.d,
+           "config": {"workload": s.name + (" (e4m3 cache)" if cls is PagedPrefillFp8Case else ""), "B": s.B,
+                      "H": s.H, "Hkv": workloads.PAGED_PREFILL_KV_HEADS, "d": s.d,
                       "Nq": case.Nq, "ctx_total": sum(case.ctx), "flops_per_call": case.flops,
                       "ms_per_call": round(ms, 4), "l2": "inputs larger than L2 (no flush)"},
            "gpu_launches": case.launches * args.steps}
@@ -890,7 +909,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8",
                                            *[f"decode_d{d}{s}" for d in (32, 64, 80, 96) for s in ("", "_fp8")],
-                                           "prefill_paged", "backward",
+                                           "prefill_paged", "prefill_paged_fp8", "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

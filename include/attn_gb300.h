@@ -232,6 +232,12 @@ int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v
  *   code = e4m3 nearest-even rounding of fp32(x) * fp32(1 / scale), saturating at
  *          +-448 (1 / scale is computed in fp32 on the host).
  *
+ * paged_attn_prefill_fp8: paged_attn_prefill over an e4m3 cache (k_pages, v_pages
+ *   [num_pages, Hkv, page_size, d] uint8 codes; k_scale, v_scale > 0 and finite): the
+ *   chunked prefill of a serving loop that keeps its cache in e4m3.  q, o, lse, the
+ *   table, the masks and the result are as in paged_attn_prefill, for the dequantised
+ *   cache.  The codes are widened exactly to bf16 in shared memory before the products;
+ *   the key scale multiplies the scores and the value scale the output.
  * paged_attn_decode_fp8: paged_attn_decode_gqa over an e4m3 cache (k_pages,
  *   v_pages [num_pages, Hkv, page_size, d] uint8 codes; k_scale, v_scale > 0
  *   and finite).  q, o, lse, the table, the workspace and the result are as in
@@ -246,6 +252,12 @@ int paged_attn_decode_fp8(const void *q, const void *k_pages, const void *v_page
                           int page_size, void *o, float *lse, int B, int H, int Hkv, int d,
                           int max_pages_per_seq, int num_pages, float scale, void *workspace,
                           size_t workspace_bytes, attn_stream_t stream);
+
+int paged_attn_prefill_fp8(const void *q, const void *k_pages, const void *v_pages, float k_scale,
+                           float v_scale, const int32_t *page_table, const int32_t *ctx_lens,
+                           int page_size, void *o, float *lse, int B, int H, int Hkv, int Nq, int d,
+                           int max_pages_per_seq, int num_pages, int causal, float scale,
+                           attn_stream_t stream);
 
 int kv_quantize_fp8(const void *src, void *dst, size_t n, float scale, attn_stream_t stream);
 

@@ -58,7 +58,10 @@ def test_workspace_size(lib):
     assert ws(1, 1, 64, 1, 16) == 1 * 1 * 1 * (64 + 4) * 4
     assert ws(0, 1, 64, 1, 16) == 0
     assert ws(1, 1, 96, 1, 16) == 1 * 1 * 1 * (96 + 4) * 4
-    assert ws(3, 2, 80, 33, 16) == 3 * 2 * 2 * (80 + 4) * 4  # 528 tokens: two 512-token splits
+    assert ws(3, 2, 80, 33, 16) == 3 * 2 * 1 * (80 + 4) * 4  # 528 tokens: one 1024-token split at d = 80
+    assert ws(3, 2, 96, 33, 16) == 3 * 2 * 1 * (96 + 4) * 4
+    assert ws(3, 2, 128, 33, 16) == 3 * 2 * 2 * (128 + 4) * 4  # two 512-token splits at d = 128
+    assert ws(1, 1, 32, 129, 16) == 3 * (32 + 4) * 4  # 2064 tokens: three 1024-token splits at d = 32
     assert ws(1, 1, 48, 1, 16) == 0  # not a supported head dim
     assert ws(1, 1, 64, 1, 32) == 0
 
@@ -256,3 +259,14 @@ def test_paged_prefill_and_append_argument_checks(lib):
     assert app(n=0) == 1
     assert app(d=48) == 2 and app(ps=8) == 2
     assert app(kn=ALIGNED + 8) == 3 and app(kp=ALIGNED + 4) == 3 and app(sp=ALIGNED + 2) == 3
+
+
+def test_paged_prefill_fp8_argument_checks(lib):
+    pre = lambda **kw: lib.paged_attn_prefill_fp8(
+        kw.get("q", ALIGNED), ALIGNED, ALIGNED, kw.get("ks", 0.1), kw.get("vs", 0.1), kw.get("pt", ALIGNED), ALIGNED,
+        kw.get("ps", 16), ALIGNED, None, 2, 4, kw.get("Hkv", 2), kw.get("n", 64), kw.get("d", 128), 4, 8, 1, 0.1, None)
+    assert pre(pt=None) == 1
+    assert pre(ks=0.0) == 1 and pre(vs=float("nan")) == 1 and pre(ks=-1.0) == 1
+    assert pre(Hkv=3) == 1 and pre(n=0) == 1
+    assert pre(ps=32) == 2 and pre(d=48) == 2
+    assert pre(q=ALIGNED + 4) == 3

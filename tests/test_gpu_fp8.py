@@ -162,3 +162,74 @@ def test_fp8_gqa_decode_query_beyond_fp16_range(lib, oracle_mod):
     assert np.isfinite(og).all()
     assert np.abs(og - o_ref).max() <= O_MAX and np.abs(og - o_ref).mean() <= O_MEAN
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
+
+
+# ----------------------------------------------------------------------------- chunked prefill over e4m3
+
+PREFILL_FP8_CASES = [
+    # (name, B, H, Hkv, d, Nq, ctx lengths, causal)
+    ("d128 GQA causal ragged", 3, 8, 2, 128, 200, [200, 777, 345], True),
+    ("d128 MHA non-causal", 2, 2, 2, 128, 64, [64, 1500], False),
+    ("d64 MQA causal", 2, 4, 1, 64, 130, [1000, 130], True),
+    ("d32 causal short", 4, 4, 2, 32, 17, [17, 33, 300, 2049], True),
+    ("d80 GQA causal", 2, 6, 3, 80, 150, [600, 150], True),
+    ("d96 causal Nq>ctx (rows without keys)", 2, 4, 4, 96, 100, [60, 400], True),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_FP8_CASES, ids=[c[0] for c in PREFILL_FP8_CASES])
+def test_paged_prefill_fp8_vs_oracle(lib, oracle_mod, case):
+    name, B, H, Hkv, d, Nq, ctx, causal = case
+    shape = workloads.DecodeShape(name, B, H, d, (1, max(ctx)), seed=750 + len(name))
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
+    g = torch.Generator().manual_seed(751)
+    q = torch.randn(B, H, Nq, d, generator=g).to(torch.bfloat16)
+    dv = {k: v.cuda() for k, v in inp.items()}
+    ks, vs = KV_SCALE, 2 * KV_SCALE
+    kc = lib.kv_quantize_fp8(dv["k_pages"], ks)
+    vc = lib.kv_quantize_fp8(dv["v_pages"], vs)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), device="cuda")
+    lib.paged_attn_prefill_fp8(q.cuda(), kc, vc, ks, vs, dv["page_table"], dv["ctx_lens"], causal, shape.scale,
+                               out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_prefill_fp8_gqa(q, kc.cpu(), vc.cpu(), ks, vs, inp["page_table"],
+                                                      inp["ctx_lens"], causal, shape.scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    err = np.abs(og - o_ref)
+    assert np.isfinite(og).all() and err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    lg = lse.cpu().numpy().astype(np.float64)
+    inf = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lg), inf)
+    assert np.abs(lg[~inf] - lse_ref[~inf]).max() <= LSE_MAX
+    assert not og[inf].any()
+
+
+def test_append_fp8_then_paged_prefill_fp8_with_unmapped_pages(lib, oracle_mod):
+    # a serving step over an e4m3 cache: append the chunk's K/V (converted), then attend; one page
+    # of the table is unmapped (its positions hold no token), as on every paged entry point
+    B, H, Hkv, d, Nq, old = 2, 8, 2, 128, 96, [700, 40]
+    ctx = [o + Nq for o in old]
+    shape = workloads.DecodeShape("fp8 step", B, H, d, (1, max(ctx)), seed=760)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
+    inp["page_table"][0, 5] = -1
+    g = torch.Generator().manual_seed(761)
+    q = torch.randn(B, H, Nq, d, generator=g).to(torch.bfloat16)
+    kn = torch.randn(B, Hkv, Nq, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Hkv, Nq, d, generator=g).to(torch.bfloat16)
+    dv = {k: v.cuda() for k, v in inp.items()}
+    ks, vs = KV_SCALE, KV_SCALE
+    kc = lib.kv_quantize_fp8(dv["k_pages"], ks)
+    vc = lib.kv_quantize_fp8(dv["v_pages"], vs)
+    lib.paged_kv_append_fp8(kn.cuda(), vn.cuda(), kc, vc, ks, vs, dv["page_table"],
+                            torch.tensor(old, dtype=torch.int32).cuda())
+    o, lse = lib.paged_attn_prefill_fp8(q.cuda(), kc, vc, ks, vs, dv["page_table"], dv["ctx_lens"], True,
+                                        shape.scale)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_prefill_fp8_gqa(q, kc.cpu(), vc.cpu(), ks, vs, inp["page_table"],
+                                                      inp["ctx_lens"], True, shape.scale, skip_bad_pages=True)
+    err = np.abs(o.float().cpu().numpy() - o_ref)
+    assert err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX

@@ -213,9 +213,10 @@ SMALL_DECODE = [
     (workloads.DecodeShape("multi-chunk contexts", 4, 2, 128, (1, 2000), seed=42), [512, 513, 2000, 1023]),
     (workloads.DecodeShape("empty context", 3, 2, 128, (1, 100), seed=43), [0, 100, 1]),
     (workloads.DecodeShape("drawn lengths", 6, 4, 128, (512, 4096), seed=44), None),
-    # more 512-token chunks than the merge keeps weights for in shared memory (256) and than it
-    # has threads (64 / 128): the merge's strided loops and its recomputed-weight path
-    (workloads.DecodeShape("over 256 chunks d64", 2, 2, 64, (1, 140000), seed=46), [140000, 131073]),
+    # more chunks (1024 tokens at d = 64, 512 at d = 128) than the merge keeps weights for in
+    # shared memory (256) and than it has threads (64 / 128): the merge's strided loops and its
+    # recomputed-weight path
+    (workloads.DecodeShape("over 256 chunks d64", 2, 2, 64, (1, 280000), seed=46), [280000, 262145]),
     (workloads.DecodeShape("over 256 chunks d128", 1, 1, 128, (1, 131585), seed=47), [131585]),
 ]
 
