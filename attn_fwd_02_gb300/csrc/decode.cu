@@ -7,7 +7,7 @@
 // is read once and used for two FMAs.
 //
 // Pass 1 (decode_split_kernel): grid (splits, H, B).  A CTA owns one chunk of
-// kDecodeChunkTokens tokens of one (sequence, head).  Each of its 4 warps owns
+// tokens (512 at d = 128, 1024 at smaller d) of one (sequence, head).  Each of its 4 warps owns
 // every 4th page of the chunk and streams those pages through a private ring of
 // shared-memory slots with cp.async.bulk (one 1-D bulk copy per page per K/V:
 // a page of one head is a contiguous page_size x d block), so each SM keeps
@@ -56,10 +56,18 @@ constexpr int kPS = 16;    // page size (tokens)
 // x 8 key/value heads (4 query heads each), contexts U[512, 8192]: 512 tokens 5.84-5.90 TB/s,
 // 1024 5.97, 2048 5.78-5.81 (too few CTAs for an even last wave).
 constexpr int kGqaChunkTokens = 2 * kDecodeChunkTokens;
+// Tokens per split of the multi-head kernel by head dim: kDecodeChunkTokens at d = 128, 1024 at
+// smaller d, so that each CTA streams more bytes and its start (page-table read, first loads) is
+// spread over more of them.  Measured on 32 sequences x 32 heads, contexts U[512, 8192] (fraction
+// of HBM at 512 / 1024 / 2048 tokens): d = 32 0.754 / 0.749 / 0.704, d = 64 0.941 / 0.948 / 0.926,
+// d = 80 0.845 / 0.881 / 0.879, d = 96 0.988 / 0.993 / 0.988.  At most 32 pages per warp (one id
+// per lane).
+constexpr int mha_chunk_tokens(int d) { return d >= 128 ? kDecodeChunkTokens : 1024; }
+static_assert(1024 <= 32 * 4 * 16 && kGqaChunkTokens <= 32 * 4 * 16, "one page id per lane");
 // Tokens per split for H query heads over Hkv cache heads: groups of two or more query heads run
-// the grouped-query kernel and its longer splits.
-__host__ __device__ constexpr int decode_chunk_tokens(int H, int Hkv) {
-    return (H / Hkv) % 2 == 0 ? kGqaChunkTokens : kDecodeChunkTokens;
+// the grouped-query kernel and its 1024-token splits.
+constexpr int decode_chunk_tokens(int H, int Hkv, int d) {
+    return (H / Hkv) % 2 == 0 ? kGqaChunkTokens : mha_chunk_tokens(d);
 }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -245,7 +253,7 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
 // Grid (chunks, Hkv * gsplit, B): blockIdx.y = kv_head * gsplit + group slice.
 template <int D, int GP, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeArgs a, int max_splits, int Hkv,
-                                                                   int gsplit) {
+                                                                   int gsplit, int chunk) {
     using LD = LaneDims<D>;
     constexpr int DPL = LD::DPL;  // head dims per lane
     constexpr int kElem = FP8 ? 1 : 2;
@@ -261,12 +269,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cap = a.max_pages * kPS;
     const int ctx = min(max(a.ctx_lens[b], 0), cap);
-    const int tok0 = split * kDecodeChunkTokens;
+    const int tok0 = split * chunk;
     if (tok0 >= ctx) return;  // uniform over the CTA: this chunk is empty
-    const int tok1 = min(ctx, tok0 + kDecodeChunkTokens);
+    const int tok1 = min(ctx, tok0 + chunk);
     const int page0 = tok0 / kPS;
-    const int npages = (tok1 - tok0 + kPS - 1) / kPS;  // <= kDecodeChunkTokens / kPS = 32
-    const int nk = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;  // pages of this warp (<= 8)
+    const int npages = (tok1 - tok0 + kPS - 1) / kPS;  // <= chunk / kPS <= 128
+    const int nk = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;  // pages of this warp (<= 32)
 
     if (threadIdx.x == 0) {
         for (int w = 0; w < kWarps; ++w)
@@ -467,11 +475,31 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
 // An e4m3 cache takes the same path: each warp widens its fp8 page block into a bf16 staging tile
 // in the same swizzled layout (exact: every e4m3 value is a bf16 value), the key scale folds into
 // the score scale and the value scale into the partial O.
+// Ring slots per warp of the grouped-query kernel: the page loads in flight per warp.  Measured
+// on 32 sequences x 8 cache heads (4 query heads each), contexts U[512, 8192], fraction of HBM:
+// bf16 pages 1 / 2 / 3 slots 0.853 / 0.880 / 0.844; e4m3 pages 2 / 3 / 4 / 5 slots 0.42 / 0.36 /
+// 0.37 / 0.25.  More pages in flight do not help the e4m3 form: it is bound by the work per page
+// (widening, two products, the softmax), not by the bytes in flight.
+template <bool FP8> constexpr int kGqaSlots = 2;
+
 template <int D, int GP, bool FP8>
 struct GqaMmaSmem {
-    DecodeSmem<D, GP, FP8> s;
+    // The page ring and the final merge's arrays are never in use at the same time (the merge
+    // starts after every warp has consumed its last page), so they share their bytes.
+    union {
+        // [warp][slot][0 = K, 1 = V][one page block]: swizzled TMA boxes (bf16) or the bulk-copied
+        // e4m3 block; 1024-byte aligned for the swizzled boxes
+        alignas(1024) uint8_t kv[kWarps][kGqaSlots<FP8>][2][kSlotBytes<D, GP, FP8>];
+        struct {
+            float o[kWarps][GP][D];
+            float m[kWarps][GP];
+            float l[kWarps][GP];
+        } red;
+    } u;
+    uint64_t full[kWarps][kGqaSlots<FP8>];
     // bf16 K, V of one page in the swizzled box layout (kBoxes<D> boxes of 16 x 64)
     alignas(128) __nv_bfloat16 stage[FP8 ? kWarps : 1][2][FP8 ? kBoxes<D> * kPS * 64 : 8];
+    int abort_flag;
 };
 
 // 16 e4m3 codes (one 16-byte chunk of a page row) -> 16 bf16 values, two 16-byte chunks.
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                                                                      int gsplit) {
     static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
     static_assert(D % 16 == 0, "k-steps of 16");
-    constexpr int kSl = kSlotsFor<FP8, GP>;
+    constexpr int kSl = kGqaSlots<FP8>;
     constexpr uint32_t kBlockBytes = kPS * D * (FP8 ? 1 : 2);   // bytes of a page block in HBM
     constexpr uint32_t kBoxBytesAll = kBoxes<D> * kPS * 128;     // a block's TMA boxes (zero-filled past D)
     constexpr int KS = D / 16;  // k-steps of S = Q K^T
@@ -504,9 +532,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     constexpr float kThresh = 8.0f;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // the swizzled boxes need 1024-byte alignment
-    GqaMmaSmem<D, GP, FP8> &smx =
+    GqaMmaSmem<D, GP, FP8> &sm =
         *reinterpret_cast<GqaMmaSmem<D, GP, FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    DecodeSmem<D, GP, FP8> &sm = smx.s;
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int kvh = (int)blockIdx.y / gsplit;
@@ -548,14 +575,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 const int row = pid * Hkv + kvh;  // page block in the pool viewed as [num_pages * Hkv, 16, D]
                 if constexpr (FP8) {
                     mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
-                    bulk_load(sm.kv[warp][k % kSl][0], kbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
-                    bulk_load(sm.kv[warp][k % kSl][1], vbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
+                    bulk_load(sm.u.kv[warp][k % kSl][0], kbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
+                    bulk_load(sm.u.kv[warp][k % kSl][1], vbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
                 } else {
                     mbar_arrive_expect_tx(bar, 2 * kBoxBytesAll);
 #pragma unroll
                     for (int i = 0; i < kBoxes<D>; ++i) {
-                        tma_load_3d(sm.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
-                        tma_load_3d(sm.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
+                        tma_load_3d(sm.u.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
+                        tma_load_3d(sm.u.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
                     }
                 }
             } else {
@@ -603,23 +630,23 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
         const int ntok = min(kPS, tok1 - page_tok0);
         if (ok) {
-            uint32_t Ks = smem_u32(sm.kv[warp][slot][0]);
-            uint32_t Vs = smem_u32(sm.kv[warp][slot][1]);
+            uint32_t Ks = smem_u32(sm.u.kv[warp][slot][0]);
+            uint32_t Vs = smem_u32(sm.u.kv[warp][slot][1]);
             if constexpr (FP8) {
                 // widen the e4m3 block into this warp's bf16 staging tiles (swizzled as the TMA boxes);
                 // V rows past the context end are written as zeros
-                uint8_t *stK = reinterpret_cast<uint8_t *>(smx.stage[warp][0]);
-                uint8_t *stV = reinterpret_cast<uint8_t *>(smx.stage[warp][1]);
+                uint8_t *stK = reinterpret_cast<uint8_t *>(sm.stage[warp][0]);
+                uint8_t *stV = reinterpret_cast<uint8_t *>(sm.stage[warp][1]);
                 constexpr int kChunks = kPS * D / 16;  // 16-byte chunks of fp8 per block
 #pragma unroll
                 for (int i = lane; i < kChunks; i += 32) {
                     const int r = i / (D / 16), c0 = (i % (D / 16)) * 16;
                     uint4 lo, hi;
-                    e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.kv[warp][slot][0])[i], lo, hi);
+                    e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.u.kv[warp][slot][0])[i], lo, hi);
                     *reinterpret_cast<uint4 *>(stK + swz_off(r, c0)) = lo;
                     *reinterpret_cast<uint4 *>(stK + swz_off(r, c0 + 8)) = hi;
                     if (r < ntok) {
-                        e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.kv[warp][slot][1])[i], lo, hi);
+                        e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.u.kv[warp][slot][1])[i], lo, hi);
                     } else {
                         lo = hi = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -634,7 +661,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 const int per_box = (kPS - ntok) * 8;  // 16-byte chunks of the dead rows of one box
                 for (int i = lane; i < per_box * kBoxes<D>; i += 32) {
                     const int box = i / per_box, j = i % per_box;
-                    *reinterpret_cast<uint4 *>(sm.kv[warp][slot][1] + box * (16 * 128) + ntok * 128 + j * 16) =
+                    *reinterpret_cast<uint4 *>(sm.u.kv[warp][slot][1] + box * (16 * 128) + ntok * 128 + j * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
@@ -723,19 +750,21 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         __syncwarp();
     }
 
-    // this warp's state of each query head -> shared memory, then the merge of the kernel above
+    // this warp's state of each query head -> shared memory (over the ring, once every warp is
+    // done with its pages), then the merge of the kernel above
+    __syncthreads();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int g = r0 + 8 * h;
         if (g < GP) {
             if ((lane & 3) == 0) {
-                sm.red_m[warp][g] = m_ref[h];
-                sm.red_l[warp][g] = l_run[h];
+                sm.u.red.m[warp][g] = m_ref[h];
+                sm.u.red.l[warp][g] = l_run[h];
             }
 #pragma unroll
             for (int nd = 0; nd < NT; ++nd) {
-                sm.red_o[warp][g][nd * 8 + kq] = o[nd][2 * h];
-                sm.red_o[warp][g][nd * 8 + kq + 1] = o[nd][2 * h + 1];
+                sm.u.red.o[warp][g][nd * 8 + kq] = o[nd][2 * h];
+                sm.u.red.o[warp][g][nd * 8 + kq + 1] = o[nd][2 * h + 1];
             }
         }
     }
@@ -745,14 +774,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         const int g = e / D, dd = e % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w][g]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.u.red.m[w][g]);
         float L = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const float wgt = ex2_approx(sm.red_m[w][g] - M);
-                L += sm.red_l[w][g] * wgt;
-                O += sm.red_o[w][g][dd] * wgt;
+                const float wgt = ex2_approx(sm.u.red.m[w][g] - M);
+                L += sm.u.red.l[w][g] * wgt;
+                O += sm.u.red.o[w][g][dd] * wgt;
             }
         }
         float *ws = reinterpret_cast<float *>(a.workspace) +
@@ -834,14 +863,14 @@ __global__ void __launch_bounds__(kCombineThreads<D>) decode_combine_kernel(cons
 }
 
 template <int D, int GP, bool FP8>
-cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
+cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, int chunk, cudaStream_t stream) {
     const size_t smem = sizeof(DecodeSmem<D, GP, FP8>);
     cudaError_t e =
         ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_split_kernel<D, GP, FP8>), (int)smem);
     if (e != cudaSuccess) return e;
     const int gsplit = (a.H / a.Hkv) / GP;  // CTAs per key/value head
     dim3 g1(max_splits, a.Hkv * gsplit, a.B);
-    decode_split_kernel<D, GP, FP8><<<g1, kWarps * 32, smem, stream>>>(a, max_splits, a.Hkv, gsplit);
+    decode_split_kernel<D, GP, FP8><<<g1, kWarps * 32, smem, stream>>>(a, max_splits, a.Hkv, gsplit, chunk);
     return cudaGetLastError();
 }
 
@@ -864,13 +893,13 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t 
 }
 
 template <int D, int GP>
-cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
+cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, int chunk, cudaStream_t stream) {
     if constexpr (GP >= 2) {
         return a.kv_fp8 ? launch_decode_mma<D, GP, true>(a, max_splits, stream)
                         : launch_decode_mma<D, GP, false>(a, max_splits, stream);
     } else {
-        return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, stream)
-                        : launch_decode_g<D, GP, false>(a, max_splits, stream);
+        return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, chunk, stream)
+                        : launch_decode_g<D, GP, false>(a, max_splits, chunk, stream);
     }
 }
 
@@ -879,13 +908,13 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t stream) {
     // query heads per CTA: the largest of 8, 4, 2, 1 dividing the group size; groups of two or more
     // run the grouped-query kernel and its longer chunks
     const int group = a.H / a.Hkv;
-    const int chunk = decode_chunk_tokens(a.H, a.Hkv);
+    const int chunk = decode_chunk_tokens(a.H, a.Hkv, D);
     const int max_splits = (a.max_pages * kPS + chunk - 1) / chunk;
     cudaError_t e;
-    if (group % 8 == 0) e = launch_decode_gk<D, 8>(a, max_splits, stream);
-    else if (group % 4 == 0) e = launch_decode_gk<D, 4>(a, max_splits, stream);
-    else if (group % 2 == 0) e = launch_decode_gk<D, 2>(a, max_splits, stream);
-    else e = launch_decode_gk<D, 1>(a, max_splits, stream);
+    if (group % 8 == 0) e = launch_decode_gk<D, 8>(a, max_splits, chunk, stream);
+    else if (group % 4 == 0) e = launch_decode_gk<D, 4>(a, max_splits, chunk, stream);
+    else if (group % 2 == 0) e = launch_decode_gk<D, 2>(a, max_splits, chunk, stream);
+    else e = launch_decode_gk<D, 1>(a, max_splits, chunk, stream);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.H, a.B);
@@ -908,7 +937,7 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int d, int max_pages, int p
     if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || max_pages <= 0 || page_size != kPS ||
         (d != 32 && d != 64 && d != 80 && d != 96 && d != 128))
         return 0;
-    const size_t chunk = (size_t)decode_chunk_tokens(H, Hkv);
+    const size_t chunk = (size_t)decode_chunk_tokens(H, Hkv, d);
     const size_t max_splits = ((size_t)max_pages * kPS + chunk - 1) / chunk;
     return (size_t)B * H * max_splits * (size_t)(d + 4) * sizeof(float);
 }

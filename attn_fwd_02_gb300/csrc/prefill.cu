@@ -67,18 +67,23 @@ template <int P> struct CfgPad;
 template <int D> struct Cfg : CfgPad<kPad<D>> {};
 template <> struct CfgPad<128> {
     static constexpr int QT = 2, BN = 128, kThreads = 384, kProducerWarp = 8, kMmaWarp = 9, kMinBlocks = 1;
+    static constexpr int kStages = 2;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr bool kSplitRegs = true;
     static constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 64;
 };
 template <> struct CfgPad<64> {
-    static constexpr int QT = 1, BN = 64, kThreads = 256, kProducerWarp = 4, kMmaWarp = 5, kMinBlocks = 4;
+    static constexpr int QT = 1, BN = 64, kThreads = 256, kProducerWarp = 4, kMmaWarp = 5;
+    static constexpr int kMinBlocks = 4, kStages = 2;
     static constexpr uint32_t kTmemCols = 128;
     static constexpr bool kSplitRegs = true;
-    static constexpr uint32_t kRegsSoftmax = 96, kRegsOther = 32;
+    // launch allocation of kMinBlocks CTAs per SM, and its split over the two warpgroups
+    static constexpr uint32_t kRegsLaunch = (65536 / (256 * kMinBlocks)) / 8 * 8;
+    static constexpr uint32_t kRegsOther = kMinBlocks >= 4 ? 32 : (kMinBlocks == 3 ? 48 : 64);
+    static constexpr uint32_t kRegsSoftmax = 2 * kRegsLaunch - kRegsOther;
 };
 static_assert(128 * (Cfg<128>::kRegsOther + 2 * Cfg<128>::kRegsSoftmax) <= 384 * 168, "d=128 register split");
-static_assert(128 * (Cfg<64>::kRegsOther + Cfg<64>::kRegsSoftmax) <= 256 * 64, "d=64 register split");
+static_assert(128 * (Cfg<64>::kRegsOther + Cfg<64>::kRegsSoftmax) <= 256 * Cfg<64>::kRegsLaunch, "d=64 register split");
 static_assert(Cfg<64>::QT * (Cfg<64>::BN + 64) <= (int)Cfg<64>::kTmemCols, "d=64 TMEM layout");
 static_assert(Cfg<128>::QT * (128 + 128) <= (int)Cfg<128>::kTmemCols, "d=128 TMEM layout");
 // keys per tile
@@ -116,10 +121,10 @@ struct PrefillParams {
 
 // K/V ring.  Step j of the MMA issuer (PV(j) then S(j+1)) needs V(j) and K(j+1) together,
 // so they travel as one ring unit: unit u = {K(u), V(u-1)} (unit 0 has only K(0), unit n only
-// V(n-1)); K(j) sits in slot j % kStages, V(j) in slot (j+1) % kStages.  One full and one
-// empty barrier per unit keeps the single MMA-issuing thread's synchronisation per step at
-// one wait and one commit for the ring.
-constexpr int kStages = 2;
+// V(n-1)); with S = kStagesOf<D> slots, K(j) sits in slot j % S, V(j) in slot (j+1) % S.  One
+// full and one empty barrier per unit keeps the single MMA-issuing thread's synchronisation per
+// step at one wait and one commit for the ring.
+template <int D> constexpr int kStagesOf = Cfg<D>::kStages;
 
 // e4m3 pages: one K tile and one V tile of codes, staged page block by page block (16 rows of d
 // bytes each) before the converter warps widen them into the bf16 ring.
@@ -137,11 +142,11 @@ struct alignas(1024) PrefillSmem {
     // q, k, v: tiles of kBM x kPad elements back to back (the MMA issuer steps between them by
     // a constant)
     __nv_bfloat16 q[Cfg<D>::QT][kBM * kPad<D>];  // kPad/64 boxes each
-    __nv_bfloat16 k[kStages][kBNd<D> * kPad<D>];  // kPad/64 boxes each
-    __nv_bfloat16 v[kStages][kBNd<D> * kPad<D>];  // kPad/64 boxes each
+    __nv_bfloat16 k[kStagesOf<D>][kBNd<D> * kPad<D>];  // kPad/64 boxes each
+    __nv_bfloat16 v[kStagesOf<D>][kBNd<D> * kPad<D>];  // kPad/64 boxes each
     KvStage<D, M> st;
     uint64_t q_full;
-    uint64_t u_full[kStages], u_empty[kStages];
+    uint64_t u_full[kStagesOf<D>], u_empty[kStagesOf<D>];
     uint64_t s_full[kQTilesMax];
     uint64_t p_full[kQTilesMax];
     uint64_t o_done[kQTilesMax];
@@ -172,22 +177,57 @@ __device__ __forceinline__ int tiles_for(const PrefillParams &p, int qs, int kv_
 }
 
 // ------------------------------------------------------------------ producer
+// Contiguous K/V: the loads that need no ring wait -- Q and the first kStages units -- issued by
+// the producer thread before the CTA's start-up barrier, so they overlap the TMEM allocation and
+// the other warps' start (at d = 64 this took the start of a CTA from about 5000 to 4200 cycles
+// and the decoder workload's span from 28.4 to 25.1 us in a timestamped copy).  Returns the first
+// unit left for run_producer.
 template <int D, int M>
-__device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
-                             const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int bh, int bh_kv, int q0,
-                             int n_all, WaitCtx wc) {
+__device__ int producer_start(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
+                              const CUtensorMap *tmK, const CUtensorMap *tmV, int bh, int bh_kv, int q0, int n_all) {
+    static_assert(M == kContig, "contiguous K/V only");
     constexpr int kBoxes = kPad<D> / 64;
+    constexpr int kBN = kBNd<D>;
     prefetch_tensormap(tmQ);
-    if constexpr (M != kPagedE4m3) {
-        prefetch_tensormap(tmK);
-        prefetch_tensormap(tmV);
-    }
+    prefetch_tensormap(tmK);
+    prefetch_tensormap(tmV);
     mbar_arrive_expect_tx(&sm.q_full, Cfg<D>::QT * kBoxes * kBoxBytes);
 #pragma unroll
     for (int t = 0; t < Cfg<D>::QT; ++t)
 #pragma unroll
         for (int i = 0; i < kBoxes; ++i)
             tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
+    const int first = n_all + 1 < kStagesOf<D> ? n_all + 1 : kStagesOf<D>;
+    for (int u = 0; u < first; ++u) {
+        const bool has_k = u < n_all, has_v = u > 0;
+        mbar_arrive_expect_tx(&sm.u_full[u], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kKvBoxBytes<D>);
+#pragma unroll
+        for (int i = 0; i < kBoxes; ++i) {
+            if (has_k) tma_load_3d(sm.k[u] + i * (kBN * 64), tmK, &sm.u_full[u], i * 64, u * kBN, bh_kv);
+            if (has_v) tma_load_3d(sm.v[u] + i * (kBN * 64), tmV, &sm.u_full[u], i * 64, (u - 1) * kBN, bh_kv);
+        }
+    }
+    return first;
+}
+
+template <int D, int M>
+__device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmQ,
+                             const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int bh, int bh_kv, int q0,
+                             int n_all, int u_begin, WaitCtx wc) {
+    constexpr int kBoxes = kPad<D> / 64;
+    if (u_begin == 0) {  // Q not yet issued (paged modes)
+        prefetch_tensormap(tmQ);
+        if constexpr (M != kPagedE4m3) {
+            prefetch_tensormap(tmK);
+            prefetch_tensormap(tmV);
+        }
+        mbar_arrive_expect_tx(&sm.q_full, Cfg<D>::QT * kBoxes * kBoxBytes);
+#pragma unroll
+        for (int t = 0; t < Cfg<D>::QT; ++t)
+#pragma unroll
+            for (int i = 0; i < kBoxes; ++i)
+                tma_load_3d(sm.q[t] + i * (kBM * 64), tmQ, &sm.q_full, i * 64, q0 + t * kBM, bh);
+    }
     // paged modes: the page ids of each tile (-1 past the sequence's last page), fetched one
     // ring unit ahead of their use, so the global loads stay in flight across the ring wait
     constexpr int kBN = kBNd<D>;
@@ -271,9 +311,9 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
                 tma_load_3d(dst + i * (kBN * 64) + pg * (kPageTokens * 64), map, bar, i * 64, 0, row);
         }
     };
-    int fills = 0;
-    for (int u = 0; u <= n_all; ++u) {
-        const int slot = u % kStages, use = u / kStages;
+    int fills = u_begin;
+    for (int u = u_begin; u <= n_all; ++u) {
+        const int slot = u % kStagesOf<D>, use = u / kStagesOf<D>;
         if (use > 0 && !mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 1)) break;
         const bool has_k = u < n_all, has_v = u > 0;
         mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kKvBoxBytes<D>);
@@ -308,17 +348,17 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
         // unwinding: let every copy still in flight land before the CTA exits
         WaitCtx drain{nullptr, wc.status};
         (void)mbar_wait(&sm.q_full, 0, drain, 90);
-        for (int f = (fills > kStages ? fills - kStages : 0); f < fills; ++f)
-            (void)mbar_wait(&sm.u_full[f % kStages], (uint32_t)((f / kStages) & 1), drain, 91);
+        for (int f = (fills > kStagesOf<D> ? fills - kStagesOf<D> : 0); f < fills; ++f)
+            (void)mbar_wait(&sm.u_full[f % kStagesOf<D>], (uint32_t)((f / kStagesOf<D>) & 1), drain, 91);
     }
 }
 
 // ------------------------------------------------------------------ e4m3 converters
-// Two warps widen each staged e4m3 tile into its bf16 ring slot, in the layout a TMA load with the
-// 128-byte swizzle gives (16-byte chunk c of row r of a 64-column box at chunk c ^ (r % 8)), so the
-// MMA issuer reads it exactly as a bf16 tile.  Each e4m3 value is a bf16 value (the widening is
-// exact); the tensor scales fold elsewhere (the key scale into the score scale, the value scale
-// into the epilogue).  Rows of pages that were not loaded become zeros.  A ring unit {K(u), V(u-1)}
+// Two warps widen each staged e4m3 tile into its ring slot (keys to bf16, values to f16), in the
+// layout a TMA load with the 128-byte swizzle gives (16-byte chunk c of row r of a 64-column box at
+// chunk c ^ (r % 8)), so the MMA issuer reads it exactly as a loaded tile.  Each e4m3 value is a
+// bf16 and an f16 value (the widening is exact); the tensor scales fold elsewhere (the key scale
+// into the score scale, the value scale into the epilogue).  Rows of pages that were not loaded become zeros.  A ring unit {K(u), V(u-1)}
 // is complete when both are written: the converters fence their shared-memory writes for the async
 // proxy, meet at a named barrier, and one of them arrives on the unit's full barrier.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
@@ -327,7 +367,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
     return pack_bf16x2(f.x, f.y);
 }
 
-template <int D>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Widens one staged e4m3 tile into a ring slot: bf16 (keys: the type of Q) or f16 (values: the
+// type P is packed in).  Both are exact: every e4m3 value is a bf16 and an f16 value.
+template <int D, bool F16>
 __device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, __nv_bfloat16 *dst, int ct) {
     constexpr int kBN = kBNd<D>;
     constexpr int kChunksPerRow = D / 16;  // 16-byte chunks of e4m3 per row
@@ -338,10 +385,17 @@ __device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, 
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         if ((loaded >> (r / kPageTokens)) & 1u) {
             const uint4 v = *reinterpret_cast<const uint4 *>(src + r * D + c16 * 16);
-            lo = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
-                            e4m3x2_to_bf16x2(v.y >> 16));
-            hi = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
-                            e4m3x2_to_bf16x2(v.w >> 16));
+            if constexpr (F16) {
+                lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                                e4m3x2_to_f16x2(v.y >> 16));
+                hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                                e4m3x2_to_f16x2(v.w >> 16));
+            } else {
+                lo = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
+                                e4m3x2_to_bf16x2(v.y >> 16));
+                hi = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
+                                e4m3x2_to_bf16x2(v.w >> 16));
+            }
         }
         const int col = c16 * 16;               // first of the 16 columns
         const int box = col >> 6, k0 = (col & 63) >> 3;  // 16-byte chunks k0, k0 + 1 of the row
@@ -364,7 +418,7 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
     bool ok = true;
     int kf = 0, vf = 0;
     for (int u = 0; u <= n_all && ok; ++u) {
-        const int slot = u % kStages, use = u / kStages;
+        const int slot = u % kStagesOf<D>, use = u / kStagesOf<D>;
         if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 4))) {
             ok = false;
             break;
@@ -374,7 +428,7 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
                 ok = false;
                 break;
             }
-            widen_tile<D>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
+            widen_tile<D, false>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
             if (!(ok = sync_converters())) break;
             if (ct == 0) mbar_arrive(&sm.st.k_empty);
             ++kf;
@@ -384,7 +438,7 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
                 ok = false;
                 break;
             }
-            widen_tile<D>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
+            widen_tile<D, true>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
             ++vf;
         }
         fence_proxy_async_smem();  // this thread's tile writes, before the MMA's reads
@@ -401,8 +455,11 @@ template <int D, int M>
 __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
     constexpr int kBN = kBNd<D>;
     constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
-    constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
-    static_assert(kStages == 2, "slot selects below");
+    // e4m3 pages: V is widened to f16 and P packed as f16, so PV runs f16 x f16 (the key tile
+    // stays bf16, the type of Q)
+    constexpr uint32_t idPV =
+        M == kPagedE4m3 ? idesc_f16_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
+
     // Descriptors of the operand buffers, built once (the Q tiles, the K tiles and the V tiles
     // are each equally spaced: kQTile and kKvTile descriptor units); each MMA advances one by a
     // constant.
@@ -418,7 +475,7 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
     static_assert(kPad<D> == 64 || kBN * 128 == 16384, "k-step layout of the grouped issue");
     auto issue_S = [&](int t, int j) {
         const uint64_t a = dq + (t ? kQTile : 0);
-        const uint64_t b = dk + ((j & 1) ? kKvTile : 0);  // K(j) sits in slot j % 2
+        const uint64_t b = dk + (uint64_t)(j % kStagesOf<D>) * kKvTile;  // K(j) sits in slot j % S
         const uint32_t tS = tmem + (uint32_t)(t * kBN);
         tc_mma_ss_ksteps<D / 16>(tS, a, b, idS, 0u);
         tc_commit(&sm.s_full[t]);
@@ -426,7 +483,7 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
     // O_t += P_t V_j  (A = P_t from TMEM, 8 columns per 16 keys; B = V_j MN-major, 16 keys = 2048 B)
     static_assert(kBN == 128 || kBN == 64, "PV is one group of eight or four k-steps");
     auto issue_PV = [&](int t, int j) {
-        const uint64_t b = dv + ((j & 1) ? 0 : kKvTile);  // V(j) sits in slot (j + 1) % 2
+        const uint64_t b = dv + (uint64_t)((j + 1) % kStagesOf<D>) * kKvTile;  // V(j) sits in slot (j + 1) % S
         const uint32_t tP = tmem + p_col<D>(t);
         const uint32_t tO = tmem + o_col<D>(t);
         if constexpr (kBN == 128) tc_mma_ts_k8(tO, tP, b, idPV, j > 0 ? 1u : 0u);
@@ -444,7 +501,7 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
         tc_commit(&sm.u_empty[0]);
         for (int j = 0; j < n_all && ok; ++j) {
             const int u = j + 1;  // unit with V(j) and K(j+1)
-            ok = mbar_wait(&sm.u_full[u % kStages], (uint32_t)((u / kStages) & 1), wc, 13);
+            ok = mbar_wait(&sm.u_full[u % kStagesOf<D>], (uint32_t)((u / kStagesOf<D>) & 1), wc, 13);
             if (!ok) break;
             // P over S: PV_t(j) must be issued before S_t(j+1) overwrites its buffer
             for (int t = 0; t < Cfg<D>::QT; ++t) {
@@ -457,7 +514,7 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
                 if (j + 1 < n[t]) issue_S(t, j + 1);
             }
             if (!ok) break;
-            tc_commit(&sm.u_empty[u % kStages]);
+            tc_commit(&sm.u_empty[u % kStagesOf<D>]);
         }
     }
     // wait (bounded) until every MMA issued above has finished with TMEM and smem
@@ -521,7 +578,8 @@ __device__ __forceinline__ float max64(const uint32_t (&s)[2][32]) {
 }
 
 // p = 2^(s*c - m) for 64 scores (two per packed FMA), summed into rs2 and stored to TMEM
-// as 32 columns of bf16 pairs starting at tP.
+// as 32 columns of bf16 pairs (f16 pairs when F16P) starting at tP.
+template <bool F16P = false>
 __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t tP, uint64_t c2, uint64_t negm2,
                                           uint64_t (&rs2)[4]) {
 #pragma unroll
@@ -536,7 +594,7 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t t
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
             rs2[(i >> 1) & 3] = f32x2_add(rs2[(i >> 1) & 3], f32x2_pack(p0, p1));
-            pk[i / 2] = pack_bf16x2(p0, p1);
+            pk[i / 2] = F16P ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
         tmem_st16(tP + cc * 16, pk);
     }
@@ -630,10 +688,11 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint3
 
         // P = 2^(s*c - m_use) as bf16 pairs (even key in the low half, as the TMEM A operand
         // expects): keys 64h .. 64h + 63 -> columns 32h .. 32h + 31, over the scores already
-        // read into registers.
+        // read into registers.  Over e4m3 pages P is packed as f16 pairs instead, the type of the
+        // widened V tile (P <= 2^8 with the lazy reference max, well inside f16's range).
         uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h) exp_store(s[h], tS + 32 * h, c2, negm2, rs2);
+        for (int h = 0; h < kHalves; ++h) exp_store<M == kPagedE4m3>(s[h], tS + 32 * h, c2, negm2, rs2);
         {
             const uint64_t t01 = f32x2_add(rs2[0], rs2[1]);
             const uint64_t t23 = f32x2_add(rs2[2], rs2[3]);
@@ -707,11 +766,14 @@ template <int D, int M> struct Occ {
     static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;
 };
 template <> struct Occ<32, kPagedE4m3> {
-    static constexpr int kMinBlocks = 3;
-    static constexpr uint32_t kRegsSoftmax = 104, kRegsOther = 56;
+    static constexpr int kMinBlocks = Cfg<32>::kMinBlocks < 3 ? Cfg<32>::kMinBlocks : 3;
+    static constexpr uint32_t kLaunch = (65536 / (256 * kMinBlocks)) / 8 * 8;
+    static constexpr uint32_t kRegsOther = kMinBlocks == 3 ? 56 : 64;
+    static constexpr uint32_t kRegsSoftmax = 2 * kLaunch - kRegsOther;
 };
 template <> struct Occ<64, kPagedE4m3> : Occ<32, kPagedE4m3> {};
-static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kRegsOther) <= 256 * 80,
+static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kRegsOther) <=
+                  256 * Occ<64, kPagedE4m3>::kLaunch,
               "e4m3 d<=64 register split");
 
 template <int D, int M>
@@ -755,9 +817,13 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
     for (int t = 0; t < Cfg<D>::QT; ++t) n[t] = tiles_for<kBNd<D>>(p, q0 + t * kBM, kv_end, delta);
     const int n_all = max(n[0], n[1]);
 
-    if (threadIdx.x == 0) {
+    // The producer thread initialises the barriers and, for contiguous K/V, issues the loads that
+    // need no ring wait before the start-up barrier.
+    const bool producer = (warp == Cfg<D>::kProducerWarp && lane == 0);
+    int u_begin = 0;
+    if (producer) {
         mbar_init(&sm.q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStagesOf<D>; ++s) {
             mbar_init(&sm.u_full[s], 1);
             mbar_init(&sm.u_empty[s], 1);
         }
@@ -776,6 +842,9 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
         }
         sm.abort_flag = 0;
         fence_mbar_init();
+        if constexpr (M == kContig) {
+            if (n_all > 0) u_begin = producer_start<D, M>(sm, p, &tmQ, &tmK, &tmV, bh, bh_kv, q0, n_all);
+        }
     }
     if (warp == Cfg<D>::kMmaWarp) {
         tmem_alloc(&sm.tmem_base, Cfg<D>::kTmemCols);
@@ -790,7 +859,8 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
     if (warp >= 4 * Cfg<D>::QT) {
         if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_dec<Occ<D, M>::kRegsOther>();
         if (warp == Cfg<D>::kProducerWarp) {
-            if (lane == 0 && n_all > 0) run_producer<D, M>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, wc);
+            if (lane == 0 && n_all > 0)
+                run_producer<D, M>(sm, p, &tmQ, &tmK, &tmV, b, bh, bh_kv, q0, n_all, u_begin, wc);
         } else if (warp == Cfg<D>::kMmaWarp) {
             if (lane == 0 && n_all > 0) run_mma<D, M>(sm, tmem, n, n_all, wc);
         } else if constexpr (M == kPagedE4m3) {
