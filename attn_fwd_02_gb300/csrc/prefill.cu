@@ -150,6 +150,7 @@ struct alignas(1024) PrefillSmem {
     uint64_t s_full[kQTilesMax];
     uint64_t p_full[kQTilesMax];
     uint64_t o_done[kQTilesMax];
+    uint64_t o_staged[kQTilesMax];  // the warpgroup's O rows are in shared memory
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -601,8 +602,8 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t t
 }
 
 template <int D, int M>
-__device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint32_t tmem, int t, int bh, int q0,
-                            int n_tiles, int kv_end, int delta, WaitCtx wc) {
+__device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmO, uint32_t tmem,
+                            int t, int bh, int q0, int n_tiles, int n_all, int kv_end, int delta, WaitCtx wc) {
     const int r = threadIdx.x & 127;  // query row in the tile = TMEM lane
     const int wq = (threadIdx.x >> 5) & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
@@ -709,16 +710,30 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint3
         mbar_arrive(&sm.p_full[t]);
     }
 
-    // epilogue: O / l -> bf16, LSE = ln2 * (m_ref + log2 l)
+    // epilogue: O / l -> bf16, LSE = ln2 * (m_ref + log2 l).  Each thread writes its row into the Q
+    // tile's shared memory, free once the tile's last product has completed (o_done; if the tile had
+    // no key, once its Q load has landed), in the 128-byte swizzled box layout of a TMA load; one
+    // thread of the warpgroup then stores the tile with TMA (rows past Nq and columns past d are not
+    // written).
     if (ok && n_tiles > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], 0, wc, 22 + t))) ok = false;
         else tc_fence_after_sync();
+    } else if (ok && n_all > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, wc, 24))) ok = false;
     }
     if (!ok) return;
     const bool have = (n_tiles > 0) && (l > 0.f);
     const float inv_l = have ? (M == kPagedE4m3 ? p.o_scale : 1.f) / l : 0.f;
-    const bool store = row < p.Nq;
-    __nv_bfloat16 *orow = p.o + ((size_t)bh * p.Nq + (store ? row : 0)) * D;
+    uint8_t *stage = reinterpret_cast<uint8_t *>(sm.q[t]) + r * 128;
+    auto put = [&](int col0, const uint32_t *pk, int nchunks) {  // 16-byte chunks from column col0
+#pragma unroll
+        for (int q = 0; q < nchunks; ++q) {
+            const int col = col0 + 8 * q;
+            const int c = (col & 63) >> 3;
+            *reinterpret_cast<uint4 *>(stage + (col >> 6) * (kBM * 128) + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+    };
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t ov[32];
@@ -726,16 +741,12 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint3
             tmem_ld32(tO + cc * 32, ov);
             tmem_wait_ld(ov);
         }
-        if (store) {
-            uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = have ? pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l)
-                             : 0u;
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < 16; ++i)
+            pk[i] = have ? pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l)
+                         : 0u;
+        put(cc * 32, pk, 4);
     }
     if constexpr (D % 32 != 0) {  // d = 80: the last 16 columns
         constexpr int c0 = D / 32 * 32;
@@ -744,18 +755,25 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, uint3
             tmem_ld16(tO + c0, ov);
             tmem_wait_ld16(ov);
         }
-        if (store) {
-            uint32_t pk[8];
+        uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                pk[i] = have ? pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l)
-                             : 0u;
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        for (int i = 0; i < 8; ++i)
+            pk[i] = have ? pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l)
+                         : 0u;
+        put(c0, pk, 2);
+    }
+    if (row < p.Nq && p.lse) p.lse[(size_t)bh * p.Nq + row] = have ? kLn2 * (m_ref + __log2f(l)) : -INFINITY;
+    fence_proxy_async_smem();  // the staged rows, before the TMA store reads them
+    mbar_arrive(&sm.o_staged[t]);
+    if (r == 0 && qs < p.Nq) {
+        if (mbar_wait(&sm.o_staged[t], 0, wc, 25 + t)) {
+#pragma unroll
+            for (int i = 0; i < kPad<D> / 64; ++i)
+                if (i * 64 < D) tma_store_3d(tmO, reinterpret_cast<const uint8_t *>(sm.q[t]) + i * (kBM * 128), i * 64, qs, bh);
+            bulk_commit_group();
+            bulk_wait_group_all();
         }
     }
-    if (store && p.lse) p.lse[(size_t)bh * p.Nq + row] = have ? kLn2 * (m_ref + __log2f(l)) : -INFINITY;
 }
 
 // CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
@@ -779,7 +797,8 @@ static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kR
 template <int D, int M>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem<D, M> &sm =
         *reinterpret_cast<PrefillSmem<D, M> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -831,6 +850,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
             mbar_init(&sm.s_full[t], 1);
             mbar_init(&sm.p_full[t], kBM);
             mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.o_staged[t], kBM);
         }
         mbar_init(&sm.drain, 1);
         if constexpr (M == kPagedE4m3) {
@@ -870,7 +890,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
     } else {
         if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<Occ<D, M>::kRegsSoftmax>();
         const int t = warp >> 2;  // warpgroup = query tile
-        run_softmax<D, M>(sm, p, tmem, t, bh, q0, n[t], kv_end, delta, wc);
+        run_softmax<D, M>(sm, p, &tmO, tmem, t, bh, q0, n[t], n_all, kv_end, delta, wc);
     }
 
     tc_fence_before_sync();
@@ -901,9 +921,9 @@ cudaError_t check_register_split() {
 
 template <int D, int M>
 cudaError_t launch_prefill_dm(const PrefillArgs &a, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const int BH = a.B * a.H, BHkv = a.B * a.Hkv;
-    bool ok_maps = encode_qkv_map(&tq, a.q, BH, a.Nq, D);
+    bool ok_maps = encode_qkv_map(&tq, a.q, BH, a.Nq, D) && encode_qkv_map(&to, a.o, BH, a.Nq, D);
     if constexpr (M == kPagedBf16)  // pages [num_pages * Hkv] of 16 x D, one 16-row box per page
         ok_maps = ok_maps && encode_qkv_map(&tk, a.k, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens) &&
                   encode_qkv_map(&tv, a.v, a.num_pages * a.Hkv, kPageTokens, D, kPageTokens);
@@ -948,7 +968,7 @@ cudaError_t launch_prefill_dm(const PrefillArgs &a, cudaStream_t stream) {
     e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<D, M>), (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)p.n_units * BH);
-    prefill_kernel<D, M><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, M><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
