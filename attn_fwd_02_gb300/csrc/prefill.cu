@@ -101,6 +101,37 @@ constexpr int kPageTokens = 16;            // tokens per page of the paged KV ca
 // pages, widened to bf16 in shared memory before the products.
 enum KvMode : int { kContig = 0, kPagedBf16 = 1, kPagedE4m3 = 2 };
 
+// CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
+// d <= 64 CTA 56 KB, so three of them share an SM, launched at 80 registers (128 x (104 + 56) =
+// 20480 = 256 x 80); the converter warps take registers from the producer's warpgroup.
+template <int D, int M> struct Occ {
+    static constexpr int kMinBlocks = Cfg<D>::kMinBlocks, kThreads = Cfg<D>::kThreads;
+    static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;
+};
+// e4m3 pages at d > 64: a fourth warpgroup widens with the third's two idle warps -- six converter
+// warps -- launched at 128 registers (512 threads); the two non-softmax warpgroups keep 40 each:
+// 128 x (2 x 216 + 2 x 40) = 65536.
+template <int D> struct OccWide {
+    static constexpr int kMinBlocks = 1, kThreads = 512;
+    static constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 40;
+};
+template <> struct Occ<80, kPagedE4m3> : OccWide<80> {};
+template <> struct Occ<96, kPagedE4m3> : OccWide<96> {};
+template <> struct Occ<128, kPagedE4m3> : OccWide<128> {};
+static_assert(128 * (2 * OccWide<128>::kRegsSoftmax + 2 * OccWide<128>::kRegsOther) <= 65536, "wide e4m3 split");
+template <> struct Occ<32, kPagedE4m3> {
+    static constexpr int kMinBlocks = Cfg<32>::kMinBlocks < 3 ? Cfg<32>::kMinBlocks : 3;
+    static constexpr int kThreads = Cfg<32>::kThreads;
+    static constexpr uint32_t kLaunch = (65536 / (256 * kMinBlocks)) / 8 * 8;
+    static constexpr uint32_t kRegsOther = kMinBlocks == 3 ? 56 : 64;
+    static constexpr uint32_t kRegsSoftmax = 2 * kLaunch - kRegsOther;
+};
+template <> struct Occ<64, kPagedE4m3> : Occ<32, kPagedE4m3> {};
+static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kRegsOther) <=
+                  256 * Occ<64, kPagedE4m3>::kLaunch,
+              "e4m3 d<=64 register split");
+
+
 struct PrefillParams {
     __nv_bfloat16 *o;
     float *lse;
@@ -375,13 +406,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
 
 // Widens one staged e4m3 tile into a ring slot: bf16 (keys: the type of Q) or f16 (values: the
 // type P is packed in).  Both are exact: every e4m3 value is a bf16 and an f16 value.
-template <int D, bool F16>
+template <int D, bool F16, int NCV>
 __device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, __nv_bfloat16 *dst, int ct) {
     constexpr int kBN = kBNd<D>;
     constexpr int kChunksPerRow = D / 16;  // 16-byte chunks of e4m3 per row
     uint8_t *d8 = reinterpret_cast<uint8_t *>(dst);
 #pragma unroll 4
-    for (int idx = ct; idx < kBN * kChunksPerRow; idx += 64) {
+    for (int idx = ct; idx < kBN * kChunksPerRow; idx += NCV) {
         const int r = idx / kChunksPerRow, c16 = idx % kChunksPerRow;
         uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
         if ((loaded >> (r / kPageTokens)) & 1u) {
@@ -406,8 +437,12 @@ __device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, 
     }
 }
 
+// NCV converter threads (the warps after the MMA issuer's).
+template <int D> constexpr int kConverters = Occ<D, kPagedE4m3>::kThreads - (Cfg<D>::kMmaWarp + 1) * 32;
+
 template <int D>
 __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, WaitCtx wc) {
+    constexpr int NCV = kConverters<D>;
     // every converter arrives, then waits for the phase to complete (bounded like every wait)
     uint32_t cv_phase = 0;
     auto sync_converters = [&]() -> bool {
@@ -429,7 +464,7 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
                 ok = false;
                 break;
             }
-            widen_tile<D, false>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
+            widen_tile<D, false, NCV>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
             if (!(ok = sync_converters())) break;
             if (ct == 0) mbar_arrive(&sm.st.k_empty);
             ++kf;
@@ -439,7 +474,7 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
                 ok = false;
                 break;
             }
-            widen_tile<D, true>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
+            widen_tile<D, true, NCV>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
             ++vf;
         }
         fence_proxy_async_smem();  // this thread's tile writes, before the MMA's reads
@@ -776,26 +811,8 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, const
     }
 }
 
-// CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
-// d <= 64 CTA 56 KB, so three of them share an SM, launched at 80 registers (128 x (104 + 56) =
-// 20480 = 256 x 80); the converter warps take registers from the producer's warpgroup.
-template <int D, int M> struct Occ {
-    static constexpr int kMinBlocks = Cfg<D>::kMinBlocks;
-    static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;
-};
-template <> struct Occ<32, kPagedE4m3> {
-    static constexpr int kMinBlocks = Cfg<32>::kMinBlocks < 3 ? Cfg<32>::kMinBlocks : 3;
-    static constexpr uint32_t kLaunch = (65536 / (256 * kMinBlocks)) / 8 * 8;
-    static constexpr uint32_t kRegsOther = kMinBlocks == 3 ? 56 : 64;
-    static constexpr uint32_t kRegsSoftmax = 2 * kLaunch - kRegsOther;
-};
-template <> struct Occ<64, kPagedE4m3> : Occ<32, kPagedE4m3> {};
-static_assert(128 * (Occ<64, kPagedE4m3>::kRegsSoftmax + Occ<64, kPagedE4m3>::kRegsOther) <=
-                  256 * Occ<64, kPagedE4m3>::kLaunch,
-              "e4m3 d<=64 register split");
-
 template <int D, int M>
-__global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
+__global__ void __launch_bounds__((Occ<D, M>::kThreads), (Occ<D, M>::kMinBlocks))
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                    const PrefillParams p) {
@@ -858,7 +875,7 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
             mbar_init(&sm.st.v_full, 1);
             mbar_init(&sm.st.k_empty, 1);
             mbar_init(&sm.st.v_empty, 1);
-            mbar_init(&sm.st.cv_bar, 64);
+            mbar_init(&sm.st.cv_bar, kConverters<D>);
         }
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -884,8 +901,8 @@ __global__ void __launch_bounds__(Cfg<D>::kThreads, (Occ<D, M>::kMinBlocks))
         } else if (warp == Cfg<D>::kMmaWarp) {
             if (lane == 0 && n_all > 0) run_mma<D, M>(sm, tmem, n, n_all, wc);
         } else if constexpr (M == kPagedE4m3) {
-            // the last two warps of the CTA convert e4m3 tiles into the ring
-            if (n_all > 0) run_convert<D>(sm, n_all, (int)threadIdx.x - (Cfg<D>::kThreads - 64), wc);
+            // the warps after the MMA issuer's convert e4m3 tiles into the ring
+            if (n_all > 0) run_convert<D>(sm, n_all, (int)threadIdx.x - (Cfg<D>::kMmaWarp + 1) * 32, wc);
         }
     } else {
         if constexpr (Cfg<D>::kSplitRegs) setmaxnreg_inc<Occ<D, M>::kRegsSoftmax>();
@@ -911,9 +928,9 @@ cudaError_t check_register_split() {
         cudaFuncAttributes fa;
         const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, M>);
         if (e != cudaSuccess) return e;
-        const long pool = (long)fa.numRegs * Cfg<D>::kThreads;
+        const long pool = (long)fa.numRegs * Occ<D, M>::kThreads;
         const long need = 128L * (Cfg<D>::QT * (long)Occ<D, M>::kRegsSoftmax +
-                                  (Cfg<D>::kThreads / 128 - Cfg<D>::QT) * (long)Occ<D, M>::kRegsOther);
+                                  (Occ<D, M>::kThreads / 128 - Cfg<D>::QT) * (long)Occ<D, M>::kRegsOther);
         verdict = (!Cfg<D>::kSplitRegs || need <= pool) ? 1 : -1;
     }
     return verdict == 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
@@ -968,7 +985,7 @@ cudaError_t launch_prefill_dm(const PrefillArgs &a, cudaStream_t stream) {
     e = ensure_max_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<D, M>), (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)p.n_units * BH);
-    prefill_kernel<D, M><<<grid, Cfg<D>::kThreads, smem, stream>>>(tq, tk, tv, to, p);
+    prefill_kernel<D, M><<<grid, Occ<D, M>::kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
