@@ -846,8 +846,10 @@ def reference_arm(args):
     # about a minute of oracle work in all: each step is a seeded sample of query rows (at least one
     # block of 64) sized to its share of the minute
     budget = min(10.0, 60.0 / max(1, args.steps + args.warmup))
-    if shape is None:  # decode only
+    if shape is None:  # decode only: the decode workload the GPU arm would time (its bf16 cache)
         dshape = workloads.PAGED_DECODE
+        if args.workload.startswith("decode_d"):
+            dshape = workloads.PAGED_DECODE_BY_DIM[int(args.workload[len("decode_d"):].split("_")[0])]
         inp = workloads.decode_inputs(dshape)
         bytes_ = metrics.decode_bytes(dshape.H, dshape.d, [int(x) for x in inp["ctx_lens"]], dshape.page_size)
         times = time_oracle_decode(oracle, dshape, inp, args.steps)
