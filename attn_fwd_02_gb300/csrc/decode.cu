@@ -76,15 +76,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 // D of the last box are read as zeros by TMA and never used by the products).
 template <int D> constexpr int kBoxes = (D + 63) / 64;
 // Bytes of one ring buffer (one page block of K or V): the bulk-copied block (kPS rows of D
-// elements), or kBoxes swizzled 16 x 64 boxes for the grouped-query kernel's bf16 TMA loads.
+// elements), or the grouped-query kernel's swizzled TMA boxes: kBoxes boxes of 16 x 64 bf16, or
+// one box of 16 x 128 e4m3 codes.
 template <int D, int GP, bool FP8>
-constexpr int kSlotBytes = (!FP8 && GP > 1) ? kBoxes<D> * kPS * 128 : kPS * D * (FP8 ? 1 : 2);
+constexpr int kSlotBytes = GP > 1 ? (FP8 ? kPS * 128 : kBoxes<D> * kPS * 128) : kPS * D * (FP8 ? 1 : 2);
 
 template <int D, int GP, bool FP8>
 struct DecodeSmem {
     // [warp][slot][0 = K, 1 = V][one page block]; 16-byte aligned blocks (1024-byte alignment for
     // the swizzled TMA boxes of the grouped-query mma kernel)
-    alignas((!FP8 && GP > 1) ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kSlotBytes<D, GP, FP8>];
+    alignas(GP > 1 ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kSlotBytes<D, GP, FP8>];
     uint64_t full[kWarps][kSlotsFor<FP8, GP>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
@@ -465,6 +466,26 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The same product over f16 fragments.
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Byte permute: byte i of the result is byte (sel >> 4i) & 7 of {hi:lo}.
+__device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+    return r;
+}
+// Two e4m3 codes (the low 16 bits, low byte first) -> an f16x2 word (exact: every e4m3 value is
+// an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
 
 // Byte offset of the 16-byte chunk holding column col (a multiple of 8) of row r in a page block
 // stored as 128-byte-swizzled boxes of 16 rows x 64 bf16 columns.
@@ -472,14 +493,27 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
     return (uint32_t)((col >> 6) * (16 * 128) + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-// An e4m3 cache takes the same path: each warp widens its fp8 page block into a bf16 staging tile
-// in the same swizzled layout (exact: every e4m3 value is a bf16 value), the key scale folds into
-// the score scale and the value scale into the partial O.
+// An e4m3 cache takes the same path with f16 products.  Each page block arrives by TMA as one
+// 128-byte-swizzled box of 16 rows x 128 codes, and ldmatrix hands every lane its codes in
+// fragment order, so they are widened in registers (one conversion per two codes, exact) with no
+// staging copy:
+//  - K (plain ldmatrix of 8 tokens x 16 codes): lane (g, t) gets dims 16c + 4t .. 16c + 4t + 3 of
+//    token g, the B fragment of k-step c when the k-step's logical index 2t + {0, 1} stands for dims
+//    16c + 4t + {0, 1} and 2t + 8 + {0, 1} for 16c + 4t + 2 + {0, 1}.  Q's A fragments are loaded in
+//    the same order (a permutation of the contraction index leaves Q K^T unchanged).
+//  - V (transposed ldmatrix, codes taken in pairs): lane (g, t) gets tokens 2t, 2t + 1 of dims
+//    16c + 2g and 16c + 2g + 1; one byte permute splits them into the B fragments of two n-tiles,
+//    one over the chunk's even dims and one over its odd dims, and the final write of O puts
+//    column n of n-tile (c, parity) at dim 16c + 2n + parity.
+// Q is rounded to f16 once per CTA after a power-of-two factor that keeps |Q| below 2^15 (exact
+// for every bf16 value in f16's normal range); the factor, the key scale and the softmax scale fold
+// into the score scale, the value scale into the partial O.
 // Ring slots per warp of the grouped-query kernel: the page loads in flight per warp.  Measured
 // on 32 sequences x 8 cache heads (4 query heads each), contexts U[512, 8192], fraction of HBM:
-// bf16 pages 1 / 2 / 3 slots 0.853 / 0.880 / 0.844; e4m3 pages 2 / 3 / 4 / 5 slots 0.42 / 0.36 /
-// 0.37 / 0.25.  More pages in flight do not help the e4m3 form: it is bound by the work per page
-// (widening, two products, the softmax), not by the bytes in flight.
+// bf16 pages 1 / 2 / 3 slots 0.853 / 0.880 / 0.844; e4m3 pages 2 / 3 / 4 slots 0.565 / 0.555 /
+// 0.557, and with registers capped for four CTAs per SM 0.53 / 0.53 / 0.50.  More pages in flight
+// do not help the e4m3 form: it is bound by the work per page (two products, the softmax), not by
+// the bytes in flight.
 template <bool FP8> constexpr int kGqaSlots = 2;
 
 template <int D, int GP, bool FP8>
@@ -497,24 +531,8 @@ struct GqaMmaSmem {
         } red;
     } u;
     uint64_t full[kWarps][kGqaSlots<FP8>];
-    // bf16 K, V of one page in the swizzled box layout (kBoxes<D> boxes of 16 x 64)
-    alignas(128) __nv_bfloat16 stage[FP8 ? kWarps : 1][2][FP8 ? kBoxes<D> * kPS * 64 : 8];
     int abort_flag;
 };
-
-// 16 e4m3 codes (one 16-byte chunk of a page row) -> 16 bf16 values, two 16-byte chunks.
-__device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 &lo, uint4 &hi) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 a = e4m3x2_to_float2(w[i]), b = e4m3x2_to_float2(w[i] >> 16);
-        o[2 * i] = pack_bf16x2(a.x, a.y);
-        o[2 * i + 1] = pack_bf16x2(b.x, b.y);
-    }
-    lo = make_uint4(o[0], o[1], o[2], o[3]);
-    hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
 
 template <int D, int GP, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -524,8 +542,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
     static_assert(D % 16 == 0, "k-steps of 16");
     constexpr int kSl = kGqaSlots<FP8>;
-    constexpr uint32_t kBlockBytes = kPS * D * (FP8 ? 1 : 2);   // bytes of a page block in HBM
-    constexpr uint32_t kBoxBytesAll = kBoxes<D> * kPS * 128;     // a block's TMA boxes (zero-filled past D)
+    constexpr int kBx = FP8 ? 1 : kBoxes<D>;              // TMA boxes per page block (128-byte rows)
+    constexpr uint32_t kBoxBytesAll = kBx * kPS * 128;    // a block's boxes (zero-filled past D)
     constexpr int KS = D / 16;  // k-steps of S = Q K^T
     constexpr int NT = D / 8;   // n-tiles of O += P V (even: n-tiles go in pairs)
     static_assert(NT % 2 == 0, "pairs of n-tiles");
@@ -560,12 +578,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     int my_pid = -1;
     if (lane < nk) my_pid = a.page_table[(size_t)b * a.max_pages + page0 + warp + kWarps * lane];
     const bool my_ok = (my_pid >= 0 && my_pid < a.num_pages);
-    if (!FP8 && lane == 0) {
+    if (lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    const uint8_t *kbase = reinterpret_cast<const uint8_t *>(a.k_pages);
-    const uint8_t *vbase = reinterpret_cast<const uint8_t *>(a.v_pages);
     auto issue = [&](int k) {
         const int pid = __shfl_sync(0xffffffffu, my_pid, k);
         const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
@@ -573,17 +589,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             uint64_t *bar = &sm.full[warp][k % kSl];
             if (ok) {
                 const int row = pid * Hkv + kvh;  // page block in the pool viewed as [num_pages * Hkv, 16, D]
-                if constexpr (FP8) {
-                    mbar_arrive_expect_tx(bar, 2 * kBlockBytes);
-                    bulk_load(sm.u.kv[warp][k % kSl][0], kbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
-                    bulk_load(sm.u.kv[warp][k % kSl][1], vbase + (size_t)row * kBlockBytes, kBlockBytes, bar);
-                } else {
-                    mbar_arrive_expect_tx(bar, 2 * kBoxBytesAll);
+                mbar_arrive_expect_tx(bar, 2 * kBoxBytesAll);
 #pragma unroll
-                    for (int i = 0; i < kBoxes<D>; ++i) {
-                        tma_load_3d(sm.u.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
-                        tma_load_3d(sm.u.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
-                    }
+                for (int i = 0; i < kBx; ++i) {  // box i: columns 64 i .. 64 i + 63 (bf16) or all 128 codes (e4m3)
+                    tma_load_3d(sm.u.kv[warp][k % kSl][0] + i * (16 * 128), &tmK, bar, i * 64, 0, row);
+                    tma_load_3d(sm.u.kv[warp][k % kSl][1] + i * (16 * 128), &tmV, bar, i * 64, 0, row);
                 }
             } else {
                 mbar_arrive(bar);
@@ -598,15 +608,44 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     const uint32_t *q32 = reinterpret_cast<const uint32_t *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
                                                              ((size_t)b * a.H + qh0) * D);
     uint32_t qa[KS][4];
+    float c = a.scale * kLog2e;
+    if constexpr (FP8) {
+        // dims 16 ks + 2 kq + {0, 1} (a0, a1) and + {2, 3} (a2, a3): the order of the K fragments
+        float amax = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-        const int c0 = ks * 16 + kq;
-        qa[ks][0] = r0 < GP ? q32[(r0 * D + c0) / 2] : 0u;
-        qa[ks][1] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0) / 2] : 0u;
-        qa[ks][2] = r0 < GP ? q32[(r0 * D + c0 + 8) / 2] : 0u;
-        qa[ks][3] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0 + 8) / 2] : 0u;
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rr = r0 + 8 * h;
+                const uint2 u = rr < GP ? *reinterpret_cast<const uint2 *>(q32 + (rr * D + ks * 16 + 2 * kq) / 2)
+                                        : make_uint2(0u, 0u);
+                qa[ks][h] = u.x;
+                qa[ks][h + 2] = u.y;
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(u.x << 16)), fabsf(__uint_as_float(u.x & 0xffff0000u))),
+                                         fmaxf(fabsf(__uint_as_float(u.y << 16)), fabsf(__uint_as_float(u.y & 0xffff0000u)))));
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        // 2^-sh * |Q| < 2^15: sh = e - 14 when |Q| >= 2^15 (e its binary exponent); at most 113
+        const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+        const int sh = e >= 15 ? min(e - 14, 113) : 0;
+        const float f = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                qa[ks][i] = pack_f16x2(__uint_as_float(qa[ks][i] << 16) * f, __uint_as_float(qa[ks][i] & 0xffff0000u) * f);
+        c *= a.k_scale * __uint_as_float((uint32_t)(127 + sh) << 23);
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int c0 = ks * 16 + kq;
+            qa[ks][0] = r0 < GP ? q32[(r0 * D + c0) / 2] : 0u;
+            qa[ks][1] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0) / 2] : 0u;
+            qa[ks][2] = r0 < GP ? q32[(r0 * D + c0 + 8) / 2] : 0u;
+            qa[ks][3] = r0 + 8 < GP ? q32[((r0 + 8) * D + c0 + 8) / 2] : 0u;
+        }
     }
-    const float c = a.scale * kLog2e * (FP8 ? a.k_scale : 1.f);
 
     float o[NT][4];
 #pragma unroll
@@ -617,6 +656,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
     const int mi = lane >> 3, mr = lane & 7;
     const int k_row = (mi >> 1) * 8 + mr, k_col = (mi & 1) * 8;  // + ks * 16 columns
     const int v_row = (mi & 1) * 8 + mr, v_col = (mi >> 1) * 8;  // + nd * 8 columns
+    // e4m3 boxes: matrices {tokens 0-7, tokens 8-15} x {chunk c, chunk c + 1} (16 codes a chunk)
+    const int f_row = (mi & 1) * 8 + mr, f_chunk = mi >> 1;
+    auto f_off = [](int r, int chunk) { return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4)); };
 
     int issued = first;
     bool failed = false;
@@ -630,36 +672,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
         const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
         const int ntok = min(kPS, tok1 - page_tok0);
         if (ok) {
-            uint32_t Ks = smem_u32(sm.u.kv[warp][slot][0]);
-            uint32_t Vs = smem_u32(sm.u.kv[warp][slot][1]);
-            if constexpr (FP8) {
-                // widen the e4m3 block into this warp's bf16 staging tiles (swizzled as the TMA boxes);
-                // V rows past the context end are written as zeros
-                uint8_t *stK = reinterpret_cast<uint8_t *>(sm.stage[warp][0]);
-                uint8_t *stV = reinterpret_cast<uint8_t *>(sm.stage[warp][1]);
-                constexpr int kChunks = kPS * D / 16;  // 16-byte chunks of fp8 per block
-#pragma unroll
-                for (int i = lane; i < kChunks; i += 32) {
-                    const int r = i / (D / 16), c0 = (i % (D / 16)) * 16;
-                    uint4 lo, hi;
-                    e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.u.kv[warp][slot][0])[i], lo, hi);
-                    *reinterpret_cast<uint4 *>(stK + swz_off(r, c0)) = lo;
-                    *reinterpret_cast<uint4 *>(stK + swz_off(r, c0 + 8)) = hi;
-                    if (r < ntok) {
-                        e4m3x16_to_bf16(reinterpret_cast<const uint4 *>(sm.u.kv[warp][slot][1])[i], lo, hi);
-                    } else {
-                        lo = hi = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    *reinterpret_cast<uint4 *>(stV + swz_off(r, c0)) = lo;
-                    *reinterpret_cast<uint4 *>(stV + swz_off(r, c0 + 8)) = hi;
-                }
-                __syncwarp();
-                Ks = smem_u32(stK);
-                Vs = smem_u32(stV);
-            } else if (ntok < kPS) {
+            const uint32_t Ks = smem_u32(sm.u.kv[warp][slot][0]);
+            const uint32_t Vs = smem_u32(sm.u.kv[warp][slot][1]);
+            if (ntok < kPS) {
                 // slots past the context end: zero their V rows (every box) so P = 0 meets finite values
                 const int per_box = (kPS - ntok) * 8;  // 16-byte chunks of the dead rows of one box
-                for (int i = lane; i < per_box * kBoxes<D>; i += 32) {
+                for (int i = lane; i < per_box * kBx; i += 32) {
                     const int box = i / per_box, j = i % per_box;
                     *reinterpret_cast<uint4 *>(sm.u.kv[warp][slot][1] + box * (16 * 128) + ntok * 128 + j * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
@@ -667,12 +685,26 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 __syncwarp();
             }
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            if constexpr (FP8) {
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t bk[4];
-                ldsm_x4(Ks + swz_off(k_row, ks * 16 + k_col), bk);
-                mma_16816(sc[0], qa[ks], bk[0], bk[1]);
-                mma_16816(sc[1], qa[ks], bk[2], bk[3]);
+                for (int ks = 0; ks < KS; ks += 2) {
+                    uint32_t bk[4];  // tokens 0-7 / 8-15 of chunk ks, then of chunk ks + 1 (zeros past D)
+                    ldsm_x4(Ks + f_off(f_row, ks + f_chunk), bk);
+                    mma_16816_f16(sc[0], qa[ks], e4m3x2_f16x2(bk[0]), e4m3x2_f16x2(bk[0] >> 16));
+                    mma_16816_f16(sc[1], qa[ks], e4m3x2_f16x2(bk[1]), e4m3x2_f16x2(bk[1] >> 16));
+                    if (ks + 1 < KS) {
+                        mma_16816_f16(sc[0], qa[ks + 1], e4m3x2_f16x2(bk[2]), e4m3x2_f16x2(bk[2] >> 16));
+                        mma_16816_f16(sc[1], qa[ks + 1], e4m3x2_f16x2(bk[3]), e4m3x2_f16x2(bk[3] >> 16));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t bk[4];
+                    ldsm_x4(Ks + swz_off(k_row, ks * 16 + k_col), bk);
+                    mma_16816(sc[0], qa[ks], bk[0], bk[1]);
+                    mma_16816(sc[1], qa[ks], bk[2], bk[3]);
+                }
             }
             // log2-domain scores; this lane holds tokens nt*8 + (lane&3)*2 + {0,1} of rows r0 / r0+8
             float x[2][4];
@@ -724,14 +756,33 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 ps[h] += __shfl_xor_sync(0xffffffffu, ps[h], 2);
                 l_run[h] += ps[h];
             }
-            const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
-                                    pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+            if constexpr (FP8) {
+                const uint32_t pa[4] = {pack_f16x2(p[0][0], p[0][1]), pack_f16x2(p[0][2], p[0][3]),
+                                        pack_f16x2(p[1][0], p[1][1]), pack_f16x2(p[1][2], p[1][3])};
 #pragma unroll
-            for (int nd = 0; nd < NT; nd += 2) {
-                uint32_t bv[4];
-                ldsm_x4_trans(Vs + swz_off(v_row, nd * 8 + v_col), bv);
-                mma_16816(o[nd], pa, bv[0], bv[1]);
-                mma_16816(o[nd + 1], pa, bv[2], bv[3]);
+                for (int ch = 0; ch < KS; ch += 2) {
+                    uint32_t bv[4];  // per lane: tokens 2t, 2t+1 (+ 8) x dims 2g, 2g+1 of chunks ch, ch + 1
+                    ldsm_x4_trans(Vs + f_off(f_row, ch + f_chunk), bv);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if (ch + j < KS) {
+                            // {tok 2t dim 2g, tok 2t+1 dim 2g} | {tok 2t dim 2g+1, tok 2t+1 dim 2g+1}
+                            const uint32_t lo = prmt(bv[2 * j], 0u, 0x3120u), hi = prmt(bv[2 * j + 1], 0u, 0x3120u);
+                            mma_16816_f16(o[2 * (ch + j)], pa, e4m3x2_f16x2(lo), e4m3x2_f16x2(hi));
+                            mma_16816_f16(o[2 * (ch + j) + 1], pa, e4m3x2_f16x2(lo >> 16), e4m3x2_f16x2(hi >> 16));
+                        }
+                    }
+                }
+            } else {
+                const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
+                                        pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+#pragma unroll
+                for (int nd = 0; nd < NT; nd += 2) {
+                    uint32_t bv[4];
+                    ldsm_x4_trans(Vs + swz_off(v_row, nd * 8 + v_col), bv);
+                    mma_16816(o[nd], pa, bv[0], bv[1]);
+                    mma_16816(o[nd + 1], pa, bv[2], bv[3]);
+                }
             }
         }
         fence_proxy_async_smem();
@@ -763,8 +814,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             }
 #pragma unroll
             for (int nd = 0; nd < NT; ++nd) {
-                sm.u.red.o[warp][g][nd * 8 + kq] = o[nd][2 * h];
-                sm.u.red.o[warp][g][nd * 8 + kq + 1] = o[nd][2 * h + 1];
+                // columns kq, kq + 1 of n-tile nd: dims nd * 8 + kq + {0, 1}, or for e4m3 pages
+                // 16 (nd / 2) + 2 kq + (nd % 2) + {0, 2}
+                const int d0 = FP8 ? (nd >> 1) * 16 + 2 * kq + (nd & 1) : nd * 8 + kq;
+                sm.u.red.o[warp][g][d0] = o[nd][2 * h];
+                sm.u.red.o[warp][g][d0 + (FP8 ? 2 : 1)] = o[nd][2 * h + 1];
             }
         }
     }
@@ -876,12 +930,15 @@ cudaError_t launch_decode_g(const DecodeArgs &a, int max_splits, int chunk, cuda
 
 template <int D, int GP, bool FP8>
 cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t stream) {
-    // bf16 pages: page pool [num_pages * Hkv, 16, D], one 16 x 64 box per page block and 64 columns.
-    // e4m3 pages are fetched as plain bulk copies and the maps are not used.
+    // page pool [num_pages * Hkv, 16, D]: bf16 pages in 16 x 64 boxes (one per 64 columns), e4m3
+    // pages in one 16 x 128-code box per page block
     CUtensorMap tk{}, tv{};
-    if (!FP8 && (!encode_qkv_map(&tk, a.k_pages, a.num_pages * a.Hkv, kPS, D, kPS) ||
-                 !encode_qkv_map(&tv, a.v_pages, a.num_pages * a.Hkv, kPS, D, kPS)))
-        return cudaErrorInvalidValue;
+    const int rows = a.num_pages * a.Hkv;
+    const bool ok = FP8 ? (encode_page_map_u8(&tk, a.k_pages, rows, kPS, D) &&
+                           encode_page_map_u8(&tv, a.v_pages, rows, kPS, D))
+                        : (encode_qkv_map(&tk, a.k_pages, rows, kPS, D, kPS) &&
+                           encode_qkv_map(&tv, a.v_pages, rows, kPS, D, kPS));
+    if (!ok) return cudaErrorInvalidValue;
     const size_t smem = sizeof(GqaMmaSmem<D, GP, FP8>) + 1024;
     cudaError_t e =
         ensure_max_dynamic_smem(reinterpret_cast<const void *>(decode_gqa_mma_kernel<D, GP, FP8>), (int)smem);

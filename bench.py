@@ -47,6 +47,7 @@ KERNEL_SOURCES = {
     "decode_split_kernel": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
     "decode_split_kernel_e4m3": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
     "decode_gqa_mma_kernel": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
+    "decode_gqa_mma_kernel_e4m3": ["attn_fwd_02_gb300/csrc/decode.cu", "attn_fwd_02_gb300/csrc/sm103_ptx.cuh"],
 }
 
 PREFILL_BY_NAME = {
@@ -542,7 +543,7 @@ def roofline_decode(case, ms_split, ms_total, peaks, peak_kind):
     fp8 = isinstance(case, DecodeFp8Case)
     if case.kv_heads is not None and case.kv_heads < case.shape.H:
         kernel = "decode_gqa_mma_kernel"
-        key = kernel if (not fp8 and case.shape is workloads.PAGED_DECODE_GQA) else None
+        key = (kernel + "_e4m3" if fp8 else kernel) if case.shape is workloads.PAGED_DECODE_GQA else None
     else:
         kernel = "decode_split_kernel"
         key = ("decode_split_kernel_e4m3" if fp8 else "decode_split_kernel") \
