@@ -179,7 +179,7 @@ bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, int b
     return r == CUDA_SUCCESS;
 }
 
-bool encode_page_map_u8(CUtensorMap *m, const void *ptr, int rows, int page_rows, int D) {
+bool encode_page_map_u8(CUtensorMap *m, const void *ptr, int rows, int page_rows, int D, bool swizzle) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)page_rows, (cuuint64_t)rows};
@@ -187,8 +187,8 @@ bool encode_page_map_u8(CUtensorMap *m, const void *ptr, int rows, int page_rows
     cuuint32_t box[3] = {128, (cuuint32_t)page_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -64,8 +64,8 @@ cudaError_t ensure_max_dynamic_smem(const void *kernel, int bytes);
 // 64 x box_rows x 1 and the 128-byte swizzle; rows past N read as zeros.
 bool encode_qkv_map(CUtensorMap *m, const void *ptr, int BH, int N, int D, int box_rows = 128);
 // [rows, page_rows, D] one-byte (e4m3) page blocks, one box of page_rows x 128 bytes per block,
-// 128-byte swizzle; the bytes of a box past D are read as zeros.
-bool encode_page_map_u8(CUtensorMap *m, const void *ptr, int rows, int page_rows, int D);
+// with the 128-byte swizzle or none; the bytes of a box past D are read as zeros.
+bool encode_page_map_u8(CUtensorMap *m, const void *ptr, int rows, int page_rows, int D, bool swizzle = true);
 
 // Encodes the TMA descriptors and launches the prefill kernel.
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);

@@ -98,7 +98,7 @@ constexpr int kPageTokens = 16;            // tokens per page of the paged KV ca
 
 // Where K/V come from (a compile-time parameter of the kernel, so that each form carries only
 // its own code): contiguous [B, Hkv, Nkv, d] tensors; bf16 pages of a paged KV cache; or e4m3
-// pages, widened to bf16 in shared memory before the products.
+// pages, widened to f16 in shared memory before the products.
 enum KvMode : int { kContig = 0, kPagedBf16 = 1, kPagedE4m3 = 2 };
 
 // CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
@@ -157,16 +157,10 @@ struct PrefillParams {
 // step at one wait and one commit for the ring.
 template <int D> constexpr int kStagesOf = Cfg<D>::kStages;
 
-// e4m3 pages: one K tile and one V tile of codes, staged page block by page block (16 rows of d
-// bytes each) before the converter warps widen them into the bf16 ring.
-template <int D, int M> struct KvStage {};
-template <int D> struct alignas(128) KvStage<D, kPagedE4m3> {
-    uint8_t k[kBNd<D> * D];
-    uint8_t v[kBNd<D> * D];
-    uint64_t k_full, k_empty, v_full, v_empty;
-    uint64_t cv_bar;              // rendezvous of the 64 converter threads (bounded, unlike bar.sync)
-    uint32_t k_loaded, v_loaded;  // bit pg: page pg of the staged tile was loaded (else it is zeros)
-};
+// e4m3 pages: a ring unit's codes land by TMA in its own slots -- in each tile's last 64-column
+// box, one 128-byte row per key (zeros past d) -- and the converter warps widen them to f16 in place
+// (code_off is that box's byte offset).
+template <int D> constexpr int kCodeOff = (kPad<D> / 64 - 1) * kBNd<D> * 128;
 
 template <int D, int M>
 struct alignas(1024) PrefillSmem {
@@ -175,13 +169,14 @@ struct alignas(1024) PrefillSmem {
     __nv_bfloat16 q[Cfg<D>::QT][kBM * kPad<D>];  // kPad/64 boxes each
     __nv_bfloat16 k[kStagesOf<D>][kBNd<D> * kPad<D>];  // kPad/64 boxes each
     __nv_bfloat16 v[kStagesOf<D>][kBNd<D> * kPad<D>];  // kPad/64 boxes each
-    KvStage<D, M> st;
     uint64_t q_full;
     uint64_t u_full[kStagesOf<D>], u_empty[kStagesOf<D>];
+    uint64_t c_full[kStagesOf<D>];  // e4m3 pages: the unit's codes have landed (u_full: widened)
     uint64_t s_full[kQTilesMax];
     uint64_t p_full[kQTilesMax];
     uint64_t o_done[kQTilesMax];
     uint64_t o_staged[kQTilesMax];  // the warpgroup's O rows are in shared memory
+    uint64_t q_conv[kQTilesMax];    // e4m3 pages: the warpgroup's Q rows are f16 in shared memory
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -249,10 +244,8 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
     constexpr int kBoxes = kPad<D> / 64;
     if (u_begin == 0) {  // Q not yet issued (paged modes)
         prefetch_tensormap(tmQ);
-        if constexpr (M != kPagedE4m3) {
-            prefetch_tensormap(tmK);
-            prefetch_tensormap(tmV);
-        }
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
         mbar_arrive_expect_tx(&sm.q_full, Cfg<D>::QT * kBoxes * kBoxBytes);
 #pragma unroll
         for (int t = 0; t < Cfg<D>::QT; ++t)
@@ -278,69 +271,24 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
     for (int pg = 0; pg < kTilePages; ++pg) ids_prev[pg] = ids_cur[pg] = ids_next[pg] = -1;
     if constexpr (M != kContig) fetch_ids(0, ids_next);
 
-    if constexpr (M == kPagedE4m3) {
-        // e4m3 pages: one bulk copy per mapped page block (16 rows of d codes) into the staging
-        // tiles; pages past the sequence's end or unmapped are not loaded (the converters write
-        // zeros there, and the softmax masks those keys).  K(u) and V(u-1) are staged as the
-        // converters free the staging tiles; the ring slots are the converters' to fill.
-        constexpr uint32_t kPageBytes = kPageTokens * D;
-        auto stage = [&](uint8_t *dst, const uint8_t *pool, uint64_t *full, uint32_t *loaded,
-                         const int (&ids)[kTilePages]) {
-            uint32_t mask = 0, bytes = 0;
-#pragma unroll
-            for (int pg = 0; pg < kTilePages; ++pg)
-                if (ids[pg] >= 0 && ids[pg] < p.num_pages) {
-                    mask |= 1u << pg;
-                    bytes += kPageBytes;
-                }
-            *loaded = mask;
-            mbar_arrive_expect_tx(full, bytes);
-#pragma unroll
-            for (int pg = 0; pg < kTilePages; ++pg)
-                if ((mask >> pg) & 1u)
-                    bulk_load(dst + pg * kPageBytes, pool + ((size_t)ids[pg] * p.Hkv + kvh) * kPageBytes, kPageBytes,
-                              full);
-        };
-        int kf = 0, vf = 0;  // tiles staged so far
-        for (int u = 0; u <= n_all; ++u) {
-#pragma unroll
-            for (int pg = 0; pg < kTilePages; ++pg) {
-                ids_prev[pg] = ids_cur[pg];
-                ids_cur[pg] = ids_next[pg];
-            }
-            if (u + 1 < n_all) fetch_ids(u + 1, ids_next);
-            if (u < n_all) {  // K(u)
-                if (kf > 0 && !mbar_wait(&sm.st.k_empty, (uint32_t)((kf - 1) & 1), wc, 2)) break;
-                stage(sm.st.k, p.k8, &sm.st.k_full, &sm.st.k_loaded, ids_cur);
-                ++kf;
-            }
-            if (u > 0) {  // V(u-1)
-                if (vf > 0 && !mbar_wait(&sm.st.v_empty, (uint32_t)((vf - 1) & 1), wc, 3)) break;
-                stage(sm.st.v, p.v8, &sm.st.v_full, &sm.st.v_loaded, ids_prev);
-                ++vf;
-            }
-        }
-        if (*wc.abort_flag) {
-            // unwinding: let every copy still in flight land before the CTA exits
-            WaitCtx drain{nullptr, wc.status};
-            (void)mbar_wait(&sm.q_full, 0, drain, 90);
-            if (kf > 0) (void)mbar_wait(&sm.st.k_full, (uint32_t)((kf - 1) & 1), drain, 92);
-            if (vf > 0) (void)mbar_wait(&sm.st.v_full, (uint32_t)((vf - 1) & 1), drain, 93);
-        }
-        return;
-    }
-
-    // bf16 K/V by TMA into the ring slots.  Paged: pool row (page * Hkv + head) of each page of a
-    // tile; pages past the sequence's last page, or with an id outside the pool (an unmapped page,
-    // whose keys the softmax masks), get an out-of-range row, which TMA reads as zeros.
+    // K/V by TMA into the ring slots.  Paged: pool row (page * Hkv + head) of each page of a tile;
+    // pages past the sequence's last page, or with an id outside the pool (an unmapped page, whose
+    // keys the softmax masks), get an out-of-range row, which TMA reads as zeros.  bf16 pages: one
+    // 16-row box per page and 64-column block; e4m3 pages: one box of 16 rows x 128 codes per page,
+    // into the tile's code rows (kCodeOff), for the converters to widen.
     auto load_tile = [&](__nv_bfloat16 *dst, const CUtensorMap *map, uint64_t *bar, const int (&ids)[kTilePages]) {
 #pragma unroll
         for (int pg = 0; pg < kTilePages; ++pg) {
             const int id = ids[pg];
             const int row = (id >= 0 && id < p.num_pages) ? id * p.Hkv + kvh : p.num_pages * p.Hkv;
+            if constexpr (M == kPagedE4m3) {
+                tma_load_3d(reinterpret_cast<uint8_t *>(dst) + kCodeOff<D> + pg * (kPageTokens * 128), map, bar, 0, 0,
+                            row);
+            } else {
 #pragma unroll
-            for (int i = 0; i < kBoxes; ++i)
-                tma_load_3d(dst + i * (kBN * 64) + pg * (kPageTokens * 64), map, bar, i * 64, 0, row);
+                for (int i = 0; i < kBoxes; ++i)
+                    tma_load_3d(dst + i * (kBN * 64) + pg * (kPageTokens * 64), map, bar, i * 64, 0, row);
+            }
         }
     };
     int fills = u_begin;
@@ -348,7 +296,10 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
         const int slot = u % kStagesOf<D>, use = u / kStagesOf<D>;
         if (use > 0 && !mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 1)) break;
         const bool has_k = u < n_all, has_v = u > 0;
-        mbar_arrive_expect_tx(&sm.u_full[slot], ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kBoxes * kKvBoxBytes<D>);
+        // e4m3 pages: the codes complete c_full, and the converters then complete u_full
+        uint64_t *full = (M == kPagedE4m3) ? &sm.c_full[slot] : &sm.u_full[slot];
+        constexpr uint32_t kTileBytes = (M == kPagedE4m3) ? (uint32_t)kBN * 128 : kBoxes * kKvBoxBytes<D>;
+        mbar_arrive_expect_tx(full, ((has_k ? 1 : 0) + (has_v ? 1 : 0)) * kTileBytes);
         if constexpr (M == kContig) {
             if (has_k) {
 #pragma unroll
@@ -371,8 +322,8 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
                 ids_cur[pg] = ids_next[pg];
             }
             if (u + 1 < n_all) fetch_ids(u + 1, ids_next);
-            if (has_k) load_tile(sm.k[slot], tmK, &sm.u_full[slot], ids_cur);
-            if (has_v) load_tile(sm.v[slot], tmV, &sm.u_full[slot], ids_prev);
+            if (has_k) load_tile(sm.k[slot], tmK, full, ids_cur);
+            if (has_v) load_tile(sm.v[slot], tmV, full, ids_prev);
         }
         ++fills;
     }
@@ -381,57 +332,46 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
         WaitCtx drain{nullptr, wc.status};
         (void)mbar_wait(&sm.q_full, 0, drain, 90);
         for (int f = (fills > kStagesOf<D> ? fills - kStagesOf<D> : 0); f < fills; ++f)
-            (void)mbar_wait(&sm.u_full[f % kStagesOf<D>], (uint32_t)((f / kStagesOf<D>) & 1), drain, 91);
+            (void)mbar_wait(M == kPagedE4m3 ? &sm.c_full[f % kStagesOf<D>] : &sm.u_full[f % kStagesOf<D>],
+                            (uint32_t)((f / kStagesOf<D>) & 1), drain, 91);
     }
 }
 
 // ------------------------------------------------------------------ e4m3 converters
-// Two warps widen each staged e4m3 tile into its ring slot (keys to bf16, values to f16), in the
-// layout a TMA load with the 128-byte swizzle gives (16-byte chunk c of row r of a 64-column box at
-// chunk c ^ (r % 8)), so the MMA issuer reads it exactly as a loaded tile.  Each e4m3 value is a
-// bf16 and an f16 value (the widening is exact); the tensor scales fold elsewhere (the key scale
-// into the score scale, the value scale into the epilogue).  Rows of pages that were not loaded become zeros.  A ring unit {K(u), V(u-1)}
-// is complete when both are written: the converters fence their shared-memory writes for the async
-// proxy, meet at a named barrier, and one of them arrives on the unit's full barrier.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-    return pack_bf16x2(f.x, f.y);
-}
-
+// The converter warps widen each ring unit's e4m3 codes to f16 in place, into the layout a TMA
+// load with the 128-byte swizzle gives (16-byte chunk c of row r of a 64-column box at chunk
+// c ^ (r % 8)), so the MMA issuer reads the tile exactly as a loaded bf16 one.  Each e4m3 value is
+// an f16 value (the widening is exact, one conversion per pair); the tensor scales fold elsewhere
+// (the key scale into the score scale, the value scale into the epilogue), and Q is rounded to f16
+// by the softmax warps (run_softmax).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
-// Widens one staged e4m3 tile into a ring slot: bf16 (keys: the type of Q) or f16 (values: the
-// type P is packed in).  Both are exact: every e4m3 value is a bf16 and an f16 value.
-template <int D, bool F16, int NCV>
-__device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, __nv_bfloat16 *dst, int ct) {
+// Widens one tile in place.  Row r's codes (128 bytes at kCodeOff + 128 r) lie inside the bytes of
+// row r of the tile's last box, and nothing else of the f16 tile overlaps them, so a warp that owns
+// whole rows reads a row's codes, meets at __syncwarp, and writes the row over them: no other warp
+// touches those bytes.  Lanes take 16-code chunks, kPad/16 lanes per row.
+template <int D, int kCW>
+__device__ __forceinline__ void widen_in_place(__nv_bfloat16 *tile, int cw, int lane) {
     constexpr int kBN = kBNd<D>;
-    constexpr int kChunksPerRow = D / 16;  // 16-byte chunks of e4m3 per row
-    uint8_t *d8 = reinterpret_cast<uint8_t *>(dst);
-#pragma unroll 4
-    for (int idx = ct; idx < kBN * kChunksPerRow; idx += NCV) {
-        const int r = idx / kChunksPerRow, c16 = idx % kChunksPerRow;
-        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-        if ((loaded >> (r / kPageTokens)) & 1u) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + r * D + c16 * 16);
-            if constexpr (F16) {
-                lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
-                                e4m3x2_to_f16x2(v.y >> 16));
-                hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
-                                e4m3x2_to_f16x2(v.w >> 16));
-            } else {
-                lo = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
-                                e4m3x2_to_bf16x2(v.y >> 16));
-                hi = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
-                                e4m3x2_to_bf16x2(v.w >> 16));
-            }
-        }
-        const int col = c16 * 16;               // first of the 16 columns
-        const int box = col >> 6, k0 = (col & 63) >> 3;  // 16-byte chunks k0, k0 + 1 of the row
-        uint8_t *row = d8 + box * (kBN * 128) + r * 128;
+    constexpr int kLanesPerRow = kPad<D> / 16;  // the chunks that carry columns < kPad
+    constexpr int kRowsPerStep = 32 / kLanesPerRow;
+    static_assert(kBN % kRowsPerStep == 0, "whole steps of rows");
+    uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
+    const int rsub = lane / kLanesPerRow, c16 = lane % kLanesPerRow;
+    const int box = c16 >> 2, k0 = (c16 & 3) * 2;  // the row's 16-byte f16 chunks k0, k0 + 1 of this box
+#pragma unroll 2
+    for (int r0 = cw * kRowsPerStep; r0 < kBN; r0 += kCW * kRowsPerStep) {
+        const int r = r0 + rsub;
+        const uint4 v = *reinterpret_cast<const uint4 *>(t8 + kCodeOff<D> + r * 128 + c16 * 16);
+        __syncwarp();
+        const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                                    e4m3x2_to_f16x2(v.y >> 16));
+        const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                                    e4m3x2_to_f16x2(v.w >> 16));
+        uint8_t *row = t8 + box * (kBN * 128) + r * 128;
         *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) = lo;
         *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ (r & 7)) << 4)) = hi;
     }
@@ -440,49 +380,21 @@ __device__ __forceinline__ void widen_tile(const uint8_t *src, uint32_t loaded, 
 // NCV converter threads (the warps after the MMA issuer's).
 template <int D> constexpr int kConverters = Occ<D, kPagedE4m3>::kThreads - (Cfg<D>::kMmaWarp + 1) * 32;
 
+// Per ring unit u = {K(u), V(u-1)}: wait for its codes, widen them, fence the writes for the async
+// proxy, and arrive (one lane per warp) on the unit's full barrier, which completes when every
+// converter warp has.
 template <int D>
 __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, WaitCtx wc) {
-    constexpr int NCV = kConverters<D>;
-    // every converter arrives, then waits for the phase to complete (bounded like every wait)
-    uint32_t cv_phase = 0;
-    auto sync_converters = [&]() -> bool {
-        mbar_arrive(&sm.st.cv_bar);
-        const bool done = __all_sync(0xffffffffu, mbar_wait(&sm.st.cv_bar, cv_phase & 1u, wc, 7));
-        ++cv_phase;
-        return done;
-    };
-    bool ok = true;
-    int kf = 0, vf = 0;
-    for (int u = 0; u <= n_all && ok; ++u) {
+    constexpr int kCW = kConverters<D> / 32;
+    const int cw = ct >> 5, lane = ct & 31;
+    for (int u = 0; u <= n_all; ++u) {
         const int slot = u % kStagesOf<D>, use = u / kStagesOf<D>;
-        if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.u_empty[slot], (uint32_t)((use - 1) & 1), wc, 4))) {
-            ok = false;
-            break;
-        }
-        if (u < n_all) {  // K(u): stage -> slot u % 2
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.st.k_full, (uint32_t)(kf & 1), wc, 5))) {
-                ok = false;
-                break;
-            }
-            widen_tile<D, false, NCV>(sm.st.k, sm.st.k_loaded, sm.k[slot], ct);
-            if (!(ok = sync_converters())) break;
-            if (ct == 0) mbar_arrive(&sm.st.k_empty);
-            ++kf;
-        }
-        if (u > 0) {  // V(u-1): stage -> slot u % 2
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.st.v_full, (uint32_t)(vf & 1), wc, 6))) {
-                ok = false;
-                break;
-            }
-            widen_tile<D, true, NCV>(sm.st.v, sm.st.v_loaded, sm.v[slot], ct);
-            ++vf;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.c_full[slot], (uint32_t)(use & 1), wc, 5))) break;
+        if (u < n_all) widen_in_place<D, kCW>(sm.k[slot], cw, lane);
+        if (u > 0) widen_in_place<D, kCW>(sm.v[slot], cw, lane);
         fence_proxy_async_smem();  // this thread's tile writes, before the MMA's reads
-        if (!(ok = sync_converters())) break;
-        if (ct == 0) {
-            if (u > 0) mbar_arrive(&sm.st.v_empty);
-            mbar_arrive(&sm.u_full[slot]);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.u_full[slot]);
     }
 }
 
@@ -490,9 +402,10 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
 template <int D, int M>
 __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQTilesMax], int n_all, WaitCtx wc) {
     constexpr int kBN = kBNd<D>;
-    constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
-    // e4m3 pages: V is widened to f16 and P packed as f16, so PV runs f16 x f16 (the key tile
-    // stays bf16, the type of Q)
+    // e4m3 pages: Q, K and V are f16 in shared memory and P is packed as f16, so both products run
+    // f16 x f16
+    constexpr uint32_t idS =
+        M == kPagedE4m3 ? idesc_f16_f32(kBM, kBN, false, false) : idesc_bf16_f32(kBM, kBN, false, false);
     constexpr uint32_t idPV =
         M == kPagedE4m3 ? idesc_f16_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
 
@@ -529,7 +442,10 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
     // The data waits below (Q, ring units) need no tcgen05 fence: TMA writes and the MMA's
     // operand reads are both async-proxy traffic ordered by the mbarrier.  The P waits do
     // (P was written to TMEM by other threads).
-    bool ok = mbar_wait(&sm.q_full, 0, wc, 11) && mbar_wait(&sm.u_full[0], 0, wc, 10);
+    bool ok = mbar_wait(&sm.q_full, 0, wc, 11);
+    if constexpr (M == kPagedE4m3)  // the Q tiles rounded to f16 in place (generic-proxy writes, fenced)
+        for (int t = 0; t < Cfg<D>::QT && ok; ++t) ok = mbar_wait(&sm.q_conv[t], 0, wc, 14);
+    ok = ok && mbar_wait(&sm.u_full[0], 0, wc, 10);
     if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < Cfg<D>::QT; ++t)
@@ -636,6 +552,39 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[2][32], uint32_t t
     }
 }
 
+// Row r of a Q tile (kPad/64 boxes of kBM x 64 bf16, 128-byte swizzle) rounded to f16 in place after
+// the factor 2^-sh, sh = 0 unless |q| reaches 2^15 (then the smallest that brings the row below 2^15,
+// at most 113); returns 2^sh.  Chunk j of the row is read from position j ^ (r % 8) so that eight
+// consecutive rows fall in different banks.
+template <int D>
+__device__ __forceinline__ float q_row_to_f16(__nv_bfloat16 *qt, int r) {
+    constexpr int kBx = kPad<D> / 64;
+    uint8_t *base = reinterpret_cast<uint8_t *>(qt) + r * 128;
+    uint4 v[kBx * 8];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBx * 8; ++i) {
+        v[i] = *reinterpret_cast<const uint4 *>(base + (i >> 3) * (kBM * 128) + (((i & 7) ^ (r & 7)) << 4));
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+    }
+    const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+    const int sh = e >= 15 ? min(e - 14, 113) : 0;
+    const float f = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+    for (int i = 0; i < kBx * 8; ++i) {
+        uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = pack_f16x2(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xffff0000u) * f);
+        *reinterpret_cast<uint4 *>(base + (i >> 3) * (kBM * 128) + (((i & 7) ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return __uint_as_float((uint32_t)(127 + sh) << 23);
+}
+
 template <int D, int M>
 __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, const CUtensorMap *tmO, uint32_t tmem,
                             int t, int bh, int q0, int n_tiles, int n_all, int kv_end, int delta, WaitCtx wc) {
@@ -648,7 +597,18 @@ __device__ void run_softmax(PrefillSmem<D, M> &sm, const PrefillParams &p, const
     const uint32_t tO = lane_base + o_col<D>(t);
     const int qs = q0 + t * kBM;  // first row of this tile
     const int row = qs + r;
-    const float c = p.scale_log2;
+    float c = p.scale_log2;
+    if constexpr (M == kPagedE4m3) {
+        // Over e4m3 pages the products run in f16: each thread rounds its Q row to f16 in place once
+        // Q has landed, after a power-of-two factor 2^-sh that keeps the row below 2^15 (exact for
+        // every value in f16's normal range), and folds 2^sh into its score scale.
+        if (n_all > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, wc, 25))) return;
+            c *= q_row_to_f16<D>(sm.q[t], r);
+            fence_proxy_async_smem();  // before the MMA's reads of the tile
+            mbar_arrive(&sm.q_conv[t]);
+        }
+    }
     const uint64_t c2 = f32x2_pack(c, c);
 
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by l and O
@@ -860,23 +820,19 @@ __global__ void __launch_bounds__((Occ<D, M>::kThreads), (Occ<D, M>::kMinBlocks)
     if (producer) {
         mbar_init(&sm.q_full, 1);
         for (int s = 0; s < kStagesOf<D>; ++s) {
-            mbar_init(&sm.u_full[s], 1);
+            // e4m3 pages: the unit is full once every converter warp has widened its rows
+            mbar_init(&sm.u_full[s], M == kPagedE4m3 ? kConverters<D> / 32 : 1);
             mbar_init(&sm.u_empty[s], 1);
+            mbar_init(&sm.c_full[s], 1);
         }
         for (int t = 0; t < Cfg<D>::QT; ++t) {
             mbar_init(&sm.s_full[t], 1);
             mbar_init(&sm.p_full[t], kBM);
             mbar_init(&sm.o_done[t], 1);
             mbar_init(&sm.o_staged[t], kBM);
+            mbar_init(&sm.q_conv[t], kBM);
         }
         mbar_init(&sm.drain, 1);
-        if constexpr (M == kPagedE4m3) {
-            mbar_init(&sm.st.k_full, 1);
-            mbar_init(&sm.st.v_full, 1);
-            mbar_init(&sm.st.k_empty, 1);
-            mbar_init(&sm.st.v_empty, 1);
-            mbar_init(&sm.st.cv_bar, kConverters<D>);
-        }
         sm.abort_flag = 0;
         fence_mbar_init();
         if constexpr (M == kContig) {
@@ -947,8 +903,9 @@ cudaError_t launch_prefill_dm(const PrefillArgs &a, cudaStream_t stream) {
     else if constexpr (M == kContig)  // boxes of kBNd<D> key rows
         ok_maps = ok_maps && encode_qkv_map(&tk, a.k, BHkv, a.Nkv, D, kBNd<D>) &&
                   encode_qkv_map(&tv, a.v, BHkv, a.Nkv, D, kBNd<D>);
-    else  // e4m3 pages travel by plain bulk copies: the K/V maps are not used
-        tk = tv = tq;
+    else  // e4m3 pages: one box of 16 rows x 128 codes per page (zeros past d), unswizzled
+        ok_maps = ok_maps && encode_page_map_u8(&tk, a.k, a.num_pages * a.Hkv, kPageTokens, D, false) &&
+                  encode_page_map_u8(&tv, a.v, a.num_pages * a.Hkv, kPageTokens, D, false);
     if (!ok_maps) return cudaErrorInvalidValue;
     cudaError_t e = check_register_split<D, M>();
     if (e != cudaSuccess) return e;

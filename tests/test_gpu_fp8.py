@@ -206,6 +206,33 @@ def test_paged_prefill_fp8_vs_oracle(lib, oracle_mod, case):
     assert not og[inf].any()
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_paged_prefill_fp8_query_beyond_fp16_range(lib, oracle_mod, d):
+    # over e4m3 pages the products run in fp16 with each query row brought below 2^15 by a power of
+    # two: rows of magnitude ~1e5 (past fp16's 65504) next to rows of ordinary size, with a softmax
+    # scale that keeps the large rows' scores O(1), must give the oracle's attention
+    B, H, Hkv, Nq, ctx = 2, 4, 2, 150, [150, 900]
+    shape = workloads.DecodeShape("fp8 prefill big q", B, H, d, (1, max(ctx)), seed=770 + d)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
+    g = torch.Generator().manual_seed(771)
+    big = 3.0e4
+    rows = torch.where(torch.rand(B, H, Nq, 1, generator=g) < 0.5, big, 1.0)
+    q = (torch.randn(B, H, Nq, d, generator=g) * rows).to(torch.bfloat16)
+    scale = shape.scale / big
+    kc = torch.from_numpy(oracle_mod.e4m3_quantize(inp["k_pages"], KV_SCALE))
+    vc = torch.from_numpy(oracle_mod.e4m3_quantize(inp["v_pages"], KV_SCALE))
+    o, lse = lib.paged_attn_prefill_fp8(q.cuda(), kc.cuda(), vc.cuda(), KV_SCALE, KV_SCALE,
+                                        inp["page_table"].cuda(), inp["ctx_lens"].cuda(), True, scale)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_prefill_fp8_gqa(q, kc, vc, KV_SCALE, KV_SCALE, inp["page_table"],
+                                                      inp["ctx_lens"], True, scale)
+    og = o.float().cpu().numpy().astype(np.float64)
+    err = np.abs(og - o_ref)
+    assert np.isfinite(og).all() and err.max() <= O_MAX and err.mean() <= O_MEAN, (err.max(), err.mean())
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
+
+
 def test_append_fp8_then_paged_prefill_fp8_with_unmapped_pages(lib, oracle_mod):
     # a serving step over an e4m3 cache: append the chunk's K/V (converted), then attend; one page
     # of the table is unmapped (its positions hold no token), as on every paged entry point
