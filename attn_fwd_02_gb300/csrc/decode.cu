@@ -480,12 +480,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
     return r;
 }
-// Two e4m3 codes (the low 16 bits, low byte first) -> an f16x2 word (exact: every e4m3 value is
-// an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
 
 // Byte offset of the 16-byte chunk holding column col (a multiple of 8) of row r in a page block
 // stored as 128-byte-swizzled boxes of 16 rows x 64 bf16 columns.
@@ -690,11 +684,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 for (int ks = 0; ks < KS; ks += 2) {
                     uint32_t bk[4];  // tokens 0-7 / 8-15 of chunk ks, then of chunk ks + 1 (zeros past D)
                     ldsm_x4(Ks + f_off(f_row, ks + f_chunk), bk);
-                    mma_16816_f16(sc[0], qa[ks], e4m3x2_f16x2(bk[0]), e4m3x2_f16x2(bk[0] >> 16));
-                    mma_16816_f16(sc[1], qa[ks], e4m3x2_f16x2(bk[1]), e4m3x2_f16x2(bk[1] >> 16));
+                    uint32_t b[4][2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(bk[i], b[i][0], b[i][1]);
+                    mma_16816_f16(sc[0], qa[ks], b[0][0], b[0][1]);
+                    mma_16816_f16(sc[1], qa[ks], b[1][0], b[1][1]);
                     if (ks + 1 < KS) {
-                        mma_16816_f16(sc[0], qa[ks + 1], e4m3x2_f16x2(bk[2]), e4m3x2_f16x2(bk[2] >> 16));
-                        mma_16816_f16(sc[1], qa[ks + 1], e4m3x2_f16x2(bk[3]), e4m3x2_f16x2(bk[3] >> 16));
+                        mma_16816_f16(sc[0], qa[ks + 1], b[2][0], b[2][1]);
+                        mma_16816_f16(sc[1], qa[ks + 1], b[3][0], b[3][1]);
                     }
                 }
             } else {
@@ -767,9 +764,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                     for (int j = 0; j < 2; ++j) {
                         if (ch + j < KS) {
                             // {tok 2t dim 2g, tok 2t+1 dim 2g} | {tok 2t dim 2g+1, tok 2t+1 dim 2g+1}
-                            const uint32_t lo = prmt(bv[2 * j], 0u, 0x3120u), hi = prmt(bv[2 * j + 1], 0u, 0x3120u);
-                            mma_16816_f16(o[2 * (ch + j)], pa, e4m3x2_f16x2(lo), e4m3x2_f16x2(hi));
-                            mma_16816_f16(o[2 * (ch + j) + 1], pa, e4m3x2_f16x2(lo >> 16), e4m3x2_f16x2(hi >> 16));
+                            uint32_t e0, o0, e1, o1;  // even / odd dim of tokens 2t, 2t+1 and of 2t+8, 2t+9
+                            e4m3x4_to_f16x2x2(prmt(bv[2 * j], 0u, 0x3120u), e0, o0);
+                            e4m3x4_to_f16x2x2(prmt(bv[2 * j + 1], 0u, 0x3120u), e1, o1);
+                            mma_16816_f16(o[2 * (ch + j)], pa, e0, e1);
+                            mma_16816_f16(o[2 * (ch + j) + 1], pa, o0, o1);
                         }
                     }
                 }

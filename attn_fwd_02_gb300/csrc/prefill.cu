@@ -344,11 +344,6 @@ __device__ void run_producer(PrefillSmem<D, M> &sm, const PrefillParams &p, cons
 // an f16 value (the widening is exact, one conversion per pair); the tensor scales fold elsewhere
 // (the key scale into the score scale, the value scale into the epilogue), and Q is rounded to f16
 // by the softmax warps (run_softmax).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
 // Widens one tile in place.  Row r's codes (128 bytes at kCodeOff + 128 r) lie inside the bytes of
 // row r of the tile's last box, and nothing else of the f16 tile overlaps them, so a warp that owns
 // whole rows reads a row's codes, meets at __syncwarp, and writes the row over them: no other warp
@@ -367,10 +362,11 @@ __device__ __forceinline__ void widen_in_place(__nv_bfloat16 *tile, int cw, int 
         const int r = r0 + rsub;
         const uint4 v = *reinterpret_cast<const uint4 *>(t8 + kCodeOff<D> + r * 128 + c16 * 16);
         __syncwarp();
-        const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
-                                    e4m3x2_to_f16x2(v.y >> 16));
-        const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
-                                    e4m3x2_to_f16x2(v.w >> 16));
+        uint4 lo, hi;
+        e4m3x4_to_f16x2x2(v.x, lo.x, lo.y);
+        e4m3x4_to_f16x2x2(v.y, lo.z, lo.w);
+        e4m3x4_to_f16x2x2(v.z, hi.x, hi.y);
+        e4m3x4_to_f16x2x2(v.w, hi.z, hi.w);
         uint8_t *row = t8 + box * (kBN * 128) + r * 128;
         *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) = lo;
         *reinterpret_cast<uint4 *>(row + (((k0 + 1) ^ (r & 7)) << 4)) = hi;

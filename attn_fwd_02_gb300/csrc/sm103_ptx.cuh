@@ -98,6 +98,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCt
     return mbar_wait_slow(bar, parity, w, site);
 }
 
+// ---------------------------------------------------------------- e4m3
+// Four e4m3 codes (byte 0 lowest) -> two f16x2 words: lo = codes 0, 1 and hi = codes 2, 3, the lower
+// code in the lower half.  Exact: every e4m3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
