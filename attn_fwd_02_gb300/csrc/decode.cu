@@ -151,22 +151,41 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&f)[DPL
     }
 }
 
-// Two e4m3 codes (low byte first) -> two fp32 values (exact: every e4m3 value is an fp16 value).
+// Two e4m3 codes (the low 16 bits, low byte first) -> two fp32 values (exact: every e4m3 value is
+// an fp16 value, and every fp16 value an fp32 value).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    float2 r;
+    asm("{\n\t.reg .b16 l, h, a, b;\n\t.reg .b32 x;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 x, l;\n\t"
+        "mov.b32 {a, b}, x;\n\t"
+        "cvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(two));
+    return r;
+}
+
+// Four e4m3 codes (byte 0 lowest) -> four fp32 values (exact).
+__device__ __forceinline__ void e4m3x4_to_float4(uint32_t w, float (&f)[4]) {
+    uint32_t lo, hi;
+    e4m3x4_to_f16x2x2(w, lo, hi);
+    asm("{\n\t.reg .b16 a, b, c, d;\n\t"
+        "mov.b32 {a, b}, %4;\n\t"
+        "mov.b32 {c, d}, %5;\n\t"
+        "cvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t"
+        "cvt.f32.f16 %2, c;\n\t"
+        "cvt.f32.f16 %3, d;\n\t}"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+        : "r"(lo), "r"(hi));
 }
 
 // Load DPL consecutive e4m3 codes from shared memory as fp32 (unscaled).
 template <int DPL>
 __device__ __forceinline__ void load_e4m3(const uint8_t *p, float (&f)[DPL]) {
     if constexpr (DPL == 4) {
-        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
-        const float2 a = e4m3x2_to_float2(u), b = e4m3x2_to_float2(u >> 16);
-        f[0] = a.x;
-        f[1] = a.y;
-        f[2] = b.x;
-        f[3] = b.y;
+        e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(p), f);
     } else if constexpr (DPL == 2) {
         const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t *>(p));
         f[0] = a.x;
@@ -703,22 +722,24 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                     mma_16816(sc[1], qa[ks], bk[2], bk[3]);
                 }
             }
-            // log2-domain scores; this lane holds tokens nt*8 + (lane&3)*2 + {0,1} of rows r0 / r0+8
-            float x[2][4];
+            // this lane holds the scores of tokens nt*8 + (lane&3)*2 + {0,1} of rows r0 / r0+8; slots
+            // past the context end (only on a sequence's last page) become -inf
+            if (ntok < kPS) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = nt * 8 + kq + (i & 1);
-                    x[nt][i] = tok < ntok ? sc[nt][i] * c : -INFINITY;
-                }
+                    for (int i = 0; i < 4; ++i)
+                        if (nt * 8 + kq + (i & 1) >= ntok) sc[nt][i] = -INFINITY;
+            }
+            // row maxima of the raw scores, then the log2 domain (c > 0 keeps the order)
             float mx[2];
-            mx[0] = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-            mx[1] = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+            mx[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+            mx[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
                 mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                mx[h] *= c;
             }
             float al[2] = {1.f, 1.f};
             bool resc = false;
@@ -740,11 +761,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                 }
             }
             float p[2][4], ps[2] = {0.f, 0.f};
+            const float nm[2] = {-m_ref[0], -m_ref[1]};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    p[nt][i] = ex2_approx(x[nt][i] - m_ref[i >> 1]);
+                    p[nt][i] = ex2_approx(fmaf(sc[nt][i], c, nm[i >> 1]));
                     ps[i >> 1] += p[nt][i];
                 }
 #pragma unroll
