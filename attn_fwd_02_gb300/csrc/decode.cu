@@ -699,6 +699,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
             }
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             if constexpr (FP8) {
+                // even and odd chunks accumulate in separate tiles (two shorter dependency chains)
+                float sc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < KS; ks += 2) {
                     uint32_t bk[4];  // tokens 0-7 / 8-15 of chunk ks, then of chunk ks + 1 (zeros past D)
@@ -709,10 +711,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                     mma_16816_f16(sc[0], qa[ks], b[0][0], b[0][1]);
                     mma_16816_f16(sc[1], qa[ks], b[1][0], b[1][1]);
                     if (ks + 1 < KS) {
-                        mma_16816_f16(sc[0], qa[ks + 1], b[2][0], b[2][1]);
-                        mma_16816_f16(sc[1], qa[ks + 1], b[3][0], b[3][1]);
+                        mma_16816_f16(sc2[0], qa[ks + 1], b[2][0], b[2][1]);
+                        mma_16816_f16(sc2[1], qa[ks + 1], b[3][0], b[3][1]);
                     }
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sc[nt][i] += sc2[nt][i];
             } else {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
