@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) o[g][i] *= alpha;
             }
-            for (int t = 0; t < ntok; ++t) {
+            auto pv_token = [&](int t) {
                 float vf[DPL];
                 load_kv<D, FP8>(Vs + t * kRowBytes, lane, vf);
 #pragma unroll
@@ -395,6 +395,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
 #pragma unroll
                     for (int i = 0; i < DPL; ++i) o[g][i] = fmaf(pt, vf[i], o[g][i]);
                 }
+            };
+            // V rows past the context end are never read (they may hold anything); every page but a
+            // sequence's last is full and takes the unrolled form
+            if (ntok == kPS) {
+#pragma unroll
+                for (int t = 0; t < kPS; ++t) pv_token(t);
+            } else {
+                for (int t = 0; t < ntok; ++t) pv_token(t);
             }
         }
         // the slot is free again: order this warp's reads before the next bulk write
