@@ -75,17 +75,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 // 64-column boxes of a page block in the grouped-query kernel's swizzled layout (the columns past
 // D of the last box are read as zeros by TMA and never used by the products).
 template <int D> constexpr int kBoxes = (D + 63) / 64;
-// Bytes of one ring buffer (one page block of K or V): the bulk-copied block (kPS rows of D
-// elements), or the grouped-query kernel's swizzled TMA boxes: kBoxes boxes of 16 x 64 bf16, or
-// one box of 16 x 128 e4m3 codes.
-template <int D, int GP, bool FP8>
-constexpr int kSlotBytes = GP > 1 ? (FP8 ? kPS * 128 : kBoxes<D> * kPS * 128) : kPS * D * (FP8 ? 1 : 2);
+// Bytes of one ring buffer (one page block of K or V): the scalar kernel's bulk-copied block (kPS
+// rows of D elements), or the tensor-core kernel's swizzled TMA boxes: kBoxes boxes of 16 x 64
+// bf16, or one box of 16 x 128 e4m3 codes.
+template <int D, bool FP8> constexpr int kSlotBytes = kPS * D * (FP8 ? 1 : 2);
+template <int D, bool FP8> constexpr int kBoxSlotBytes = FP8 ? kPS * 128 : kBoxes<D> * kPS * 128;
 
 template <int D, int GP, bool FP8>
 struct DecodeSmem {
-    // [warp][slot][0 = K, 1 = V][one page block]; 16-byte aligned blocks (1024-byte alignment for
-    // the swizzled TMA boxes of the grouped-query mma kernel)
-    alignas(GP > 1 ? 1024 : 128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kSlotBytes<D, GP, FP8>];
+    // [warp][slot][0 = K, 1 = V][one page block]; 16-byte aligned blocks
+    alignas(128) uint8_t kv[kWarps][kSlotsFor<FP8, GP>][2][kSlotBytes<D, FP8>];
     uint64_t full[kWarps][kSlotsFor<FP8, GP>];
     float red_o[kWarps][GP][D];
     float red_m[kWarps][GP];
@@ -544,7 +543,7 @@ struct GqaMmaSmem {
     union {
         // [warp][slot][0 = K, 1 = V][one page block]: swizzled TMA boxes (bf16) or the bulk-copied
         // e4m3 block; 1024-byte aligned for the swizzled boxes
-        alignas(1024) uint8_t kv[kWarps][kGqaSlots<FP8>][2][kSlotBytes<D, GP, FP8>];
+        alignas(1024) uint8_t kv[kWarps][kGqaSlots<FP8>][2][kBoxSlotBytes<D, FP8>];
         struct {
             float o[kWarps][GP][D];
             float m[kWarps][GP];
@@ -560,7 +559,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gqa_mma_kernel(const __gri
                                                                      const __grid_constant__ CUtensorMap tmV,
                                                                      const DecodeArgs a, int max_splits, int Hkv,
                                                                      int gsplit) {
-    static_assert(GP >= 2 && GP <= 16, "query heads per CTA");
+    static_assert(GP >= 1 && GP <= 16, "query heads per CTA");
     static_assert(D % 16 == 0, "k-steps of 16");
     constexpr int kSl = kGqaSlots<FP8>;
     constexpr int kBx = FP8 ? 1 : kBoxes<D>;              // TMA boxes per page block (128-byte rows)
@@ -984,14 +983,29 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t 
     return cudaGetLastError();
 }
 
+// Multi-head attention (one query head per CTA) runs on the tensor-core kernel where that measured
+// faster than the scalar kernel, whose per-token shuffles (a 16-token reduce-scatter and 16
+// broadcasts per page) do not shrink with d.  Fraction of HBM on 32 sequences x 32 heads, contexts
+// U[512, 8192], scalar / tensor-core: bf16 d = 32 0.81 / 0.64, 64 0.96 / 0.99, 80 0.96 / 0.96,
+// 96 1.00 / 1.00; e4m3 d = 32 0.41 / 0.45, 64 0.69 / 0.66, 80 0.63 / 0.52, 96 0.81 / 0.84.  Both
+// split at 1024 tokens below d = 128.
+template <int D, bool FP8> constexpr bool kMhaOnMma = FP8 ? (D == 32 || D == 96) : (D == 64);
+
+template <int D, bool FP8>
+cudaError_t launch_decode_gf(const DecodeArgs &a, int max_splits, int chunk, cudaStream_t stream) {
+    static_assert(!kMhaOnMma<D, FP8> || mha_chunk_tokens(D) == kGqaChunkTokens, "the workspace's split length");
+    if constexpr (kMhaOnMma<D, FP8>) return launch_decode_mma<D, 1, FP8>(a, max_splits, stream);
+    else return launch_decode_g<D, 1, FP8>(a, max_splits, chunk, stream);
+}
+
 template <int D, int GP>
 cudaError_t launch_decode_gk(const DecodeArgs &a, int max_splits, int chunk, cudaStream_t stream) {
     if constexpr (GP >= 2) {
         return a.kv_fp8 ? launch_decode_mma<D, GP, true>(a, max_splits, stream)
                         : launch_decode_mma<D, GP, false>(a, max_splits, stream);
     } else {
-        return a.kv_fp8 ? launch_decode_g<D, GP, true>(a, max_splits, chunk, stream)
-                        : launch_decode_g<D, GP, false>(a, max_splits, chunk, stream);
+        return a.kv_fp8 ? launch_decode_gf<D, true>(a, max_splits, chunk, stream)
+                        : launch_decode_gf<D, false>(a, max_splits, chunk, stream);
     }
 }
 
