@@ -109,11 +109,13 @@ template <int D, int M> struct Occ {
     static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;
 };
 // e4m3 pages at d > 64: a fourth warpgroup widens with the third's two idle warps -- six converter
-// warps -- launched at 128 registers (512 threads); the two non-softmax warpgroups keep 40 each:
-// 128 x (2 x 216 + 2 x 40) = 65536.
+// warps -- launched at 128 registers (512 threads); the two non-softmax warpgroups keep 64 each:
+// 128 x (2 x 192 + 2 x 64) = 65536.  Measured (TFLOP/s on the chunked prefill over e4m3 pages) for
+// softmax / other: 216 / 40 889, 208 / 48 914, 200 / 56 993, 192 / 64 995, 184 / 72 985, 168 / 88 976
+// (at 40 the producer and converters spill).
 template <int D> struct OccWide {
     static constexpr int kMinBlocks = 1, kThreads = 512;
-    static constexpr uint32_t kRegsSoftmax = 216, kRegsOther = 40;
+    static constexpr uint32_t kRegsSoftmax = 192, kRegsOther = 64;
 };
 template <> struct Occ<80, kPagedE4m3> : OccWide<80> {};
 template <> struct Occ<96, kPagedE4m3> : OccWide<96> {};
