@@ -541,8 +541,8 @@ struct GqaMmaSmem {
     // The page ring and the final merge's arrays are never in use at the same time (the merge
     // starts after every warp has consumed its last page), so they share their bytes.
     union {
-        // [warp][slot][0 = K, 1 = V][one page block]: swizzled TMA boxes (bf16) or the bulk-copied
-        // e4m3 block; 1024-byte aligned for the swizzled boxes
+        // [warp][slot][0 = K, 1 = V][one page block]: swizzled TMA boxes (16 x 64 bf16 each, or one
+        // of 16 x 128 e4m3 codes); 1024-byte aligned for the swizzle
         alignas(1024) uint8_t kv[kWarps][kGqaSlots<FP8>][2][kBoxSlotBytes<D, FP8>];
         struct {
             float o[kWarps][GP][D];

@@ -101,9 +101,10 @@ constexpr int kPageTokens = 16;            // tokens per page of the paged KV ca
 // pages, widened to f16 in shared memory before the products.
 enum KvMode : int { kContig = 0, kPagedBf16 = 1, kPagedE4m3 = 2 };
 
-// CTAs per SM and the register split per KV mode: the e4m3 staging (two tiles of codes) makes a
-// d <= 64 CTA 56 KB, so three of them share an SM, launched at 80 registers (128 x (104 + 56) =
-// 20480 = 256 x 80); the converter warps take registers from the producer's warpgroup.
+// CTAs per SM and the register split per KV mode.  e4m3 pages at d <= 64: the two converter warps
+// (the non-softmax warpgroup's idle pair) need more than the 32 registers that four CTAs per SM
+// would leave them, so three CTAs share an SM, launched at 80 registers (128 x (104 + 56) = 20480 =
+// 256 x 80).
 template <int D, int M> struct Occ {
     static constexpr int kMinBlocks = Cfg<D>::kMinBlocks, kThreads = Cfg<D>::kThreads;
     static constexpr uint32_t kRegsSoftmax = Cfg<D>::kRegsSoftmax, kRegsOther = Cfg<D>::kRegsOther;

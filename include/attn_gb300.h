@@ -236,12 +236,16 @@ int paged_kv_append(const void *k_new, const void *v_new, void *k_pages, void *v
  *   [num_pages, Hkv, page_size, d] uint8 codes; k_scale, v_scale > 0 and finite): the
  *   chunked prefill of a serving loop that keeps its cache in e4m3.  q, o, lse, the
  *   table, the masks and the result are as in paged_attn_prefill, for the dequantised
- *   cache.  The codes are widened exactly to bf16 in shared memory before the products;
- *   the key scale multiplies the scores and the value scale the output.
+ *   cache.  The codes are widened exactly to f16 in shared memory and both products run
+ *   in f16 with fp32 accumulation: each query row is rounded to f16 after a power-of-two
+ *   factor that keeps it below 2^15 (exact for bf16 values in f16's normal range).  The
+ *   key scale multiplies the scores and the value scale the output.
  * paged_attn_decode_fp8: paged_attn_decode_gqa over an e4m3 cache (k_pages,
  *   v_pages [num_pages, Hkv, page_size, d] uint8 codes; k_scale, v_scale > 0
  *   and finite).  q, o, lse, the table, the workspace and the result are as in
- *   paged_attn_decode_gqa, for the dequantised cache.
+ *   paged_attn_decode_gqa, for the dequantised cache.  The codes are widened exactly
+ *   to f16 or fp32; where the products run on tensor cores they run in f16 with fp32
+ *   accumulation, the query rounded to f16 after a power-of-two factor as above.
  * kv_quantize_fp8: n contiguous bf16 elements of src -> n codes in dst (n a
  *   multiple of 8; both 16-byte aligned).  Converts a whole bf16 page pool.
  * paged_kv_append_fp8: paged_kv_append into an e4m3 cache, converting each new
