@@ -267,6 +267,27 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
     return x + __shfl_xor_sync(0xffffffffu, x, 1);
 }
 
+// Multi-head decode at d = 32 and 64 splits the warp into groups of T = d / 4 lanes, each lane
+// holding 4 consecutive dims of one token, and the 32 / T groups take different tokens of a page in
+// each round.  A score then needs a sum over T lanes only (3 or 4 shuffles instead of a 16-token
+// reduce-scatter), and each group keeps its own tokens' probabilities for O += P V (no per-token
+// broadcasts); the groups' partial O are summed once per CTA.  At d = 128 a token fills the warp.
+template <int D> constexpr bool kLaneGroups = (D == 32 || D == 64);
+
+// Four consecutive elements of a cache row (bf16, or e4m3 codes) as fp32.
+template <bool FP8>
+__device__ __forceinline__ void load4(const uint8_t *p, float (&f)[4]) {
+    if constexpr (FP8) {
+        e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(p), f);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
 // One CTA: one chunk of one sequence's cache for one key/value head, applied to GP query
 // heads that share that head (grouped-query attention; GP = 1 for multi-head attention).
 // Grid (chunks, Hkv * gsplit, B): blockIdx.y = kv_head * gsplit + group slice.
@@ -345,6 +366,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
 #pragma unroll
         for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
     }
+    // lane groups (d = 32, 64): this lane's token group and its dims 4 cq .. 4 cq + 3
+    constexpr int kT = kLaneGroups<D> ? D / 4 : 32;  // lanes per token
+    constexpr int kG = 32 / kT;                      // tokens per round
+    constexpr int kR = kPS / kG;                     // rounds per page
+    const int gq = lane / kT, cq = lane % kT;
+    float q4[4] = {0.f, 0.f, 0.f, 0.f}, o4[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (kLaneGroups<D>) {
+        load4<false>(reinterpret_cast<const uint8_t *>(a.q) + (((size_t)b * a.H + qh0) * D + 4 * cq) * 2, q4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q4[i] *= c;
+    }
 
     int issued = first;
     bool failed = false;
@@ -357,7 +389,64 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, k) != 0;
         const int page_tok0 = tok0 + (warp + kWarps * k) * kPS;
         const int ntok = min(kPS, tok1 - page_tok0);
-        if (ok) {
+        if (ok && kLaneGroups<D>) {
+            const uint8_t *Ks = sm.kv[warp][slot][0];
+            const uint8_t *Vs = sm.kv[warp][slot][1];
+            // round r: token r * kG + gq of the page, scored by its group of kT lanes
+            float x[kR];
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                float k4[4];
+                load4<FP8>(Ks + (r * kG + gq) * kRowBytes + 4 * cq * kElem, k4);
+                float acc = q4[0] * k4[0];
+                acc = fmaf(q4[1], k4[1], acc);
+                acc = fmaf(q4[2], k4[2], acc);
+                acc = fmaf(q4[3], k4[3], acc);
+#pragma unroll
+                for (int off = 1; off < kT; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                x[r] = acc;
+            }
+            if (ntok < kPS) {  // slots past the context end (a sequence's last page)
+#pragma unroll
+                for (int r = 0; r < kR; ++r)
+                    if (r * kG + gq >= ntok) x[r] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int r = 1; r < kR; ++r) mx = fmaxf(mx, x[r]);
+#pragma unroll
+            for (int off = kT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m_run[0], mx);  // finite: ntok >= 1
+            const float alpha = ex2_approx(m_run[0] - m_new);
+            float pr[kR], ps = 0.f;
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                pr[r] = ex2_approx(x[r] - m_new);
+                ps += pr[r];
+            }
+            // each group's lanes hold the same values: sum over the groups only
+#pragma unroll
+            for (int off = kT; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            l_run[0] = l_run[0] * alpha + ps;
+            m_run[0] = m_new;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o4[i] *= alpha;
+            auto pv_round = [&](int r) {
+                float v4[4];
+                load4<FP8>(Vs + (r * kG + gq) * kRowBytes + 4 * cq * kElem, v4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o4[i] = fmaf(pr[r], v4[i], o4[i]);
+            };
+            // V rows past the context end are never read (they may hold anything)
+            if (ntok == kPS) {
+#pragma unroll
+                for (int r = 0; r < kR; ++r) pv_round(r);
+            } else {
+#pragma unroll
+                for (int r = 0; r < kR; ++r)
+                    if (r * kG + gq < ntok) pv_round(r);
+            }
+        } else if (ok) {
             const uint8_t *Ks = sm.kv[warp][slot][0];
             const uint8_t *Vs = sm.kv[warp][slot][1];
             // this lane's DPL dims of the 16 keys, read once and used for every query head
@@ -423,15 +512,28 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     }
 
     // merge the four warp states of every query head
+    if constexpr (kLaneGroups<D>) {  // the token groups' partial O (they share m_run)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int off = kT; off < 32; off <<= 1) o4[i] += __shfl_xor_sync(0xffffffffu, o4[i], off);
+    }
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
         if (lane == 0) {
             sm.red_m[warp][g] = m_run[g];
             sm.red_l[warp][g] = l_run[g];
         }
+        if constexpr (kLaneGroups<D>) {
+            if (gq == 0) {
 #pragma unroll
-        for (int i = 0; i < DPL; ++i)
-            if (LD::has(lane, i)) sm.red_o[warp][g][LD::dim(lane, i)] = o[g][i];
+                for (int i = 0; i < 4; ++i) sm.red_o[warp][g][4 * cq + i] = o4[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < DPL; ++i)
+                if (LD::has(lane, i)) sm.red_o[warp][g][LD::dim(lane, i)] = o[g][i];
+        }
     }
     __syncthreads();
     if (sm.abort_flag) return;
@@ -984,12 +1086,11 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, int max_splits, cudaStream_t 
 }
 
 // Multi-head attention (one query head per CTA) runs on the tensor-core kernel where that measured
-// faster than the scalar kernel, whose per-token shuffles (a 16-token reduce-scatter and 16
-// broadcasts per page) do not shrink with d.  Fraction of HBM on 32 sequences x 32 heads, contexts
-// U[512, 8192], scalar / tensor-core: bf16 d = 32 0.81 / 0.64, 64 0.96 / 0.99, 80 0.96 / 0.96,
-// 96 1.00 / 1.00; e4m3 d = 32 0.41 / 0.45, 64 0.69 / 0.66, 80 0.63 / 0.52, 96 0.81 / 0.84.  Both
-// split at 1024 tokens below d = 128.
-template <int D, bool FP8> constexpr bool kMhaOnMma = FP8 ? (D == 32 || D == 96) : (D == 64);
+// faster than the scalar kernel.  Fraction of HBM on 32 sequences x 32 heads, contexts U[512, 8192],
+// scalar / tensor-core: bf16 d = 32 0.90 / 0.64, 64 0.96 / 0.97, 80 0.96 / 0.96, 96 1.00 / 1.00; e4m3
+// d = 32 0.51 / 0.45, 64 0.71 / 0.66, 80 0.63 / 0.52, 96 0.81 / 0.84 (d = 32 and 64 on the scalar
+// kernel's lane groups).  Both split at 1024 tokens below d = 128.
+template <int D, bool FP8> constexpr bool kMhaOnMma = FP8 ? (D == 96) : (D == 64);
 
 template <int D, bool FP8>
 cudaError_t launch_decode_gf(const DecodeArgs &a, int max_splits, int chunk, cudaStream_t stream) {
