@@ -119,11 +119,17 @@ def test_fp8_gqa_decode_full_size(lib, oracle_mod):
     run_fp8_decode(lib, oracle_mod, workloads.PAGED_DECODE_GQA, kv_heads=workloads.PAGED_DECODE_GQA_KV_HEADS)
 
 
-def test_fp8_gqa_decode_ignores_nan_codes_past_the_context(lib, oracle_mod):
+# every decode form: grouped-query tensor-core kernel, multi-head lane groups (d = 32, 64), the split
+# dim layout (d = 80), a token per warp (d = 128), multi-head on the tensor-core kernel (d = 96)
+NAN_TAIL_FORMS = [(128, 16, 4), (32, 4, 4), (64, 4, 4), (80, 4, 4), (128, 4, 4), (96, 4, 4), (32, 8, 2)]
+
+
+@pytest.mark.parametrize("d,H,Hkv", NAN_TAIL_FORMS, ids=[f"d{d}-{h}/{k}" for d, h, k in NAN_TAIL_FORMS])
+def test_fp8_decode_ignores_nan_codes_past_the_context(lib, oracle_mod, d, H, Hkv):
     # e4m3 NaN codes (0x7F) in cache slots past each sequence's end must not reach O
-    shape = workloads.DecodeShape("fp8 NaN tail", 3, 16, 128, (1, 700), seed=730)
+    shape = workloads.DecodeShape("fp8 NaN tail", 3, H, d, (1, 700), seed=730 + d + H)
     ctx = [700, 33, 129]
-    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=4)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
     kc = oracle_mod.e4m3_quantize(inp["k_pages"], KV_SCALE)
     vc = oracle_mod.e4m3_quantize(inp["v_pages"], KV_SCALE)
     for b, n in enumerate(ctx):

@@ -173,3 +173,33 @@ def test_append_fp8_head_dim_bit_exact(lib, oracle_mod, d):
     torch.cuda.synchronize()
     assert lib.attn_check_device_status() == 0
     assert torch.equal(kd.cpu(), kp) and torch.equal(vd.cpu(), vp)
+
+
+# every decode form over bf16 pages: multi-head lane groups (d = 32), multi-head on the tensor-core
+# kernel (d = 64), the split dim layout (d = 80, 96), a token per warp (d = 128), grouped-query
+BF16_NAN_TAIL_FORMS = [(32, 4, 4), (64, 4, 4), (80, 4, 4), (96, 4, 4), (128, 4, 4), (128, 8, 2), (32, 8, 2)]
+
+
+@pytest.mark.parametrize("d,H,Hkv", BF16_NAN_TAIL_FORMS, ids=[f"d{d}-{h}/{k}" for d, h, k in BF16_NAN_TAIL_FORMS])
+def test_decode_ignores_nan_past_the_context(lib, oracle_mod, d, H, Hkv):
+    # NaN in the cache slots past each sequence's end (K and V) must not reach O or LSE
+    ctx = [700, 33, 129, 16]
+    shape = workloads.DecodeShape(f"nan tail d{d}", len(ctx), H, d, (1, max(ctx)), seed=740 + d + H)
+    inp = workloads.decode_inputs(shape, ctx_lens=ctx, kv_heads=Hkv)
+    kp, vp = inp["k_pages"].clone(), inp["v_pages"].clone()
+    for b, n in enumerate(ctx):
+        if n % 16:
+            last = int(inp["page_table"][b, n // 16])
+            kp[last, :, n % 16:] = float("nan")
+            vp[last, :, n % 16:] = float("nan")
+    dv = {k: v.cuda() for k, v in inp.items()}
+    if Hkv == H:
+        o, lse = lib.paged_attn_decode(dv["q"], kp.cuda(), vp.cuda(), dv["page_table"], dv["ctx_lens"], shape.scale)
+    else:
+        o, lse = lib.paged_attn_decode_gqa(dv["q"], kp.cuda(), vp.cuda(), dv["page_table"], dv["ctx_lens"],
+                                           shape.scale)
+    torch.cuda.synchronize()
+    assert lib.attn_check_device_status() == 0
+    o_ref, lse_ref = oracle_mod.paged_decode_gqa(inp["q"], kp, vp, inp["page_table"], inp["ctx_lens"], shape.scale)
+    assert np.isfinite(o.float().cpu().numpy()).all()
+    _compare_decode(o, lse, o_ref, lse_ref, shape.name)
