@@ -174,7 +174,8 @@ struct alignas(1024) PrefillSmem {
     __nv_bfloat16 v[kStagesOf<D>][kBNd<D> * kPad<D>];  // kPad/64 boxes each
     uint64_t q_full;
     uint64_t u_full[kStagesOf<D>], u_empty[kStagesOf<D>];
-    uint64_t c_full[kStagesOf<D>];  // e4m3 pages: the unit's codes have landed (u_full: widened)
+    uint64_t c_full[kStagesOf<D>];  // e4m3 pages: the unit's codes have landed
+    uint64_t v_full[kStagesOf<D>];  // e4m3 pages: the unit's V tile is widened (u_full: its K tile)
     uint64_t s_full[kQTilesMax];
     uint64_t p_full[kQTilesMax];
     uint64_t o_done[kQTilesMax];
@@ -379,9 +380,10 @@ __device__ __forceinline__ void widen_in_place(__nv_bfloat16 *tile, int cw, int 
 // NCV converter threads (the warps after the MMA issuer's).
 template <int D> constexpr int kConverters = Occ<D, kPagedE4m3>::kThreads - (Cfg<D>::kMmaWarp + 1) * 32;
 
-// Per ring unit u = {K(u), V(u-1)}: wait for its codes, widen them, fence the writes for the async
-// proxy, and arrive (one lane per warp) on the unit's full barrier, which completes when every
-// converter warp has.
+// Per ring unit u = {K(u), V(u-1)}: wait for its codes; widen V(u-1) first, fence the writes for
+// the async proxy and arrive (one lane per warp) on the unit's V barrier; then K(u) and the unit's
+// full barrier.  Each completes when every converter warp has arrived (unit 0 has no V and the
+// last unit no K: the arrivals keep the barriers' phases in step).
 template <int D>
 __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, WaitCtx wc) {
     constexpr int kCW = kConverters<D> / 32;
@@ -389,9 +391,12 @@ __device__ void run_convert(PrefillSmem<D, kPagedE4m3> &sm, int n_all, int ct, W
     for (int u = 0; u <= n_all; ++u) {
         const int slot = u % kStagesOf<D>, use = u / kStagesOf<D>;
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.c_full[slot], (uint32_t)(use & 1), wc, 5))) break;
-        if (u < n_all) widen_in_place<D, kCW>(sm.k[slot], cw, lane);
         if (u > 0) widen_in_place<D, kCW>(sm.v[slot], cw, lane);
         fence_proxy_async_smem();  // this thread's tile writes, before the MMA's reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.v_full[slot]);
+        if (u < n_all) widen_in_place<D, kCW>(sm.k[slot], cw, lane);
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.u_full[slot]);
     }
@@ -452,8 +457,12 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
         tc_commit(&sm.u_empty[0]);
         for (int j = 0; j < n_all && ok; ++j) {
             const int u = j + 1;  // unit with V(j) and K(j+1)
-            ok = mbar_wait(&sm.u_full[u % kStagesOf<D>], (uint32_t)((u / kStagesOf<D>) & 1), wc, 13);
+            const uint32_t ph = (uint32_t)((u / kStagesOf<D>) & 1);
+            // e4m3 pages: V(j) is widened before K(j+1) and signalled on its own barrier, so the
+            // first PV can start while the converters still widen the keys
+            ok = mbar_wait(M == kPagedE4m3 ? &sm.v_full[u % kStagesOf<D>] : &sm.u_full[u % kStagesOf<D>], ph, wc, 13);
             if (!ok) break;
+            bool k_ready = (M != kPagedE4m3);
             // P over S: PV_t(j) must be issued before S_t(j+1) overwrites its buffer
             for (int t = 0; t < Cfg<D>::QT; ++t) {
                 if (j < n[t]) {
@@ -462,7 +471,13 @@ __device__ void run_mma(PrefillSmem<D, M> &sm, uint32_t tmem, const int (&n)[kQT
                     issue_PV(t, j);
                     if (j == n[t] - 1) tc_commit(&sm.o_done[t]);
                 }
-                if (j + 1 < n[t]) issue_S(t, j + 1);
+                if (j + 1 < n[t]) {
+                    if (!k_ready) {
+                        if (!(ok = mbar_wait(&sm.u_full[u % kStagesOf<D>], ph, wc, 15))) break;
+                        k_ready = true;
+                    }
+                    issue_S(t, j + 1);
+                }
             }
             if (!ok) break;
             tc_commit(&sm.u_empty[u % kStagesOf<D>]);
@@ -823,6 +838,7 @@ __global__ void __launch_bounds__((Occ<D, M>::kThreads), (Occ<D, M>::kMinBlocks)
             mbar_init(&sm.u_full[s], M == kPagedE4m3 ? kConverters<D> / 32 : 1);
             mbar_init(&sm.u_empty[s], 1);
             mbar_init(&sm.c_full[s], 1);
+            mbar_init(&sm.v_full[s], M == kPagedE4m3 ? kConverters<D> / 32 : 1);
         }
         for (int t = 0; t < Cfg<D>::QT; ++t) {
             mbar_init(&sm.s_full[t], 1);
