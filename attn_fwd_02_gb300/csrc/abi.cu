@@ -228,7 +228,7 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
     // q, k, v, dq and the sizes get the forward's checks (dq in the place of o)
     int st = prefill_checks(q, k, v, dq, nullptr, B, Hq, Hkv, Nq, Nkv, d, causal, scale, kv_lens);
     if (st != ATTN_OK) return st;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (d != 32 && d != 64 && d != 80 && d != 96 && d != 128) return ATTN_ERR_UNSUPPORTED;
     const uint64_t kv_ctas = ((uint64_t)Nkv + 127) / 128 * (uint64_t)B * (uint64_t)Hkv;
     if (kv_ctas > (1ull << 31) - 1) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse))

@@ -7,7 +7,7 @@
 // (s = scale q.k), dP = dO V^T and dS = P * (dP - D):
 //     dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
 //
-// GB300 mapping of the two tile kernels (d = 64 or 128):
+// GB300 mapping of the two tile kernels (d in {32, 64, 80, 96, 128}):
 //   * One CTA owns a 128-row tile of what it accumulates (dK and dV of 128 keys, or dQ of 128
 //     queries) in TMEM, and streams the other side's 128-row tiles through a 2-slot TMA ring
 //     (128-byte swizzled boxes of 128 rows x 64 columns).
@@ -43,6 +43,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
+// Tiles are padded to 64 (d <= 64) or 128 columns of 64-column TMA boxes, which read zeros past d:
+// the score products run over d/16 k-steps and the accumulations over N = d columns, so the padding
+// costs shared memory only.  Accumulators in TMEM sit at padded column offsets.
+template <int D> constexpr int kBPad = D <= 64 ? 64 : 128;
+template <int D> constexpr int kBBoxes = kBPad<D> / 64;
+// dQ columns of the first warpgroup (the second takes the rest): halves in multiples of 16
+template <int D> constexpr int kDqSplit = ((D / 16 + 1) / 2) * 16;
 
 struct BwdParams {
     const float *lse, *dterm;
@@ -100,10 +107,11 @@ __device__ __forceinline__ void load64(uint32_t taddr, uint32_t (&x)[2][32]) {
     tmem_wait_ld(x[1]);
 }
 
-// Writes 128 rows x d of an fp32 TMEM accumulator (columns c0 .. c0+ncols-1) times `mul` as
-// bf16 to dst + row * D (the thread's row; `store` false skips the write).  Zeros if !have.
-template <int D, int NCOLS>
+// Writes NCOLS (a multiple of 16) columns of this thread's row of an fp32 TMEM accumulator,
+// times `mul`, as bf16 to dst (`store` false skips the write).  Zeros if !have.
+template <int NCOLS>
 __device__ __forceinline__ void store_rows(uint32_t tacc, bool have, bool store, float mul, __nv_bfloat16 *dst) {
+    static_assert(NCOLS % 16 == 0, "16-column steps");
 #pragma unroll
     for (int cc = 0; cc < NCOLS / 32; ++cc) {
         uint32_t v[32];
@@ -121,19 +129,38 @@ __device__ __forceinline__ void store_rows(uint32_t tacc, bool have, bool store,
             for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
     }
+    if constexpr (NCOLS % 32 != 0) {  // the last 16 columns
+        constexpr int c0 = NCOLS / 32 * 32;
+        uint32_t v[16];
+        if (have) {
+            tmem_ld16(tacc + c0, v);
+            tmem_wait_ld16(v);
+        }
+        if (store) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                pk[i] = have ? pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul) : 0u;
+            uint4 *o = reinterpret_cast<uint4 *>(dst + c0);
+            o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    }
 }
 
 // ================================================================== row term D = rowsum(dO * O)
-// D / 8 threads per row, one 16-byte load of O and of dO each, then a shuffle reduction.
+// kTpr threads per row (d / 8 rounded up to a power of two), one 16-byte load of O and of dO each
+// for the threads whose 8 columns lie inside d, then a shuffle reduction.
+template <int D> constexpr int kRowThreads = D / 8 <= 4 ? 4 : (D / 8 <= 8 ? 8 : 16);
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16 *o, const __nv_bfloat16 *dout,
                                                          float *dterm, long long rows) {
-    constexpr int kTpr = D / 8;
+    constexpr int kTpr = kRowThreads<D>;
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long row = gid / kTpr;
     const int part = (int)(gid % kTpr);
     float acc = 0.f;
-    if (row < rows) {
+    if (row < rows && part * 8 < D) {
         const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
         const uint4 b = *reinterpret_cast<const uint4 *>(dout + row * D + part * 8);
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -153,10 +180,10 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16 *o,
 // ================================================================== dK / dV
 template <int D>
 struct alignas(1024) DkvSmem {
-    __nv_bfloat16 k[kT * D];              // the CTA's 128 keys (D/64 boxes)
-    __nv_bfloat16 v[kT * D];
-    __nv_bfloat16 q[kStages][kT * D];     // streamed query tiles
-    __nv_bfloat16 dout[kStages][kT * D];  // and their upstream gradients
+    __nv_bfloat16 k[kT * kBPad<D>];              // the CTA's 128 keys (kBBoxes boxes)
+    __nv_bfloat16 v[kT * kBPad<D>];
+    __nv_bfloat16 q[kStages][kT * kBPad<D>];     // streamed query tiles
+    __nv_bfloat16 dout[kStages][kT * kBPad<D>];  // and their upstream gradients
     float nlse2[kStages][kT];             // minus the log2-domain LSE of each streamed query (0 past Nq)
     float dterm[kStages][kT];             // row term D of each streamed query (0 past Nq)
     uint64_t kv_full;
@@ -186,7 +213,7 @@ template <int D>
 __device__ void dkdv_producer(DkvSmem<D> &sm, const BwdParams &p, const CUtensorMap *tmQ, const CUtensorMap *tmdO,
                               const CUtensorMap *tmK, const CUtensorMap *tmV, int b, int hkv, int bh_kv, int k0,
                               int qi_start, int nqt, int n, WaitCtx wc) {
-    constexpr int kBoxes = D / 64;
+    constexpr int kBoxes = kBBoxes<D>;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         prefetch_tensormap(tmQ);
@@ -250,7 +277,7 @@ __device__ void dkdv_producer(DkvSmem<D> &sm, const BwdParams &p, const CUtensor
 
 template <int D>
 __device__ void dkdv_mma(DkvSmem<D> &sm, uint32_t tmem, int n, WaitCtx wc) {
-    const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+    const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + kBPad<D>;
     bool ok = mbar_wait(&sm.kv_full, 0, wc, 63) && mbar_wait(&sm.u_full[0], 0, wc, 64);
     if (ok) {
         tc_fence_after_sync();
@@ -396,7 +423,7 @@ __device__ void dkdv_compute(DkvSmem<D> &sm, const BwdParams &p, uint32_t tmem, 
     // warpgroup 0 writes dV, warpgroup 1 writes dK (times scale); rows past Nkv are not stored
     const bool store = key < p.Nkv;
     __nv_bfloat16 *dst = (w == 0 ? p.dv : p.dk) + ((size_t)bh_kv * p.Nkv + (store ? key : 0)) * D;
-    store_rows<D, D>(lane_base + 256u + (uint32_t)(w * D), n > 0, store, w == 0 ? 1.f : p.scale, dst);
+    store_rows<D>(lane_base + 256u + (uint32_t)(w * kBPad<D>), n > 0, store, w == 0 ? 1.f : p.scale, dst);
 }
 
 template <int D>
@@ -463,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ================================================================== dQ
 template <int D>
 struct alignas(1024) DqSmem {
-    __nv_bfloat16 q[kT * D];  // the CTA's 128 queries
-    __nv_bfloat16 dout[kT * D];
-    __nv_bfloat16 k[kStages][kT * D];  // streamed key tiles
-    __nv_bfloat16 v[kStages][kT * D];
+    __nv_bfloat16 q[kT * kBPad<D>];  // the CTA's 128 queries
+    __nv_bfloat16 dout[kT * kBPad<D>];
+    __nv_bfloat16 k[kStages][kT * kBPad<D>];  // streamed key tiles
+    __nv_bfloat16 v[kStages][kT * kBPad<D>];
     uint64_t qd_full;
     uint64_t u_full[kStages], u_empty[kStages];
     uint64_t s_full, s_free, dp_full, ds_full, acc_done, drain;
@@ -477,7 +504,7 @@ struct alignas(1024) DqSmem {
 template <int D>
 __device__ void dq_producer(DqSmem<D> &sm, const CUtensorMap *tmQ, const CUtensorMap *tmdO, const CUtensorMap *tmK,
                             const CUtensorMap *tmV, int bh, int bh_kv, int q0, int n, WaitCtx wc) {
-    constexpr int kBoxes = D / 64;
+    constexpr int kBoxes = kBBoxes<D>;
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
     mbar_arrive_expect_tx(&sm.qd_full, 2 * kBoxes * kBoxBytes);
@@ -618,9 +645,10 @@ __device__ void dq_compute(DqSmem<D> &sm, const BwdParams &p, uint32_t tmem, int
         else tc_fence_after_sync();
     }
     if (!ok) return;
-    // warpgroup w writes columns w*D/2 .. (w+1)*D/2 - 1 of dQ (times scale)
-    __nv_bfloat16 *dst = p.dq + ((size_t)bh * p.Nq + (row_ok ? row : 0)) * D + w * (D / 2);
-    store_rows<D, D / 2>(lane_base + 256u + (uint32_t)(w * (D / 2)), n > 0, row_ok, p.scale, dst);
+    // warpgroup 0 writes columns 0 .. kDqSplit - 1 of dQ, warpgroup 1 the rest (times scale)
+    __nv_bfloat16 *dst = p.dq + ((size_t)bh * p.Nq + (row_ok ? row : 0)) * D + (w ? kDqSplit<D> : 0);
+    if (w == 0) store_rows<kDqSplit<D>>(lane_base + 256u, n > 0, row_ok, p.scale, dst);
+    else store_rows<D - kDqSplit<D>>(lane_base + 256u + (uint32_t)kDqSplit<D>, n > 0, row_ok, p.scale, dst);
 }
 
 template <int D>
@@ -696,7 +724,7 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
     const long long rows = (long long)a.B * a.Hq * a.Nq;
     {
-        const long long threads = rows * (D / 8);
+        const long long threads = rows * kRowThreads<D>;
         const unsigned grid = (unsigned)((threads + 255) / 256);
         bwd_rowdot_kernel<D><<<grid, 256, 0, stream>>>(reinterpret_cast<const __nv_bfloat16 *>(a.o),
                                                        reinterpret_cast<const __nv_bfloat16 *>(a.dout), a.dterm, rows);
@@ -758,8 +786,14 @@ cudaError_t launch_bwd_d(const BwdArgs &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
-    if (a.d == 128) return launch_bwd_d<128>(a, stream);
-    return launch_bwd_d<64>(a, stream);
+    switch (a.d) {
+        case 32: return launch_bwd_d<32>(a, stream);
+        case 64: return launch_bwd_d<64>(a, stream);
+        case 80: return launch_bwd_d<80>(a, stream);
+        case 96: return launch_bwd_d<96>(a, stream);
+        case 128: return launch_bwd_d<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 size_t bwd_workspace_bytes(int B, int Hq, int Nq) {

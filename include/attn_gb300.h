@@ -61,8 +61,8 @@
  *     page-locking of the library's static page of host flags (once per process)
  *     and one small synchronous copy into the status word.  Make that first call
  *     before any stream capture.
- *   - Supported: head dim d in {32, 64, 80, 96, 128} for the prefill, decode
- *     and KV-cache entry points, {64, 128} for the backward; page_size 16.
+ *   - Supported: head dim d in {32, 64, 80, 96, 128} for every entry point
+ *     (prefill, decode, KV cache, backward); page_size 16.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -289,7 +289,7 @@ int paged_kv_append_fp8(const void *k_new, const void *v_new, void *k_pages, voi
  *       bytes, 16-byte aligned; it holds D [B, Hq, Nq] fp32 when the call ends.
  * dq, dk and dv are fully written (rows past a sequence's key length get zero
  * dk/dv).  Products run on bf16 operands with fp32 accumulation: P and dS are
- * rounded to bf16 before they multiply dO, Q and K.  d in {64, 128}.
+ * rounded to bf16 before they multiply dO, Q and K.  d in {32, 64, 80, 96, 128}.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
 

@@ -139,8 +139,8 @@ def test_backward_argument_checks(lib):
     assert call_bwd(lib, Hkv=3) == 1
     assert call_bwd(lib, causal=5) == 1
     assert call_bwd(lib, scale=float("nan")) == 1
-    assert call_bwd(lib, d=96) == 2
     assert call_bwd(lib, d=48) == 2
+    assert call_bwd(lib, d=112) == 2
     for name in ("q", "o", "do", "dq", "dk", "dv"):
         assert call_bwd(lib, **{name: ALIGNED + 8}) == 3, name
     assert call_bwd(lib, lse=ALIGNED + 2) == 3

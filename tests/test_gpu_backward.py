@@ -51,6 +51,13 @@ CASES = [
     (3, 2, 2, 140, 140, 128, False, [0, 140, 77]),  # a sequence with no keys at all
     (1, 4, 4, 1024, 1024, 128, True, None),         # several tiles each way
     (1, 8, 1, 384, 384, 64, True, None),            # multi-query
+    # head dims 32, 80, 96: tiles padded to 64 / 128 columns, dQ split 16 / 16, 48 / 32, 48 / 48
+    (1, 2, 2, 300, 300, 32, True, None),
+    (2, 4, 2, 200, 333, 80, True, [333, 150]),
+    (1, 2, 2, 260, 260, 96, False, None),
+    (2, 3, 3, 384, 384, 80, True, None),
+    (1, 4, 1, 256, 256, 32, False, [200]),
+    (1, 2, 2, 140, 140, 96, True, [0]),
 ]
 
 
@@ -88,7 +95,7 @@ def test_backward_matches_oracle(oracle_mod, case):
         assert torch.all(dq[:, :, :Nq - Nkv] == 0)
 
 
-@pytest.mark.parametrize("d,causal", [(64, True), (128, True), (128, False)])
+@pytest.mark.parametrize("d,causal", [(64, True), (128, True), (128, False), (32, True), (80, True), (96, False)])
 def test_forward_then_backward_matches_oracle(oracle_mod, d, causal):
     import attn_fwd_02_gb300 as A
     B, H, N = 2, 4, 520
