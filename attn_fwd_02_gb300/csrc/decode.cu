@@ -24,7 +24,6 @@
 // e4m3 * scale; the FP8 e4m3 storage on the NanoInfer README's roadmap), which halves the
 // bytes a decode step reads.  The key scale folds into the query's score scale and the value
 // scale into the partial O, so the inner loops only widen codes to fp32.
-#include <cuda_fp8.h>
 
 #include <mutex>
 

@@ -33,7 +33,6 @@
 // Every tcgen05 op of the MMA thread completes in issue order, so the commit
 // that signals S_t(j) also tells warpgroup t that PV_t(j-1) has finished with
 // O_t and with the P_t columns.
-#include <cuda_fp8.h>
 
 #include <cmath>
 
