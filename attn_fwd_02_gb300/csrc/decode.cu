@@ -23,7 +23,8 @@
 // The cache holds bf16 values, or FP8 E4M3 codes with one scale per tensor (value =
 // e4m3 * scale; the FP8 e4m3 storage on the NanoInfer README's roadmap), which halves the
 // bytes a decode step reads.  The key scale folds into the query's score scale and the value
-// scale into the partial O, so the inner loops only widen codes to fp32.
+// scale into the partial O, so the inner loops only widen codes (to fp32 in the scalar kernel, to
+// f16 in the tensor-core one).
 
 #include <mutex>
 
