@@ -91,6 +91,9 @@ PAGED_PREFILL = DecodeShape("chunked prefill B8 Hq32 Hkv8 d128 Nq1024 ctx U[1024
                             8, 32, 128, (1024, 8192), 16, seed=1008)
 PAGED_PREFILL_KV_HEADS = 8
 PAGED_PREFILL_NQ = 1024
+# The same chunked prefill at the other head dims (same seed: the same context lengths and table).
+PAGED_PREFILL_BY_DIM = {d: DecodeShape(f"chunked prefill B8 Hq32 Hkv8 d{d} Nq1024 ctx U[1024,8192] page16",
+                                       8, 32, d, (1024, 8192), 16, seed=1008) for d in (32, 64, 80, 96)}
 
 # The paged decode at the other head dims the Kernel-Inference-Engine README instantiates (same
 # seed, so the same context lengths and page table as the d = 128 workload).

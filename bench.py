@@ -583,7 +583,7 @@ def gpu_arm(args):
             dec = DecodeCase(shape, torch, A)
         pre = None
         parts = [dec]
-    elif args.workload in ("prefill_paged", "prefill_paged_fp8"):
+    elif args.workload.startswith("prefill_paged"):
         return paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind)
     elif args.workload == "backward":
         return backward_arm(args, torch, A, rank, world, peaks, peak_kind)
@@ -731,10 +731,19 @@ def small_prefill_lines(args, torch, A, rank, world, peaks, peak_kind):
             "gpu_launches": len(cases) * args.steps}
 
 
+def paged_prefill_shape(workload: str):
+    """prefill_paged[_dNN][_fp8] -> the chunked-prefill shape (d = 128 unless _dNN)."""
+    rest = workload[len("prefill_paged"):]
+    if rest.startswith("_d"):
+        return workloads.PAGED_PREFILL_BY_DIM[int(rest[2:].split("_")[0])]
+    return workloads.PAGED_PREFILL
+
+
 def paged_prefill_arm(args, torch, A, rank, world, peaks, peak_kind):
     """Chunked prefill over the paged cache, timed alone (not part of the default step)."""
-    cls = PagedPrefillFp8Case if args.workload == "prefill_paged_fp8" else PagedPrefillCase
-    case = cls(workloads.PAGED_PREFILL, workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ, torch, A)
+    cls = PagedPrefillFp8Case if args.workload.endswith("_fp8") else PagedPrefillCase
+    case = cls(paged_prefill_shape(args.workload), workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ, torch,
+               A)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -835,6 +844,58 @@ def time_oracle_decode(oracle, dshape, inp, steps, max_calls=10):
     return times
 
 
+def reference_sampled_calls(oracle, args):
+    """The oracle on the chunked prefill or the backward, one bounded call per step: for the chunked
+    prefill one sequence's query-head group (query heads 0 .. group-1 over cache head 0) of the
+    workload, over the same cache (e4m3 codes from the oracle's own quantiser for the _fp8 forms); for
+    the backward one head of the long-context workload.  Returns (TFLOP/s, unit, sample, config, ms)."""
+    import torch
+    steps = []
+    if args.workload == "backward":
+        s = workloads.LONG_CAUSAL
+        inp = workloads.prefill_inputs(s)
+        do = workloads.backward_upstream(s)
+        for i in range(args.warmup + args.steps):
+            b, h = i % s.B, (i // s.B) % s.H
+            sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+            t0 = time.perf_counter()
+            oracle.attn_bwd_gqa(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(do), s.causal, s.scale)
+            if i >= args.warmup:
+                steps.append((metrics.backward_flops(1, 1, s.Nq, s.Nkv, s.d, s.causal), time.perf_counter() - t0))
+        sample = f"one (sequence, head) of the backward of {s.name} per step (fp64 C, OpenMP)"
+        cfgname = "backward of " + s.name
+    else:
+        s = paged_prefill_shape(args.workload)
+        fp8 = args.workload.endswith("_fp8")
+        hkv, nq = workloads.PAGED_PREFILL_KV_HEADS, workloads.PAGED_PREFILL_NQ
+        group = s.H // hkv
+        inp = workloads.decode_inputs(s, kv_heads=hkv)
+        q = torch.randn(s.B, s.H, nq, s.d, generator=torch.Generator().manual_seed(s.seed + 1)).to(torch.bfloat16)
+        kp, vp = inp["k_pages"][:, 0:1].contiguous(), inp["v_pages"][:, 0:1].contiguous()
+        scale8 = PagedPrefillFp8Case.SCALE
+        if fp8:
+            kp, vp = oracle.e4m3_quantize(kp, scale8), oracle.e4m3_quantize(vp, scale8)
+        ctx = [int(x) for x in inp["ctx_lens"]]
+        for i in range(args.warmup + args.steps):
+            b = i % s.B
+            args_b = (q[b:b + 1, 0:group].contiguous(), kp, vp, inp["page_table"][b:b + 1].contiguous(),
+                      inp["ctx_lens"][b:b + 1].contiguous())
+            t0 = time.perf_counter()
+            if fp8:
+                oracle.paged_prefill_fp8_gqa(args_b[0], args_b[1], args_b[2], scale8, scale8, args_b[3], args_b[4],
+                                             True, s.scale)
+            else:
+                oracle.paged_prefill_gqa(*args_b, True, s.scale)
+            if i >= args.warmup:
+                steps.append((metrics.paged_prefill_flops(group, nq, s.d, [ctx[b]], causal=True),
+                              time.perf_counter() - t0))
+        sample = (f"one sequence's query-head group ({group} query heads over one cache head) of {s.name}"
+                  f"{' (e4m3 cache)' if fp8 else ''} per step (fp64 C, OpenMP)")
+        cfgname = s.name + (" (e4m3 cache)" if fp8 else "")
+    rate = sum(f for f, _ in steps) / sum(t for _, t in steps) / 1e12
+    return rate, "TFLOP/s", sample, cfgname, statistics.mean(t for _, t in steps) * 1e3
+
+
 def reference_arm(args):
     """The oracle, as it stands, on the host cores: same metric, unit and config."""
     rank = int(os.environ.get("RANK", "0"))
@@ -847,7 +908,9 @@ def reference_arm(args):
     # about a minute of oracle work in all: each step is a seeded sample of query rows (at least one
     # block of 64) sized to its share of the minute
     budget = min(10.0, 60.0 / max(1, args.steps + args.warmup))
-    if shape is None:  # decode only: the decode workload the GPU arm would time (its bf16 cache)
+    if args.workload.startswith("prefill_paged") or args.workload == "backward":
+        val, unit, sample, cfgname, ms = reference_sampled_calls(oracle, args)
+    elif shape is None:  # decode only: the decode workload the GPU arm would time (its bf16 cache)
         dshape = workloads.PAGED_DECODE
         if args.workload.startswith("decode_d"):
             dshape = workloads.PAGED_DECODE_BY_DIM[int(args.workload[len("decode_d"):].split("_")[0])]
@@ -912,7 +975,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["default", "decode", "decode_small", "decode_gqa", "decode_fp8", "decode_gqa_fp8",
                                            *[f"decode_d{d}{s}" for d in (32, 64, 80, 96) for s in ("", "_fp8")],
-                                           "prefill_paged", "prefill_paged_fp8", "backward",
+                                           "prefill_paged", "prefill_paged_fp8",
+                                           *[f"prefill_paged_d{d}{s}" for d in (32, 64, 80, 96) for s in ("", "_fp8")],
+                                           "backward",
                                            *PREFILL_BY_NAME], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
