@@ -18,7 +18,7 @@
 //              max, and keeps a reference max that only moves when the new max
 //              exceeds it by more than 2^8 (O and l always share the reference,
 //              so the final O / l is unchanged; only then is O rescaled in TMEM).
-//              P = 2^(x - m) is rounded to bf16 and written back into TMEM over
+//              P = 2^(x - m) is rounded to bf16 (f16 over an e4m3 cache) and written back into TMEM over
 //              the scores it came from, where the PV product reads it as its A
 //              operand.  The same warps run the epilogue.
 //   warp 8     TMA producer: Q0, Q1 once, then K and V tiles through a 2-slot ring
@@ -28,6 +28,8 @@
 //              of S_t as packed bf16 pairs) | O0 | O1 (d columns each).
 //   warps 10-11 idle: the third warpgroup hands its registers to the softmax
 //              warpgroups (setmaxnreg), so a thread holds its whole 128-score row.
+//              Over an e4m3 cache they and a fourth warpgroup (warps 12-15) widen the
+//              codes, which the producer loads into the ring slots (run_convert).
 // Issue order per K/V tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1) -- while one
 // warpgroup turns S_t(j+1) into P, the tensor core works for the other.
 // Every tcgen05 op of the MMA thread completes in issue order, so the commit
