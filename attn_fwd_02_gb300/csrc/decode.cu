@@ -14,7 +14,10 @@
 // tens of KB of page data in flight.  A warp keeps an online-softmax state
 // (running max m, normaliser l, unnormalised O) in the log2 domain; the four
 // warp states merge in shared memory and the CTA writes its partial (m, l, O)
-// to the workspace.
+// to the workspace.  Grouped-query heads (and multi-head attention at the head dims where it
+// measured faster) run pass 1 on the tensor cores instead (decode_gqa_mma_kernel): the group's
+// query heads are the M rows of mma.sync products over each page, whose K/V blocks arrive by TMA in
+// swizzled boxes.
 //
 // Pass 2 (decode_combine_kernel): per (sequence, head), the partials of all
 // chunks merge with weights 2^(m_s - M):  L = sum l_s 2^(m_s-M),
