@@ -270,24 +270,53 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
     return x + __shfl_xor_sync(0xffffffffu, x, 1);
 }
 
-// Multi-head decode at d = 32 and 64 splits the warp into groups of T = d / 4 lanes, each lane
-// holding 4 consecutive dims of one token, and the 32 / T groups take different tokens of a page in
-// each round.  A score then needs a sum over T lanes only (3 or 4 shuffles instead of a 16-token
+// Multi-head decode at d = 32 and 64 splits the warp into groups of T = d / 8 lanes, each lane
+// holding 8 consecutive dims of one token, and the 32 / T groups take different tokens of a page in
+// each round.  A score then needs a sum over T lanes only (2 or 3 shuffles instead of a 16-token
 // reduce-scatter), and each group keeps its own tokens' probabilities for O += P V (no per-token
 // broadcasts); the groups' partial O are summed once per CTA.  At d = 128 a token fills the warp.
+// Measured, fraction of HBM with 4 / 8 dims per lane: bf16 d = 32 0.89 / 0.90; e4m3 d = 32
+// 0.515 / 0.550, d = 64 0.71 / 0.79.
 template <int D> constexpr bool kLaneGroups = (D == 32 || D == 64);
+// dims per lane in the lane groups (4 or 8)
+template <int D, bool FP8> constexpr int kGroupDims = 8;
 
-// Four consecutive elements of a cache row (bf16, or e4m3 codes) as fp32.
-template <bool FP8>
-__device__ __forceinline__ void load4(const uint8_t *p, float (&f)[4]) {
+// N (4 or 8) consecutive elements of a cache row (bf16, or e4m3 codes) as fp32.
+template <bool FP8, int N>
+__device__ __forceinline__ void load_n(const uint8_t *p, float (&f)[N]) {
+    static_assert(N == 4 || N == 8, "4 or 8 elements");
     if constexpr (FP8) {
-        e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(p), f);
+        if constexpr (N == 4) {
+            e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(p), f);
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            float a[4], b[4];
+            e4m3x4_to_float4(u.x, a);
+            e4m3x4_to_float4(u.y, b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                f[i] = a[i];
+                f[4 + i] = b[i];
+            }
+        }
     } else {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p);
-        f[0] = __uint_as_float(u.x << 16);
-        f[1] = __uint_as_float(u.x & 0xffff0000u);
-        f[2] = __uint_as_float(u.y << 16);
-        f[3] = __uint_as_float(u.y & 0xffff0000u);
+        uint32_t w[N / 2];
+        if constexpr (N == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            w[0] = u.x;
+            w[1] = u.y;
+        } else {
+            const uint4 u = *reinterpret_cast<const uint4 *>(p);
+            w[0] = u.x;
+            w[1] = u.y;
+            w[2] = u.z;
+            w[3] = u.w;
+        }
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
     }
 }
 
@@ -370,15 +399,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
     }
     // lane groups (d = 32, 64): this lane's token group and its dims 4 cq .. 4 cq + 3
-    constexpr int kT = kLaneGroups<D> ? D / 4 : 32;  // lanes per token
-    constexpr int kG = 32 / kT;                      // tokens per round
-    constexpr int kR = kPS / kG;                     // rounds per page
+    constexpr int kGD = kGroupDims<D, FP8>;          // dims per lane
+    constexpr int kT = kLaneGroups<D> ? D / kGD : 32;  // lanes per token
+    constexpr int kG = 32 / kT;                        // tokens per round
+    constexpr int kR = kPS / kG;                       // rounds per page
     const int gq = lane / kT, cq = lane % kT;
-    float q4[4] = {0.f, 0.f, 0.f, 0.f}, o4[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (kLaneGroups<D>) {
-        load4<false>(reinterpret_cast<const uint8_t *>(a.q) + (((size_t)b * a.H + qh0) * D + 4 * cq) * 2, q4);
+    float q4[kGD], o4[kGD];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q4[i] *= c;
+    for (int i = 0; i < kGD; ++i) q4[i] = o4[i] = 0.f;
+    if constexpr (kLaneGroups<D>) {
+        load_n<false, kGD>(reinterpret_cast<const uint8_t *>(a.q) + (((size_t)b * a.H + qh0) * D + kGD * cq) * 2, q4);
+#pragma unroll
+        for (int i = 0; i < kGD; ++i) q4[i] *= c;
     }
 
     int issued = first;
@@ -399,12 +431,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             float x[kR];
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
-                float k4[4];
-                load4<FP8>(Ks + (r * kG + gq) * kRowBytes + 4 * cq * kElem, k4);
+                float k4[kGD];
+                load_n<FP8, kGD>(Ks + (r * kG + gq) * kRowBytes + kGD * cq * kElem, k4);
                 float acc = q4[0] * k4[0];
-                acc = fmaf(q4[1], k4[1], acc);
-                acc = fmaf(q4[2], k4[2], acc);
-                acc = fmaf(q4[3], k4[3], acc);
+#pragma unroll
+                for (int i = 1; i < kGD; ++i) acc = fmaf(q4[i], k4[i], acc);
 #pragma unroll
                 for (int off = 1; off < kT; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
                 x[r] = acc;
@@ -433,12 +464,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
             l_run[0] = l_run[0] * alpha + ps;
             m_run[0] = m_new;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o4[i] *= alpha;
+            for (int i = 0; i < kGD; ++i) o4[i] *= alpha;
             auto pv_round = [&](int r) {
-                float v4[4];
-                load4<FP8>(Vs + (r * kG + gq) * kRowBytes + 4 * cq * kElem, v4);
+                float v4[kGD];
+                load_n<FP8, kGD>(Vs + (r * kG + gq) * kRowBytes + kGD * cq * kElem, v4);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o4[i] = fmaf(pr[r], v4[i], o4[i]);
+                for (int i = 0; i < kGD; ++i) o4[i] = fmaf(pr[r], v4[i], o4[i]);
             };
             // V rows past the context end are never read (they may hold anything)
             if (ntok == kPS) {
@@ -517,7 +548,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
     // merge the four warp states of every query head
     if constexpr (kLaneGroups<D>) {  // the token groups' partial O (they share m_run)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kGD; ++i)
 #pragma unroll
             for (int off = kT; off < 32; off <<= 1) o4[i] += __shfl_xor_sync(0xffffffffu, o4[i], off);
     }
@@ -530,7 +561,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const DecodeA
         if constexpr (kLaneGroups<D>) {
             if (gq == 0) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sm.red_o[warp][g][4 * cq + i] = o4[i];
+                for (int i = 0; i < kGD; ++i) sm.red_o[warp][g][kGD * cq + i] = o4[i];
             }
         } else {
 #pragma unroll
