@@ -275,43 +275,43 @@ __device__ __forceinline__ float reduce_scatter16(const float (&part)[16], int l
 // each round.  A score then needs a sum over T lanes only (2 or 3 shuffles instead of a 16-token
 // reduce-scatter), and each group keeps its own tokens' probabilities for O += P V (no per-token
 // broadcasts); the groups' partial O are summed once per CTA.  At d = 128 a token fills the warp.
-// Measured, fraction of HBM with 4 / 8 dims per lane: bf16 d = 32 0.89 / 0.90; e4m3 d = 32
-// 0.515 / 0.550, d = 64 0.71 / 0.79.
+// Measured, fraction of HBM with 4 / 8 / 16 dims per lane: bf16 d = 32 0.89 / 0.90 / 0.88; e4m3
+// d = 32 0.515 / 0.55 / 0.52, d = 64 0.71 / 0.80 / 0.79.
 template <int D> constexpr bool kLaneGroups = (D == 32 || D == 64);
 // dims per lane in the lane groups (4 or 8)
 template <int D, bool FP8> constexpr int kGroupDims = 8;
 
-// N (4 or 8) consecutive elements of a cache row (bf16, or e4m3 codes) as fp32.
+// N (4, 8 or 16) consecutive elements of a cache row (bf16, or e4m3 codes) as fp32: one 4-, 8- or
+// 16-byte load per 4, 8 or 16 codes, one per 4 or 8 bf16 values.
 template <bool FP8, int N>
 __device__ __forceinline__ void load_n(const uint8_t *p, float (&f)[N]) {
-    static_assert(N == 4 || N == 8, "4 or 8 elements");
-    if constexpr (FP8) {
-        if constexpr (N == 4) {
-            e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(p), f);
-        } else {
-            const uint2 u = *reinterpret_cast<const uint2 *>(p);
-            float a[4], b[4];
-            e4m3x4_to_float4(u.x, a);
-            e4m3x4_to_float4(u.y, b);
+    static_assert(N == 4 || N == 8 || N == 16, "4, 8 or 16 elements");
+    uint32_t w[FP8 ? N / 4 : N / 2];  // the packed elements
+    if constexpr ((FP8 ? N : 2 * N) == 8) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        w[0] = u.x;
+        w[1] = u.y;
+    } else if constexpr ((FP8 ? N : 2 * N) == 4) {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f[i] = a[i];
-                f[4 + i] = b[i];
-            }
+        for (int j = 0; j < (FP8 ? N : 2 * N) / 16; ++j) {
+            const uint4 u = reinterpret_cast<const uint4 *>(p)[j];
+            w[4 * j] = u.x;
+            w[4 * j + 1] = u.y;
+            w[4 * j + 2] = u.z;
+            w[4 * j + 3] = u.w;
+        }
+    }
+    if constexpr (FP8) {
+#pragma unroll
+        for (int j = 0; j < N / 4; ++j) {
+            float a[4];
+            e4m3x4_to_float4(w[j], a);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[4 * j + i] = a[i];
         }
     } else {
-        uint32_t w[N / 2];
-        if constexpr (N == 4) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(p);
-            w[0] = u.x;
-            w[1] = u.y;
-        } else {
-            const uint4 u = *reinterpret_cast<const uint4 *>(p);
-            w[0] = u.x;
-            w[1] = u.y;
-            w[2] = u.z;
-            w[3] = u.w;
-        }
 #pragma unroll
         for (int i = 0; i < N / 2; ++i) {
             f[2 * i] = __uint_as_float(w[i] << 16);
